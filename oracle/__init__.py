@@ -1,0 +1,203 @@
+"""Double-precision CPU oracle for decode-time MFA attention -- TEST INFRASTRUCTURE.
+
+Only the test suite, the package smoke check and the benchmark's CPU-baseline
+leg may import this package.  The CUDA library never calls it, and it shares no
+code with the CUDA library: the arithmetic lives in ``mfa_oracle.c`` (plain C,
+fp64, written from the definitions cited there) and this module only marshals
+numpy arrays through ctypes.
+
+Sources (see ``mfa_oracle.c`` for the full list):
+  * "Step-3 is Large yet Affordable" (paper summary page), section 2 / Table 1:
+    64 query heads share one key head and one value head of dimension 256.
+  * Same page, sections 7 and 8.1: decode attention over the per-sequence KV
+    cache, 8-bit KV at 512 bytes per token per layer.
+  * OCP 8-bit floating point specification, E4M3 format.
+
+Every function here has its pins in ``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mfa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libmfa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+PAGE_SIZE = 64
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mfa_oracle.c`` into ``libmfa_oracle.so`` (gcc, -O2, OpenMP if available)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+            _SRC, "-o", _LIB_PATH + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = f64
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f64.restype = f64
+        lib.oracle_e4m3_from_f32.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_from_f32.restype = ctypes.c_uint8
+        lib.oracle_e4m3_from_f32_array.argtypes = [P, i64, P]
+        lib.oracle_e4m3_from_f32_array.restype = None
+        lib.oracle_e4m3_to_f64_array.argtypes = [P, i64, P]
+        lib.oracle_e4m3_to_f64_array.restype = None
+        lib.oracle_quantize_tokens_e4m3.argtypes = [P, i64, i32, P, P]
+        lib.oracle_quantize_tokens_e4m3.restype = None
+        lib.oracle_mfa_decode_rows.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
+                                               i64, f64, P, P, i64, P, P, i32]
+        lib.oracle_mfa_decode_rows.restype = i32
+        lib.oracle_mfa_decode.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i64,
+                                          f64, P, P, i32]
+        lib.oracle_mfa_decode.restype = i32
+        lib.oracle_kv_append.argtypes = [P, P, i32, P, P, P, P, i32, P, P, i32, i32, i32, i32, i64]
+        lib.oracle_kv_append.restype = i32
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- E4M3 codec
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 codes (uint8) -> exact fp64 values (OCP OFP8 E4M3 definition)."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_to_f64_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """fp32 values -> nearest E4M3 code, ties to even, saturating to +-448."""
+    xa = _c(x, np.float32)
+    out = np.empty(xa.shape, dtype=np.uint8)
+    _load().oracle_e4m3_from_f32_array(_ptr(xa), xa.size, _ptr(out))
+    return out
+
+
+def quantize_tokens_e4m3(x_bf16_bits) -> tuple[np.ndarray, np.ndarray]:
+    """Per-token E4M3 quantisation of bf16 rows [..., d] (given as uint16 bit patterns).
+
+    Returns (codes uint8 [..., d], scales float32 [...]): scale = absmax / 448 in
+    fp32 (1 when the row is all zero), code = E4M3(x / scale)."""
+    x = _c(x_bf16_bits, np.uint16)
+    d = x.shape[-1]
+    n = x.size // d
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1], dtype=np.float32)
+    _load().oracle_quantize_tokens_e4m3(_ptr(x), n, d, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns -> exact fp64 values."""
+    b = _c(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- attention
+def mfa_decode(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_scale=None,
+               v_scale=None, rows=None, threads=None):
+    """MFA decode attention over a paged KV cache, in fp64.
+
+    q_bits     [B, H, D] uint16 (bf16 bits)
+    k_cache    [num_pages, page, D] uint16 (bf16 bits) or uint8 (E4M3 codes)
+    v_cache    same as k_cache
+    page_table [B, max_pages] int32, seq_lens [B] int32
+    k_scale/v_scale [num_pages, page] float32 for an E4M3 cache
+    rows       optional (b_idx, h_idx) int arrays: compute only those rows
+    Returns (out, lse): out [B, H, D] (or [n_rows, D]) fp64, lse [B, H] (or [n_rows]).
+    """
+    q = _c(q_bits, np.uint16)
+    B, H, D = q.shape
+    fp8 = np.asarray(k_cache).dtype == np.uint8
+    kc = _c(k_cache, np.uint8 if fp8 else np.uint16)
+    vc = _c(v_cache, np.uint8 if fp8 else np.uint16)
+    num_pages, page_size = kc.shape[0], kc.shape[1]
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ks = _c(k_scale, np.float32) if fp8 else None
+    vs = _c(v_scale, np.float32) if fp8 else None
+    if fp8 and (ks is None or vs is None):
+        raise ValueError("an E4M3 cache needs k_scale and v_scale")
+    threads = threads or default_threads()
+    lib = _load()
+    if rows is None:
+        out = np.empty((B, H, D), dtype=np.float64)
+        lse = np.empty((B, H), dtype=np.float64)
+        st = lib.oracle_mfa_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), int(fp8),
+                                   _ptr(pt), _ptr(sl), B, H, D, page_size, pt.shape[1], num_pages,
+                                   float(scale), _ptr(out), _ptr(lse), int(threads))
+    else:
+        rb = _c(rows[0], np.int32)
+        rh = _c(rows[1], np.int32)
+        out = np.empty((rb.size, D), dtype=np.float64)
+        lse = np.empty((rb.size,), dtype=np.float64)
+        st = lib.oracle_mfa_decode_rows(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), int(fp8),
+                                        _ptr(pt), _ptr(sl), B, H, D, page_size, pt.shape[1],
+                                        num_pages, float(scale), _ptr(rb), _ptr(rh), rb.size,
+                                        _ptr(out), _ptr(lse), int(threads))
+    if st != 0:
+        raise ValueError(f"oracle rejected the inputs (code {st})")
+    return out, lse
+
+
+def kv_append(k_new_bits, v_new_bits, k_cache, v_cache, page_table, seq_lens, *, k_scale=None,
+              v_scale=None):
+    """Append n_new tokens per sequence to host copies of the cache, in place.
+
+    k_new_bits/v_new_bits: [B, n_new, D] uint16 (bf16 bits).  For an E4M3 cache
+    (uint8 k_cache/v_cache) the tokens are quantised per token; k_scale/v_scale
+    are updated in place.  seq_lens is incremented in place."""
+    kn = _c(k_new_bits, np.uint16)
+    vn = _c(v_new_bits, np.uint16)
+    B, n_new, D = kn.shape
+    fp8 = k_cache.dtype == np.uint8
+    for a in (k_cache, v_cache, page_table, seq_lens) + ((k_scale, v_scale) if fp8 else ()):
+        if not a.flags.c_contiguous:
+            raise ValueError("in-place arrays must be C-contiguous")
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    st = _load().oracle_kv_append(_ptr(kn), _ptr(vn), n_new, _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(k_scale) if fp8 else None, _ptr(v_scale) if fp8 else None,
+                                  int(fp8), _ptr(page_table), _ptr(seq_lens), B, D, page_size,
+                                  page_table.shape[1], num_pages)
+    if st != 0:
+        raise ValueError(f"oracle append rejected the inputs (code {st})")
