@@ -1,0 +1,172 @@
+"""Thin ctypes binding of libmfa (include/mfa.h), same names as the C ABI.
+
+Arguments are marshalled only: a torch tensor becomes its data pointer, a
+stream its CUDA handle.  Every computation runs in the CUDA library; there is
+no CPU or PyTorch fallback, and a missing library raises at the first call.
+A status other than MFA_OK raises MFAError with the library's message.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmfa.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "mfa.h")
+
+MFA_OK = 0
+STATUS_NAMES = {0: "MFA_OK", 1: "MFA_ERR_INVALID_ARG", 2: "MFA_ERR_UNSUPPORTED", 3: "MFA_ERR_CUDA",
+                4: "MFA_ERR_WORKSPACE", 5: "MFA_ERR_DEVICE_PAGE", 6: "MFA_ERR_DEVICE_CAPACITY",
+                7: "MFA_ERR_DEVICE_TIMEOUT"}
+HEADS, HEAD_DIM, PAGE_SIZE, MAX_BATCH = 64, 256, 64, 1024
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MFAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("grid_ctas", ctypes.c_int), ("partial_slots", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+_P, _I, _F, _Z, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+_SIGNATURES = {
+    "mfa_plan_decode": ([_I, _I, _I, ctypes.POINTER(Plan)], _I),
+    "mfa_decode_workspace_bytes": ([_I, _I], _Z),
+    "mfa_workspace_init": ([_P, _Z, _P], _I),
+    "mfa_kv_append": ([_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "mfa_kv_append_fp8": ([_P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "mfa_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_check_device_errors": ([_P, _I, _P], _I),
+    "mfa_set_wait_budget_ns": ([_U64], None),
+    "mfa_selftest_wait_timeout": ([_P, _U64, _P], _I),
+    "mfa_status_string": ([_I], ctypes.c_char_p),
+    "mfa_last_error": ([], ctypes.c_char_p),
+}
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/mfa.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mfa_[a-z0-9_]+)\s*\(", text)))
+
+
+def load():
+    """Load libmfa.so (built by decode_attention_mfa_gb300.build); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmfa.so is not built ({LIB_PATH}); run "
+                               "`python -m decode_attention_mfa_gb300.build` first")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int):
+    if status != MFA_OK:
+        msg = load().mfa_last_error().decode(errors="replace")
+        raise MFAError(status, msg)
+
+
+# ----------------------------------------------------------------- C ABI
+def mfa_plan_decode(batch: int, max_len_hint: int, num_sms: int = 0) -> Plan:
+    plan = Plan()
+    _check(load().mfa_plan_decode(batch, max_len_hint, num_sms, ctypes.byref(plan)))
+    return plan
+
+
+def mfa_decode_workspace_bytes(batch: int, max_len_hint: int) -> int:
+    n = load().mfa_decode_workspace_bytes(batch, max_len_hint)
+    if n == 0:
+        _check(load().mfa_plan_decode(batch, max_len_hint, 0, ctypes.byref(Plan())))
+    return int(n)
+
+
+def mfa_workspace_init(workspace, workspace_bytes: int, stream=None):
+    _check(load().mfa_workspace_init(_ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def mfa_kv_append(k_new, v_new, n_new, k_cache, v_cache, page_table, seq_lens, batch, max_pages,
+                  num_pages, workspace, stream=None):
+    _check(load().mfa_kv_append(_ptr(k_new), _ptr(v_new), n_new, _ptr(k_cache), _ptr(v_cache),
+                                _ptr(page_table), _ptr(seq_lens), batch, max_pages, num_pages,
+                                _ptr(workspace), _stream(stream)))
+
+
+def mfa_kv_append_fp8(k_new, v_new, n_new, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                      batch, max_pages, num_pages, workspace, stream=None):
+    _check(load().mfa_kv_append_fp8(_ptr(k_new), _ptr(v_new), n_new, _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_scale), _ptr(v_scale), _ptr(page_table), _ptr(seq_lens),
+                                    batch, max_pages, num_pages, _ptr(workspace), _stream(stream)))
+
+
+def mfa_decode_attention(q, k_cache, v_cache, page_table, seq_lens, out, lse, scale, batch, max_pages,
+                         num_pages, max_len_hint, workspace, workspace_bytes, stream=None):
+    _check(load().mfa_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                       _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch,
+                                       max_pages, num_pages, max_len_hint, _ptr(workspace),
+                                       workspace_bytes, _stream(stream)))
+
+
+def mfa_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse, scale,
+                             batch, max_pages, num_pages, max_len_hint, workspace, workspace_bytes,
+                             stream=None):
+    _check(load().mfa_decode_attention_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                           _ptr(v_scale), _ptr(page_table), _ptr(seq_lens), _ptr(out),
+                                           _ptr(lse), float(scale), batch, max_pages, num_pages,
+                                           max_len_hint, _ptr(workspace), workspace_bytes,
+                                           _stream(stream)))
+
+
+def mfa_check_device_errors(workspace, clear: bool = True, stream=None):
+    _check(load().mfa_check_device_errors(_ptr(workspace), int(clear), _stream(stream)))
+
+
+def mfa_set_wait_budget_ns(budget_ns: int):
+    load().mfa_set_wait_budget_ns(int(budget_ns))
+
+
+def mfa_selftest_wait_timeout(workspace, budget_ns: int, stream=None):
+    _check(load().mfa_selftest_wait_timeout(_ptr(workspace), int(budget_ns), _stream(stream)))
+
+
+def mfa_status_string(status: int) -> str:
+    return load().mfa_status_string(status).decode()
+
+
+def mfa_last_error() -> str:
+    return load().mfa_last_error().decode(errors="replace")

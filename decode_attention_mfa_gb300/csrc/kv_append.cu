@@ -1,0 +1,119 @@
+// kv_append.cu -- in-place KV append into the paged cache (bf16 copy or
+// per-token E4M3 quantisation), advancing the device-owned length counter.
+//
+// Semantics: "DuckLLM decode fixed-cost reduction" page, sections 7.2 (static
+// KV cache written at a fixed slot, never re-materialised) and 7.6 (the append
+// offset and the attention length come from one device-owned counter, and the
+// attention after an append includes the new token). FP8 storage: "Step-3 is
+// Large yet Affordable" (paper summary page), section 7 (8-bit KV, 512 bytes
+// per token per layer); one fp32 scale per token (absmax / 448) because the
+// pages do not fix the granularity.
+#include <cuda_fp8.h>
+
+#include "mfa_device.cuh"
+
+namespace mfa {
+namespace {
+
+constexpr int kAppendThreads = 256;  // 8 warps, one token row (K or V) per warp at a time
+
+// One 512-byte bf16 row: lane i holds elements [8i, 8i + 8).
+__device__ __forceinline__ void copy_row_bf16(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                              int lane) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+  reinterpret_cast<uint4*>(dst)[lane] = v;
+}
+
+// Quantise one bf16 row to E4M3 with scale = absmax / 448 (1 for a zero row).
+// Divisions are IEEE round-to-nearest; the conversion rounds to nearest even
+// and saturates to +-448.
+__device__ __forceinline__ void quantise_row_e4m3(const uint16_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                                  float* __restrict__ scale_out, int lane) {
+  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  uint32_t packed[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float2 pr = make_float2(__fdiv_rn(x[4 * i + 2 * j], s), __fdiv_rn(x[4 * i + 2 * j + 1], s));
+      const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
+      word |= (uint32_t)c2 << (16 * j);
+    }
+    packed[i] = word;
+  }
+  reinterpret_cast<uint2*>(dst)[lane] = make_uint2(packed[0], packed[1]);
+  if (lane == 0) *scale_out = s;
+}
+
+__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendParams p) {
+  __shared__ int s_start;
+  __shared__ int s_bad;
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) {
+    const int start = p.seq_lens[b];
+    const long long cap = (long long)p.max_pages * kPageSize;
+    s_bad = 0;
+    if (start < 0 || (long long)start + p.n_new > cap) {
+      raise_error(p.err, MFA_DEVERR_CAPACITY);
+      s_bad = 1;
+    } else {
+      // validate every page id the new tokens land in before writing anything
+      for (int pg = start / kPageSize; pg <= (start + p.n_new - 1) / kPageSize; ++pg) {
+        const int page = p.page_table[(size_t)b * p.max_pages + pg];
+        if (page < 0 || page >= p.num_pages) {
+          raise_error(p.err, MFA_DEVERR_PAGE);
+          s_bad = 1;
+          break;
+        }
+      }
+    }
+    s_start = start;
+  }
+  __syncthreads();
+  if (s_bad) return;
+  const int start = s_start;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kAppendThreads / 32;
+  // work item i: token t = i / 2, K (even) or V (odd)
+  for (int i = warp; i < 2 * p.n_new; i += kWarps) {
+    const int t = i >> 1;
+    const bool is_v = i & 1;
+    const int pos = start + t;
+    const int page = p.page_table[(size_t)b * p.max_pages + pos / kPageSize];
+    const size_t slot = (size_t)page * kPageSize + (pos % kPageSize);
+    const uint16_t* src = (is_v ? p.v_new : p.k_new) + ((size_t)b * p.n_new + t) * kHeadDim;
+    if (p.fp8) {
+      uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + slot * kHeadDim;
+      float* sc = (is_v ? p.v_scale : p.k_scale) + slot;
+      quantise_row_e4m3(src, dst, sc, lane);
+    } else {
+      uint16_t* dst = static_cast<uint16_t*>(is_v ? p.v_cache : p.k_cache) + slot * kHeadDim;
+      copy_row_bf16(src, dst, lane);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) p.seq_lens[b] = start + p.n_new;
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
+  kv_append_kernel<<<p.B, kAppendThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mfa

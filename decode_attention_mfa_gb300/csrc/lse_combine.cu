@@ -1,0 +1,92 @@
+// lse_combine.cu -- merges the split-KV partial results of each sequence.
+//
+// Each partial s of sequence b holds O_s = attention over its own pages
+// (already normalised) and lse_s = ln of its softmax denominator. With
+// M = max_s lse_s and w_s = exp(lse_s - M):
+//     out = sum_s w_s O_s / sum_s w_s,   lse = M + ln sum_s w_s,
+// which equals attention over the whole sequence (the splits partition the
+// softmax sum exactly). One warp per (sequence, head): lane s reads lse_s,
+// the maximum and the sum go through warp shuffles, and each lane then
+// accumulates 8 of the 256 output dimensions.
+#include "mfa_device.cuh"
+
+namespace mfa {
+namespace {
+
+constexpr int kCombineThreads = 256;  // 8 warps = 8 heads of one sequence
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ bool cta_range_nonempty(int c, long long P, int G) {
+  return cta_page_lo(c, P, G) < cta_page_lo(c + 1, P, G);
+}
+
+__global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodeParams p) {
+  extern __shared__ int smem_i[];
+  int* s_len = smem_i;
+  int* s_prefix = smem_i + p.B;
+  build_page_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, s_len, s_prefix);
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * (kCombineThreads / 32) + warp;
+  const long long P = s_prefix[p.B];
+  const int G = p.grid;
+  const long long sp0 = s_prefix[b], sp1 = s_prefix[b + 1];
+  uint16_t* out = p.out + ((size_t)b * kHeads + h) * kHeadDim;
+  if (sp1 == sp0) {  // empty sequence
+    reinterpret_cast<uint2*>(out)[lane] = make_uint2(0u, 0u);
+    reinterpret_cast<uint2*>(out + 128)[lane] = make_uint2(0u, 0u);
+    if (lane == 0) p.lse[(size_t)b * kHeads + h] = -INFINITY;
+    return;
+  }
+  const int c_first = cta_of_page(sp0, P, G);
+  const int c_last = cta_of_page(sp1 - 1, P, G);
+  // maximum of the partial LSEs
+  float mx = -INFINITY;
+  for (int c = c_first + lane; c <= c_last; c += 32)
+    if (cta_range_nonempty(c, P, G)) mx = fmaxf(mx, __ldcg(p.part_lse + (size_t)(c + b) * kHeads + h));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  float den = 0.0f;
+  for (int base = c_first; base <= c_last; base += 32) {
+    const int c = base + lane;
+    float w = 0.0f;
+    if (c <= c_last && cta_range_nonempty(c, P, G))
+      w = exp2f((__ldcg(p.part_lse + (size_t)(c + b) * kHeads + h) - mx) * kLog2e);
+    den += w;
+    const int n = min(32, c_last - base + 1);
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      if (wj == 0.0f) continue;
+      const float* src = p.part_o + ((size_t)(base + j + b) * kHeads + h) * kHeadDim;
+      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 128) + lane);
+      a0.x += wj * x0.x; a0.y += wj * x0.y; a0.z += wj * x0.z; a0.w += wj * x0.w;
+      a1.x += wj * x1.x; a1.y += wj * x1.y; a1.z += wj * x1.z; a1.w += wj * x1.w;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float inv = 1.0f / den;
+  __nv_bfloat162 r0 = __floats2bfloat162_rn(a0.x * inv, a0.y * inv);
+  __nv_bfloat162 r1 = __floats2bfloat162_rn(a0.z * inv, a0.w * inv);
+  __nv_bfloat162 r2 = __floats2bfloat162_rn(a1.x * inv, a1.y * inv);
+  __nv_bfloat162 r3 = __floats2bfloat162_rn(a1.z * inv, a1.w * inv);
+  reinterpret_cast<uint2*>(out)[lane] =
+      make_uint2(*reinterpret_cast<uint32_t*>(&r0), *reinterpret_cast<uint32_t*>(&r1));
+  reinterpret_cast<uint2*>(out + 128)[lane] =
+      make_uint2(*reinterpret_cast<uint32_t*>(&r2), *reinterpret_cast<uint32_t*>(&r3));
+  if (lane == 0) p.lse[(size_t)b * kHeads + h] = mx + log2f(den) * kLn2;
+}
+
+}  // namespace
+
+cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream) {
+  dim3 grid(kHeads / (kCombineThreads / 32), p.B);
+  const size_t smem = sizeof(int) * (2 * (size_t)p.B + 1);
+  lse_combine_kernel<<<grid, kCombineThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mfa

@@ -1,0 +1,308 @@
+// mfa_api.cu -- host side of the libmfa C ABI: argument checks, split
+// planning and kernel launches. No call here allocates device memory or
+// synchronises, except mfa_check_device_errors.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "mfa_internal.h"
+
+namespace {
+
+using namespace mfa;
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_wait_budget_ns{2000000000ull};
+
+mfa_status_t fail(mfa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+mfa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MFA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------ device info
+struct DeviceInfo {
+  int num_sms = 0;
+  int major = 0, minor = 0;
+  bool valid = false;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mutex;
+
+mfa_status_t current_device(int* dev_out, DeviceInfo* info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MFA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.valid) {
+    if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.valid = true;
+  }
+  if (dev_out) *dev_out = dev;
+  if (info) *info = d;
+  if (!(d.major == 10 && d.minor == 3))
+    return fail(MFA_ERR_UNSUPPORTED, "libmfa is built for sm_103a; device is sm_%d%d", d.major, d.minor);
+  return MFA_OK;
+}
+
+// ------------------------------------------------------------ planning
+// Grid of the split kernel: one CTA per SM, fewer when there is too little
+// work (at least kMinPagesPerCta pages per CTA for the expected lengths).
+constexpr int kMinPagesPerCta = 2;
+
+int plan_grid(int batch, int max_len_hint, int num_sms) {
+  const long long pages = (long long)batch * ((max_len_hint + kPageSize - 1) / kPageSize);
+  long long g = (pages + kMinPagesPerCta - 1) / kMinPagesPerCta;
+  if (g < 1) g = 1;
+  if (g > num_sms) g = num_sms;
+  return (int)g;
+}
+
+void fill_plan(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan) {
+  plan->grid_ctas = plan_grid(batch, max_len_hint, num_sms);
+  plan->partial_slots = plan->grid_ctas + batch - 1;
+  plan->workspace_bytes = kWsHeaderBytes + (size_t)plan->partial_slots * (kPartialOBytes + kPartialLseBytes);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------ common checks
+mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* page_table, const int32_t* seq_lens, const void* out,
+                               const float* lse, int batch, int max_pages, int num_pages,
+                               int max_len_hint, const void* workspace, size_t workspace_bytes,
+                               int num_sms, mfa_plan_t* plan) {
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out || !lse)
+    return fail(MFA_ERR_INVALID_ARG, "null pointer argument");
+  if (batch < 1 || batch > kMaxBatch) return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxBatch);
+  if (max_pages < 1 || num_pages < 1) return fail(MFA_ERR_INVALID_ARG, "max_pages and num_pages must be >= 1");
+  if (max_len_hint < 0) return fail(MFA_ERR_INVALID_ARG, "negative max_len_hint");
+  if ((long long)max_pages * kPageSize > 0x7fffffffLL) return fail(MFA_ERR_INVALID_ARG, "max_pages too large");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4))
+    return fail(MFA_ERR_INVALID_ARG, "misaligned pointer (q, caches, out need 16 bytes)");
+  if (!workspace || !aligned(workspace, 256))
+    return fail(MFA_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
+  fill_plan(batch, max_len_hint, num_sms, plan);
+  if (workspace_bytes < plan->workspace_bytes)
+    return fail(MFA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, plan->workspace_bytes);
+  return MFA_OK;
+}
+
+DecodeParams make_decode_params(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                                const float* v_scale, const int32_t* page_table, const int32_t* seq_lens,
+                                void* out, float* lse, float scale, int batch, int max_pages, int num_pages,
+                                void* workspace, const mfa_plan_t& plan) {
+  DecodeParams p{};
+  char* ws = static_cast<char*>(workspace);
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  p.part_o = reinterpret_cast<float*>(ws + kWsHeaderBytes);
+  p.part_lse = reinterpret_cast<float*>(ws + kWsHeaderBytes + (size_t)plan.partial_slots * kPartialOBytes);
+  p.scale = scale;
+  p.B = batch;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.grid = plan.grid_ctas;
+  p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
+  return p;
+}
+
+mfa_status_t append_common(const void* k_new, const void* v_new, int n_new, void* k_cache, void* v_cache,
+                           float* k_scale, float* v_scale, int fp8, const int32_t* page_table,
+                           int32_t* seq_lens, int batch, int max_pages, int num_pages, void* workspace,
+                           void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !page_table || !seq_lens)
+    return fail(MFA_ERR_INVALID_ARG, "null pointer argument");
+  if (fp8 && (!k_scale || !v_scale)) return fail(MFA_ERR_INVALID_ARG, "null scale pointer");
+  if (fp8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return fail(MFA_ERR_INVALID_ARG, "misaligned scales");
+  if (batch < 1 || batch > kMaxBatch) return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxBatch);
+  if (n_new < 0) return fail(MFA_ERR_INVALID_ARG, "negative n_new");
+  if (max_pages < 1 || num_pages < 1) return fail(MFA_ERR_INVALID_ARG, "max_pages and num_pages must be >= 1");
+  if ((long long)max_pages * kPageSize > 0x7fffffffLL) return fail(MFA_ERR_INVALID_ARG, "max_pages too large");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(page_table, 4) || !aligned(seq_lens, 4))
+    return fail(MFA_ERR_INVALID_ARG, "misaligned pointer (rows and caches need 16 bytes)");
+  if (!workspace || !aligned(workspace, 256))
+    return fail(MFA_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
+  mfa_status_t st = current_device(nullptr, nullptr);
+  if (st != MFA_OK) return st;
+  if (n_new == 0) return MFA_OK;
+  AppendParams p{};
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.err = static_cast<uint32_t*>(workspace);
+  p.n_new = n_new;
+  p.B = batch;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.fp8 = fp8;
+  const cudaError_t e = launch_kv_append(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return MFA_OK;
+}
+
+mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, bool fp8, const int32_t* page_table, const int32_t* seq_lens,
+                           void* out, float* lse, float scale, int batch, int max_pages, int num_pages,
+                           int max_len_hint, void* workspace, size_t workspace_bytes, void* stream) {
+  DeviceInfo info;
+  mfa_status_t st = current_device(nullptr, &info);
+  if (st != MFA_OK) return st;
+  if (fp8 && (!k_scale || !v_scale)) return fail(MFA_ERR_INVALID_ARG, "null scale pointer");
+  if (fp8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return fail(MFA_ERR_INVALID_ARG, "misaligned scales");
+  mfa_plan_t plan;
+  st = check_decode_args(q, k_cache, v_cache, page_table, seq_lens, out, lse, batch, max_pages, num_pages,
+                         max_len_hint, workspace, workspace_bytes, info.num_sms, &plan);
+  if (st != MFA_OK) return st;
+  const DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out,
+                                            lse, scale, batch, max_pages, num_pages, workspace, plan);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_split_simt(p, fp8, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
+  e = launch_lse_combine(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
+  return MFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mfa_status_t mfa_plan_decode(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan) {
+  if (!plan) return fail(MFA_ERR_INVALID_ARG, "null plan");
+  if (batch < 1 || batch > kMaxBatch) return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxBatch);
+  if (max_len_hint < 0) return fail(MFA_ERR_INVALID_ARG, "negative max_len_hint");
+  if (num_sms <= 0) {
+    DeviceInfo info;
+    const mfa_status_t st = current_device(nullptr, &info);
+    if (st != MFA_OK) return st;
+    num_sms = info.num_sms;
+  }
+  fill_plan(batch, max_len_hint, num_sms, plan);
+  return MFA_OK;
+}
+
+size_t mfa_decode_workspace_bytes(int batch, int max_len_hint) {
+  mfa_plan_t plan;
+  if (mfa_plan_decode(batch, max_len_hint, 0, &plan) != MFA_OK) return 0;
+  return plan.workspace_bytes;
+}
+
+mfa_status_t mfa_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256))
+    return fail(MFA_ERR_WORKSPACE, "workspace missing, misaligned or smaller than its header");
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return MFA_OK;
+}
+
+mfa_status_t mfa_kv_append(const void* k_new, const void* v_new, int n_new, void* k_cache, void* v_cache,
+                           const int32_t* page_table, int32_t* seq_lens, int batch, int max_pages, int num_pages,
+                           void* workspace, void* stream) {
+  return append_common(k_new, v_new, n_new, k_cache, v_cache, nullptr, nullptr, 0, page_table, seq_lens, batch,
+                       max_pages, num_pages, workspace, stream);
+}
+
+mfa_status_t mfa_kv_append_fp8(const void* k_new, const void* v_new, int n_new, void* k_cache, void* v_cache,
+                               float* k_scale, float* v_scale, const int32_t* page_table, int32_t* seq_lens,
+                               int batch, int max_pages, int num_pages, void* workspace, void* stream) {
+  return append_common(k_new, v_new, n_new, k_cache, v_cache, k_scale, v_scale, 1, page_table, seq_lens, batch,
+                       max_pages, num_pages, workspace, stream);
+}
+
+mfa_status_t mfa_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
+                                  float scale, int batch, int max_pages, int num_pages, int max_len_hint,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common(q, k_cache, v_cache, nullptr, nullptr, false, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream);
+}
+
+mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale, const int32_t* page_table,
+                                      const int32_t* seq_lens, void* out, float* lse, float scale, int batch,
+                                      int max_pages, int num_pages, int max_len_hint, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream);
+}
+
+mfa_status_t mfa_check_device_errors(void* workspace, int clear, void* stream) {
+  if (!workspace) return fail(MFA_ERR_WORKSPACE, "null workspace");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the error word");
+  if (clear) {
+    e = cudaMemsetAsync(workspace, 0, sizeof word, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+  }
+  if (word & MFA_DEVERR_PAGE) return fail(MFA_ERR_DEVICE_PAGE, "device error word 0x%x", word);
+  if (word & MFA_DEVERR_CAPACITY) return fail(MFA_ERR_DEVICE_CAPACITY, "device error word 0x%x", word);
+  if (word & MFA_DEVERR_TIMEOUT) return fail(MFA_ERR_DEVICE_TIMEOUT, "device error word 0x%x", word);
+  return MFA_OK;
+}
+
+void mfa_set_wait_budget_ns(uint64_t budget_ns) { g_wait_budget_ns.store(budget_ns, std::memory_order_relaxed); }
+
+mfa_status_t mfa_selftest_wait_timeout(void* workspace, uint64_t budget_ns, void* stream) {
+  if (!workspace || !aligned(workspace, 256)) return fail(MFA_ERR_WORKSPACE, "workspace missing or misaligned");
+  const mfa_status_t st = current_device(nullptr, nullptr);
+  if (st != MFA_OK) return st;
+  const cudaError_t e =
+      launch_selftest_wait(static_cast<uint32_t*>(workspace), budget_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  return MFA_OK;
+}
+
+const char* mfa_status_string(mfa_status_t status) {
+  switch (status) {
+    case MFA_OK: return "MFA_OK";
+    case MFA_ERR_INVALID_ARG: return "MFA_ERR_INVALID_ARG";
+    case MFA_ERR_UNSUPPORTED: return "MFA_ERR_UNSUPPORTED";
+    case MFA_ERR_CUDA: return "MFA_ERR_CUDA";
+    case MFA_ERR_WORKSPACE: return "MFA_ERR_WORKSPACE";
+    case MFA_ERR_DEVICE_PAGE: return "MFA_ERR_DEVICE_PAGE";
+    case MFA_ERR_DEVICE_CAPACITY: return "MFA_ERR_DEVICE_CAPACITY";
+    case MFA_ERR_DEVICE_TIMEOUT: return "MFA_ERR_DEVICE_TIMEOUT";
+  }
+  return "MFA_ERR_UNKNOWN";
+}
+
+const char* mfa_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

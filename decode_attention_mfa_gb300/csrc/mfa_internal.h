@@ -1,0 +1,62 @@
+// mfa_internal.h -- constants, kernel parameter blocks and launch entry points
+// shared by the host side (mfa_api.cu) and the kernels of libmfa.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mfa.h"
+
+namespace mfa {
+
+constexpr int kHeads = MFA_HEADS;        // query heads sharing one K and one V head
+constexpr int kHeadDim = MFA_HEAD_DIM;   // head dimension
+constexpr int kPageSize = MFA_PAGE_SIZE; // tokens per cache page
+constexpr int kMaxBatch = MFA_MAX_BATCH;
+
+// Workspace layout: [header 256 B][partial O: slots x 64 x 256 fp32][partial lse: slots x 64 fp32]
+constexpr size_t kWsHeaderBytes = 256;
+constexpr size_t kPartialOBytes = (size_t)kHeads * kHeadDim * sizeof(float);
+constexpr size_t kPartialLseBytes = (size_t)kHeads * sizeof(float);
+
+struct AppendParams {
+  const uint16_t* k_new;  // [B][n_new][256] bf16 bits
+  const uint16_t* v_new;
+  void* k_cache;          // bf16 or E4M3 pages
+  void* v_cache;
+  float* k_scale;         // E4M3 only
+  float* v_scale;
+  const int32_t* page_table;
+  int32_t* seq_lens;
+  uint32_t* err;
+  int n_new, B, max_pages, num_pages;
+  int fp8;
+};
+
+struct DecodeParams {
+  const uint16_t* q;       // [B][64][256] bf16 bits
+  const void* k_cache;     // [num_pages][64][256] bf16 bits or E4M3 codes
+  const void* v_cache;
+  const float* k_scale;    // [num_pages][64] (E4M3 only)
+  const float* v_scale;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  uint16_t* out;           // [B][64][256] bf16 bits
+  float* lse;              // [B][64]
+  float* part_o;           // [slots][64][256]
+  float* part_lse;         // [slots][64]
+  uint32_t* err;
+  float scale;
+  int B, max_pages, num_pages, grid;
+  uint64_t wait_budget_ns;
+};
+
+// Kernel launchers (each returns the launch's cudaError_t).
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_decode_split_simt(const DecodeParams& p, bool fp8, cudaStream_t stream);
+cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_selftest_wait(uint32_t* err, uint64_t budget_ns, cudaStream_t stream);
+
+}  // namespace mfa

@@ -1,0 +1,194 @@
+/*
+ * mfa.h -- C ABI of libmfa: decode-time Multi-matrix Factorization Attention
+ * (MFA) on one NVIDIA GB300 (sm_103a).
+ *
+ * What MFA decode attention is ("Step-3 is Large yet Affordable: Model-system
+ * Co-design for Cost-effective Decoding", paper summary page):
+ *   - section 2 / Table 1: 64 query heads share ONE key head and ONE value head,
+ *     both of dimension 256;
+ *   - section 8.1: the attention instance runs a custom Flash-Attention kernel
+ *     over its own per-sequence KV cache (each GPU serves an independent batch);
+ *   - sections 5.1 and 7: with an 8-bit KV cache this reads 512 bytes per token
+ *     and does 128 FLOPs per byte, so the kernel is bound by memory bandwidth.
+ * For every sequence b and head h the library computes
+ *     out[b,h,:] = softmax_j( scale * q[b,h,:] . K[b,j,:] ) . V[b,j,:],  j < L_b
+ *     lse[b,h]   = ln sum_j exp( scale * q[b,h,:] . K[b,j,:] )
+ * (natural log of the scaled logits; L_b = 0 gives out = 0, lse = -inf).
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument is caller-owned memory. Device pointers are
+ *     marked [device]. The library never allocates, frees or synchronises
+ *     inside a compute call. Work is enqueued on `stream`, a cudaStream_t
+ *     passed as void* (NULL = the legacy default stream). A compute call may
+ *     be captured into a CUDA graph.
+ *   - The call checks its arguments on the host and returns
+ *     MFA_ERR_INVALID_ARG / MFA_ERR_WORKSPACE before it enqueues anything.
+ *   - Faults that only the device can see set bits in an error word in the
+ *     workspace header. The kernel then skips the bad access and carries on;
+ *     it never traps. These faults are a page id outside [0, num_pages), a
+ *     length beyond the page table's capacity, or a pipeline wait that gave
+ *     up. mfa_check_device_errors() reads and optionally clears the word.
+ *   - MFA_ERR_CUDA means a CUDA runtime call or a launch failed; the
+ *     message is kept per host thread and mfa_last_error() returns it.
+ *   - Layouts (all row-major, contiguous):
+ *       q          [batch][64][256] bf16
+ *       out        [batch][64][256] bf16,  lse [batch][64] fp32
+ *       k_cache, v_cache [num_pages][64][256] bf16, or E4M3 bytes for _fp8
+ *       k_scale, v_scale [num_pages][64] fp32 (one scale per cached token)
+ *       page_table [batch][max_pages] int32: token j of sequence b is row
+ *                  j % 64 of page page_table[b][j / 64]
+ *       seq_lens   [batch] int32: tokens cached per sequence (device-owned
+ *                  counter: the append writes at seq_lens[b] and advances it,
+ *                  and attention reads it, so the token just appended is
+ *                  attended -- the "DuckLLM decode fixed-cost reduction" page,
+ *                  section 7.6, decode-context kernel)
+ *   - Pages hold 64 tokens. q, out and the cache base pointers must be
+ *     16-byte aligned.
+ *   - One device: all pointers belong to the current device of the calling
+ *     thread.
+ */
+#ifndef MFA_H_
+#define MFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MFA_HEADS 64
+#define MFA_HEAD_DIM 256
+#define MFA_PAGE_SIZE 64
+#define MFA_MAX_BATCH 1024
+
+typedef enum {
+  MFA_OK = 0,
+  MFA_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size (host check) */
+  MFA_ERR_UNSUPPORTED = 2,      /* device is not sm_103 */
+  MFA_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
+  MFA_ERR_WORKSPACE = 4,        /* workspace missing or smaller than required */
+  MFA_ERR_DEVICE_PAGE = 5,      /* device saw a page id outside [0, num_pages) */
+  MFA_ERR_DEVICE_CAPACITY = 6,  /* device saw a length beyond max_pages * 64 */
+  MFA_ERR_DEVICE_TIMEOUT = 7    /* a pipeline wait inside a kernel gave up */
+} mfa_status_t;
+
+/* Error-word bits (the first uint32 of the workspace). */
+#define MFA_DEVERR_PAGE 0x1u
+#define MFA_DEVERR_CAPACITY 0x2u
+#define MFA_DEVERR_TIMEOUT 0x4u
+
+/* Static description of how a decode call splits its work.
+ * Host only; needs no GPU. */
+typedef struct {
+  int grid_ctas;            /* CTAs of the split kernel (one per SM at most) */
+  int partial_slots;        /* grid_ctas + batch - 1 split results */
+  size_t workspace_bytes;   /* bytes mfa_decode_attention* needs */
+} mfa_plan_t;
+
+/* Split-KV planning (host only). The split kernel divides the pages of all
+ * sequences, P = sum_b ceil(L_b / 64), into `grid_ctas` = G contiguous,
+ * equal ranges that cross sequence boundaries: CTA c owns pages
+ * [floor(c*P/G), floor((c+1)*P/G)) and writes one partial result per
+ * sequence b it touches, into slot c + b. `max_len_hint` is the expected
+ * maximum length and only sizes the grid; longer sequences are still handled.
+ * `num_sms` <= 0 means the current device's SM count. Returns
+ * MFA_ERR_INVALID_ARG for batch outside [1, MFA_MAX_BATCH] or a negative
+ * hint. */
+mfa_status_t mfa_plan_decode(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan);
+
+/* Workspace size for mfa_decode_attention* on the current device; 0 on a bad
+ * argument. The same workspace also serves the append calls, which use only
+ * its header. */
+size_t mfa_decode_workspace_bytes(int batch, int max_len_hint);
+
+/* Zero the workspace header (error word). Call once after allocating the
+ * workspace. [device] workspace. Enqueued on `stream`. */
+mfa_status_t mfa_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* KV append (bf16 cache). For every sequence b, writes n_new tokens
+ * k_new[b][t][:], v_new[b][t][:] (bf16 [batch][n_new][256], [device]) at
+ * positions seq_lens[b] + t, then adds n_new to seq_lens[b] on the device.
+ * n_new = 1 is the decode step. The writes go in place: the cache is never
+ * reallocated (the static-cache lesson of the "DuckLLM decode fixed-cost
+ * reduction" page, section 7.2). A sequence whose tokens would exceed
+ * max_pages * 64, or that meets a bad page id, is left unchanged and sets
+ * MFA_DEVERR_CAPACITY / MFA_DEVERR_PAGE. `workspace` is any workspace sized
+ * by mfa_decode_workspace_bytes (only its error word is used). */
+mfa_status_t mfa_kv_append(const void* k_new, const void* v_new, int n_new,
+                           void* k_cache, void* v_cache,
+                           const int32_t* page_table, int32_t* seq_lens,
+                           int batch, int max_pages, int num_pages,
+                           void* workspace, void* stream);
+
+/* KV append into an FP8-E4M3 cache ("Step-3 is Large yet Affordable",
+ * section 7: 8-bit KV, 512 bytes per token per layer). Each new bf16 row x is
+ * quantised on the device with its own fp32 scale s = absmax(x) / 448
+ * (s = 1 for an all-zero row); codes are E4M3(x / s), rounded to nearest even
+ * and saturated to +-448 (OCP OFP8 E4M3). s goes to k_scale / v_scale
+ * [num_pages][64] at the token's slot. Everything else as mfa_kv_append. */
+mfa_status_t mfa_kv_append_fp8(const void* k_new, const void* v_new, int n_new,
+                               void* k_cache, void* v_cache,
+                               float* k_scale, float* v_scale,
+                               const int32_t* page_table, int32_t* seq_lens,
+                               int batch, int max_pages, int num_pages,
+                               void* workspace, void* stream);
+
+/* MFA decode attention over a bf16 paged cache (formula at the top of this
+ * file). q, out, lse, caches, page_table, seq_lens: [device], layouts above.
+ * `scale` multiplies the logits (1/16 = 1/sqrt(256) for Step-3).
+ * `max_len_hint`: expected maximum of seq_lens; it sizes the grid only.
+ * `workspace` / `workspace_bytes`: [device] scratch of at least
+ * mfa_decode_workspace_bytes(batch, max_len_hint) bytes, initialised once by
+ * mfa_workspace_init. It holds the error word and the per-split partial
+ * results; calls that share a workspace must not overlap on the GPU.
+ * Host errors: MFA_ERR_INVALID_ARG (null or misaligned pointers, batch outside
+ * [1, MFA_MAX_BATCH], max_pages < 1, num_pages < 1, hint < 0),
+ * MFA_ERR_WORKSPACE. Device faults (bad page id, length beyond
+ * max_pages * 64, wait timeout) set the error word; the kernel then reads
+ * page 0 instead of a bad page and clamps a length to the capacity, so the
+ * outputs of that sequence are meaningless. */
+mfa_status_t mfa_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* page_table, const int32_t* seq_lens,
+                                  void* out, float* lse, float scale,
+                                  int batch, int max_pages, int num_pages, int max_len_hint,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* MFA decode attention over an FP8-E4M3 paged cache with per-token fp32
+ * scales (k_scale, v_scale [num_pages][64], [device]). The cached value is
+ * decode(code) * scale. Queries stay bf16. Everything else as
+ * mfa_decode_attention. */
+mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* page_table, const int32_t* seq_lens,
+                                      void* out, float* lse, float scale,
+                                      int batch, int max_pages, int num_pages, int max_len_hint,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, read the workspace error word and return the first
+ * device fault it records (MFA_ERR_DEVICE_PAGE, _CAPACITY, _TIMEOUT) or MFA_OK.
+ * `clear` != 0 resets the word afterwards. This call blocks the host. */
+mfa_status_t mfa_check_device_errors(void* workspace, int clear, void* stream);
+
+/* Budget, in nanoseconds, after which a pipeline wait inside a kernel gives up
+ * and sets MFA_DEVERR_TIMEOUT (default 2e9 = 2 s). Applies to launches made
+ * after the call, from any thread. */
+void mfa_set_wait_budget_ns(uint64_t budget_ns);
+
+/* Self-test of the bounded wait: launches one CTA that waits on an mbarrier
+ * nothing arrives on, with the given budget; the wait must give up, set
+ * MFA_DEVERR_TIMEOUT in the workspace error word and return. */
+mfa_status_t mfa_selftest_wait_timeout(void* workspace, uint64_t budget_ns, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* mfa_status_string(mfa_status_t status);
+
+/* Message of the last failure seen by a call on this host thread ("" if none);
+ * valid until the next call on the same thread. */
+const char* mfa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MFA_H_ */

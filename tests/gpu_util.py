@@ -1,0 +1,150 @@
+"""Helpers shared by the GPU tests: put a seeded case on the device, run the
+CUDA path through the C ABI, run the oracle on the same inputs, compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from decode_attention_mfa_gb300 import capi
+from decode_attention_mfa_gb300 import workloads as wl
+
+# Tolerances against the fp64 oracle (bf16 output, fp32 accumulation).
+MAX_ABS = 1e-2
+REL_L2 = 5e-3
+LSE_ABS = 1e-3
+
+E4M3_NAN = 0x7F
+
+
+class DeviceCache:
+    """Device buffers of one decode problem (caller-owned memory for the C ABI)."""
+
+    def __init__(self, case: wl.Case, kv_dtype: str = "bf16", device="cuda"):
+        self.case = case
+        self.kv_dtype = kv_dtype
+        self.B = case.batch
+        self.num_pages = case.num_pages
+        self.max_pages = case.page_table.shape[1]
+        self.q = case.q.to(device)
+        self.page_table = torch.from_numpy(case.page_table).to(device)
+        if kv_dtype == "bf16":
+            self.k_cache = wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, self.num_pages).to(device)
+            self.v_cache = wl.scatter_rows(case.v_rows, case.lengths0, case.page_table, self.num_pages).to(device)
+            self.k_scale = self.v_scale = None
+            self.seq_lens = torch.from_numpy(case.lengths0.astype(np.int32)).to(device)
+        else:
+            # E4M3 cache: poisoned (NaN codes, NaN scales), then filled by the device append
+            self.k_cache = torch.full((self.num_pages, wl.PAGE_SIZE, wl.HEAD_DIM), E4M3_NAN, dtype=torch.uint8,
+                                      device=device)
+            self.v_cache = torch.full_like(self.k_cache, E4M3_NAN)
+            self.k_scale = torch.full((self.num_pages, wl.PAGE_SIZE), float("nan"), dtype=torch.float32,
+                                      device=device)
+            self.v_scale = torch.full_like(self.k_scale, float("nan"))
+            self.seq_lens = torch.zeros(self.B, dtype=torch.int32, device=device)
+        self.out = torch.empty((self.B, wl.HEADS, wl.HEAD_DIM), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((self.B, wl.HEADS), dtype=torch.float32, device=device)
+        self.max_len_hint = int(case.lengths_after_append.max()) if self.B else 0
+        self.ws_bytes = capi.mfa_decode_workspace_bytes(self.B, self.max_len_hint)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        capi.mfa_workspace_init(self.workspace, self.ws_bytes)
+        if kv_dtype == "fp8":
+            self.fill_fp8(case.k_rows, case.v_rows, case.lengths0)
+
+    def fill_fp8(self, k_rows, v_rows, lengths):
+        """Quantise the initial tokens on the device: one append call per sequence."""
+        off = 0
+        kd, vd = k_rows.to(self.q.device), v_rows.to(self.q.device)
+        for b, n in enumerate(np.asarray(lengths)):
+            n = int(n)
+            if n:
+                capi.mfa_kv_append_fp8(
+                    kd[off:off + n], vd[off:off + n], n, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                    self.page_table.data_ptr() + 4 * b * self.max_pages, self.seq_lens.data_ptr() + 4 * b,
+                    1, self.max_pages, self.num_pages, self.workspace)
+            off += n
+
+    def append(self, k_new, v_new):
+        n_new = k_new.shape[1]
+        kd = k_new.to(self.q.device).contiguous()
+        vd = v_new.to(self.q.device).contiguous()
+        if self.kv_dtype == "bf16":
+            capi.mfa_kv_append(kd, vd, n_new, self.k_cache, self.v_cache, self.page_table, self.seq_lens,
+                               self.B, self.max_pages, self.num_pages, self.workspace)
+        else:
+            capi.mfa_kv_append_fp8(kd, vd, n_new, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                                   self.page_table, self.seq_lens, self.B, self.max_pages, self.num_pages,
+                                   self.workspace)
+
+    def attend(self, stream=None, max_len_hint=None):
+        hint = self.max_len_hint if max_len_hint is None else max_len_hint
+        ws_bytes = self.ws_bytes
+        if hint != self.max_len_hint:
+            ws_bytes = capi.mfa_decode_workspace_bytes(self.B, hint)
+            if ws_bytes > self.workspace.numel():
+                self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=self.q.device)
+                capi.mfa_workspace_init(self.workspace, ws_bytes)
+        if self.kv_dtype == "bf16":
+            capi.mfa_decode_attention(self.q, self.k_cache, self.v_cache, self.page_table, self.seq_lens,
+                                      self.out, self.lse, wl.SCALE, self.B, self.max_pages, self.num_pages,
+                                      hint, self.workspace, ws_bytes, stream)
+        else:
+            capi.mfa_decode_attention_fp8(self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                                          self.page_table, self.seq_lens, self.out, self.lse, wl.SCALE, self.B,
+                                          self.max_pages, self.num_pages, hint, self.workspace, ws_bytes, stream)
+
+    def check_errors(self):
+        capi.mfa_check_device_errors(self.workspace, clear=True)
+
+    def host_caches(self):
+        """(k_cache, v_cache, k_scale, v_scale, seq_lens) copied back as numpy (bits for bf16)."""
+        torch.cuda.synchronize()
+        if self.kv_dtype == "bf16":
+            return (wl.bits(self.k_cache.cpu()), wl.bits(self.v_cache.cpu()), None, None,
+                    self.seq_lens.cpu().numpy())
+        return (self.k_cache.cpu().numpy(), self.v_cache.cpu().numpy(), self.k_scale.cpu().numpy(),
+                self.v_scale.cpu().numpy(), self.seq_lens.cpu().numpy())
+
+
+def oracle_caches(oracle, case: wl.Case, kv_dtype: str):
+    """The oracle's own host copy of the cache (bf16 bits, or E4M3 via its quantiser)."""
+    n = case.num_pages
+    if kv_dtype == "bf16":
+        kc = wl.bits(wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, n)).copy()
+        vc = wl.bits(wl.scatter_rows(case.v_rows, case.lengths0, case.page_table, n)).copy()
+        return kc, vc, None, None, case.lengths0.astype(np.int32).copy()
+    kcodes, kscale = oracle.quantize_tokens_e4m3(wl.bits(case.k_rows))
+    vcodes, vscale = oracle.quantize_tokens_e4m3(wl.bits(case.v_rows))
+    slots = wl.slots_of(case.lengths0, case.page_table)
+    kc = np.full((n * wl.PAGE_SIZE, wl.HEAD_DIM), E4M3_NAN, np.uint8)
+    vc = np.full_like(kc, E4M3_NAN)
+    ks = np.full(n * wl.PAGE_SIZE, np.nan, np.float32)
+    vs = np.full_like(ks, np.nan)
+    kc[slots], vc[slots], ks[slots], vs[slots] = kcodes, vcodes, kscale, vscale
+    return (kc.reshape(n, wl.PAGE_SIZE, -1), vc.reshape(n, wl.PAGE_SIZE, -1), ks.reshape(n, -1),
+            vs.reshape(n, -1), case.lengths0.astype(np.int32).copy())
+
+
+def used_slots_equal(a, b, lengths, page_table):
+    """Compare two caches on the slots that hold tokens (bit-exact)."""
+    slots = wl.slots_of(lengths, page_table)
+    n_slots = a.shape[0] * a.shape[1]
+    fa = np.ascontiguousarray(a).reshape(n_slots, -1)
+    fb = np.ascontiguousarray(b).reshape(n_slots, -1)
+    return np.array_equal(fa[slots].view(np.uint8), fb[slots].view(np.uint8))
+
+
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, label=""):
+    """Tolerance check against the oracle; returns the error figures."""
+    o = out_gpu.float().cpu().numpy().astype(np.float64)
+    l = lse_gpu.cpu().numpy().astype(np.float64)
+    finite_ref = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(l), finite_ref), f"{label}: LSE finiteness differs"
+    assert np.all(np.isfinite(o)), f"{label}: non-finite output"
+    max_abs = float(np.max(np.abs(o - out_ref))) if o.size else 0.0
+    denom = float(np.linalg.norm(out_ref))
+    rel_l2 = float(np.linalg.norm(o - out_ref) / denom) if denom > 0 else float(np.linalg.norm(o))
+    dl = float(np.max(np.abs(l[finite_ref] - lse_ref[finite_ref]))) if finite_ref.any() else 0.0
+    assert max_abs <= MAX_ABS, f"{label}: max-abs {max_abs:.3e} > {MAX_ABS}"
+    assert rel_l2 <= REL_L2, f"{label}: rel-L2 {rel_l2:.3e} > {REL_L2}"
+    assert dl <= LSE_ABS, f"{label}: |dlse| {dl:.3e} > {LSE_ABS}"
+    return {"max_abs": max_abs, "rel_l2": rel_l2, "lse_abs": dl}

@@ -1,0 +1,82 @@
+"""C-ABI library checks that need no GPU: the library loads, exports every
+function include/mfa.h declares, plans splits, names its status codes, and
+the split partition it implements is a valid one (checked on the formulas)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from decode_attention_mfa_gb300 import build as mfa_build
+from decode_attention_mfa_gb300 import capi
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mfa_build.build()
+    return capi.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = capi.header_functions()
+    assert len(names) >= 12
+    raw = ctypes.CDLL(capi.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in include/mfa.h but not exported"
+    assert set(names) == set(capi._SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code, name in capi.STATUS_NAMES.items():
+        assert capi.mfa_status_string(code) == name
+
+
+def test_plan_without_gpu(lib):
+    p = capi.mfa_plan_decode(32, 4096, 152)
+    assert p.grid_ctas == 152 and p.partial_slots == 152 + 31
+    assert p.workspace_bytes == 256 + p.partial_slots * (64 * 256 * 4 + 64 * 4)
+    assert capi.mfa_plan_decode(2, 100, 152).grid_ctas == 2
+    one = capi.mfa_plan_decode(1, 0, 152)
+    assert one.grid_ctas == 1 and one.partial_slots == 1
+    for bad in ((0, 10), (2000, 10), (4, -1)):
+        with pytest.raises(capi.MFAError):
+            capi.mfa_plan_decode(bad[0], bad[1], 152)
+
+
+def _cta_lo(c, P, G):
+    return c * P // G
+
+
+def _cta_of_page(p, P, G):
+    return ((p + 1) * G - 1) // P
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_partition_slots_are_unique_and_combine_finds_them(seed):
+    """Split scheme used by the split and combine kernels: CTA c owns pages
+    [c*P//G, (c+1)*P//G); its piece of sequence b goes to slot c + b. Slots
+    never collide, stay below G + B - 1, and the combine's CTA interval for b
+    is exactly the CTAs that own pages of b."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 60))
+    pages = rng.integers(0, 40, size=B) * (rng.random(B) < 0.9)
+    G = int(rng.integers(1, 160))
+    P = int(pages.sum())
+    if P == 0:
+        return
+    prefix = np.concatenate([[0], np.cumsum(pages)])
+    owners, slots = {}, set()
+    for c in range(G):
+        lo, hi = _cta_lo(c, P, G), _cta_lo(c + 1, P, G)
+        for b in range(B):
+            if max(lo, prefix[b]) < min(hi, prefix[b + 1]):
+                s = c + b
+                assert s not in slots and s < G + B - 1
+                slots.add(s)
+                owners.setdefault(b, []).append(c)
+    for b in range(B):
+        if pages[b] == 0:
+            assert b not in owners
+            continue
+        cf, cl = _cta_of_page(prefix[b], P, G), _cta_of_page(prefix[b + 1] - 1, P, G)
+        found = [c for c in range(cf, cl + 1) if _cta_lo(c, P, G) < _cta_lo(c + 1, P, G)]
+        assert found == owners[b]
