@@ -49,6 +49,7 @@ _SIGNATURES = {
     "mfa_check_device_errors": ([_P, _I, _P], _I),
     "mfa_set_wait_budget_ns": ([_U64], None),
     "mfa_selftest_wait_timeout": ([_P, _U64, _P], _I),
+    "mfa_profile_split_events": ([_P, _P], None),
     "mfa_status_string": ([_I], ctypes.c_char_p),
     "mfa_last_error": ([], ctypes.c_char_p),
 }
@@ -162,6 +163,15 @@ def mfa_set_wait_budget_ns(budget_ns: int):
 
 def mfa_selftest_wait_timeout(workspace, budget_ns: int, stream=None):
     _check(load().mfa_selftest_wait_timeout(_ptr(workspace), int(budget_ns), _stream(stream)))
+
+
+def mfa_profile_split_events(start_event, stop_event):
+    """torch.cuda.Event objects (or raw handles); None, None turns the hook off."""
+    def handle(e):
+        if e is None or isinstance(e, int):
+            return e
+        return e.cuda_event
+    load().mfa_profile_split_events(handle(start_event), handle(stop_event))
 
 
 def mfa_status_string(status: int) -> str:

@@ -15,6 +15,7 @@ namespace {
 using namespace mfa;
 
 thread_local std::string g_last_error;
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 std::atomic<uint64_t> g_wait_budget_ns{2000000000ull};
 
 mfa_status_t fail(mfa_status_t st, const char* fmt, ...) {
@@ -189,8 +190,13 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   const DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out,
                                             lse, scale, batch, max_pages, num_pages, workspace, plan);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_split_simt(p, fp8, s);
+  cudaError_t e;
+  if (g_prof_start && (e = cudaEventRecordWithFlags(g_prof_start, s, cudaEventRecordExternal)) != cudaSuccess)
+    return cuda_fail(e, "profile event record");
+  e = launch_decode_split_simt(p, fp8, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
+  if (g_prof_stop && (e = cudaEventRecordWithFlags(g_prof_stop, s, cudaEventRecordExternal)) != cudaSuccess)
+    return cuda_fail(e, "profile event record");
   e = launch_lse_combine(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "lse combine launch");
   return MFA_OK;
@@ -287,6 +293,15 @@ mfa_status_t mfa_selftest_wait_timeout(void* workspace, uint64_t budget_ns, void
       launch_selftest_wait(static_cast<uint32_t*>(workspace), budget_ns, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return MFA_OK;
+}
+
+void mfa_profile_split_events(void* start_event, void* stop_event) {
+  if (start_event && stop_event) {
+    g_prof_start = static_cast<cudaEvent_t>(start_event);
+    g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  } else {
+    g_prof_start = g_prof_stop = nullptr;
+  }
 }
 
 const char* mfa_status_string(mfa_status_t status) {

@@ -180,6 +180,14 @@ void mfa_set_wait_budget_ns(uint64_t budget_ns);
  * MFA_DEVERR_TIMEOUT in the workspace error word and return. */
 mfa_status_t mfa_selftest_wait_timeout(void* workspace, uint64_t budget_ns, void* stream);
 
+/* Timing hook for benchmarks. With both handles non-NULL (cudaEvent_t created
+ * with timing enabled), every later decode call on this host thread records
+ * start_event on its stream just before the split kernel and stop_event just
+ * after it, so cudaEventElapsedTime gives that kernel's device time. Under
+ * stream capture the records become external event nodes of the graph.
+ * (NULL, NULL) turns the hook off. */
+void mfa_profile_split_events(void* start_event, void* stop_event);
+
 /* Human-readable name of a status code (static string). */
 const char* mfa_status_string(mfa_status_t status);
 
