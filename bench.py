@@ -86,7 +86,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=open(self.path + ".err", "w"))
         except (FileNotFoundError, OSError):
             self.proc = None
         time.sleep(0.3)
@@ -114,7 +114,11 @@ class ClockSampler:
                     continue
             os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+            err = ""
+            if self.path and os.path.exists(self.path + ".err"):
+                err = open(self.path + ".err").read().strip()[:200]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"no nvidia-smi samples {err}".strip()],
+                    "samples": 0}
         inside = [r for r in rows if t0 - 0.06 <= r[0] <= t1 + 0.06] or rows[-3:]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
@@ -301,12 +305,13 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.time()
-        e0.record(stream)
-        for _ in range(reps):
-            g_full.replay()
-        if g_tail is not None:
-            g_tail.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            e0.record(stream)
+            for _ in range(reps):
+                g_full.replay()
+            if g_tail is not None:
+                g_tail.replay()
+            e1.record(stream)
         torch.cuda.synchronize()
         t1 = time.time()
         mdist.barrier()

@@ -8,6 +8,8 @@
 #include <mutex>
 #include <string>
 
+#include <cudaTypedefs.h>
+
 #include "mfa_internal.h"
 
 namespace {
@@ -83,6 +85,44 @@ void fill_plan(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------ TMA descriptors
+// Tensor maps are encoded on the host per call (a pure host computation) and
+// passed to the kernel as __grid_constant__ parameters, so a captured graph
+// keeps them with its node.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+mfa_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  if (!g_encode) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  *fn = g_encode;
+  return MFA_OK;
+}
+
+// 2-D bf16 tensor [rows][256] read in [64 rows x 64 columns] boxes with the
+// 128-byte swizzle (128-byte box rows).
+mfa_status_t encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  mfa_status_t st = get_encoder(&enc);
+  if (st != MFA_OK) return st;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MFA_OK;
+}
 
 // ------------------------------------------------------------ common checks
 mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache,
@@ -193,7 +233,16 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   cudaError_t e;
   if (g_prof_start && (e = cudaEventRecordWithFlags(g_prof_start, s, cudaEventRecordExternal)) != cudaSuccess)
     return cuda_fail(e, "profile event record");
-  e = launch_decode_split_simt(p, fp8, s);
+  if (fp8) {
+    e = launch_decode_split_simt(p, true, s);
+  } else {
+    CUtensorMap kmap, vmap, qmap;
+    if ((st = encode_rows_bf16(&kmap, k_cache, (uint64_t)num_pages * kPageSize)) != MFA_OK ||
+        (st = encode_rows_bf16(&vmap, v_cache, (uint64_t)num_pages * kPageSize)) != MFA_OK ||
+        (st = encode_rows_bf16(&qmap, q, (uint64_t)batch * kHeads)) != MFA_OK)
+      return st;
+    e = launch_decode_split_tc(p, kmap, vmap, qmap, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
   if (g_prof_stop && (e = cudaEventRecordWithFlags(g_prof_stop, s, cudaEventRecordExternal)) != cudaSuccess)
     return cuda_fail(e, "profile event record");

@@ -56,6 +56,9 @@ struct DecodeParams {
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_split_simt(const DecodeParams& p, bool fp8, cudaStream_t stream);
+cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                   const CUtensorMap& q_map, cudaStream_t stream);
+size_t decode_split_tc_smem_bytes(int B);
 cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t budget_ns, cudaStream_t stream);
 
