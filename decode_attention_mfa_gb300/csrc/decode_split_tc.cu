@@ -385,6 +385,18 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   const uint32_t taddr_o = tmem + lane_base + 128;
   const float c2 = p.scale * kLog2e;
   uint32_t s_cnt = 0, p_cnt = 0, tile_i = 0;
+  // o_ready completes once per P.V; a parity wait only tells the current phase
+  // from the previous one, so its completions are observed one by one, in
+  // order. Waiting for P.V(g-1) before handing over P(g) keeps the barrier at
+  // most one phase ahead of this count.
+  uint32_t o_seen = 0;
+  auto observe_pv = [&](uint32_t k) -> bool {
+    while (o_seen <= k) {
+      if (!cx.wait(kBarOReady, o_seen & 1)) return false;
+      ++o_seen;
+    }
+    return true;
+  };
   Seg s;
   bool ok = seg_first(s_prefix, s_len, p.B, lo, hi, s);
 
@@ -433,7 +445,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         }
         if (t > 0 && rescale_o) {
           // O^T holds the previous tiles: wait for their last P.V, then scale its columns
-          if (!cx.wait(kBarOReady, (p_cnt - 1) & 1)) return;
+          if (!observe_pv(p_cnt - 1)) return;
           tc_fence_after();
           scale_o_columns(taddr_o, alpha);
         }
@@ -454,6 +466,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         packed[h >> 1] = *reinterpret_cast<uint32_t*>(&b2);
       }
       const uint32_t pbuf = p_cnt & 1;
+      if (p_cnt > 0 && !observe_pv(p_cnt - 1)) return;
       if (!cx.wait(kBarPEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
       const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
 #pragma unroll
@@ -470,7 +483,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       ++tile_i;
     }
     // ---- epilogue of this sequence piece: l = sum over the 128 lanes, O^T / l, LSE
-    if (!cx.wait(kBarOReady, (p_cnt - 1) & 1)) return;
+    if (!observe_pv(p_cnt - 1)) return;
     tc_fence_after();
     warp_reduce_scatter_sum(lp, lane);
     named_barrier_softmax();  // earlier readers of red/alpha are done

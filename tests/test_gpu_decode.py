@@ -45,16 +45,19 @@ def _oracle(oracle_mod, case, kv):
     return oracle_mod.mfa_decode(wl.bits(case.q), kc, vc, case.page_table, sl, wl.SCALE, k_scale=ks, v_scale=vs)
 
 
+@pytest.mark.parametrize("grid", ["planned", "one_cta"])
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_small_parity(oracle_mod, kv, name):
+def test_small_parity(oracle_mod, kv, name, grid):
+    """`planned` uses the grid the planner picks (few tiles per CTA); `one_cta`
+    (length hint 0) makes one CTA walk every tile of every sequence."""
     lengths = _lengths(name)
     case = _case(lengths, seed=1 + list(SMALL).index(name), kv=kv)
     dev = DeviceCache(case, kv)
-    dev.attend()
+    dev.attend(max_len_hint=0 if grid == "one_cta" else None)
     dev.check_errors()
     out_ref, lse_ref = _oracle(oracle_mod, case, kv)
-    compare(dev.out, dev.lse, out_ref, lse_ref, f"{kv}/{name}")
+    compare(dev.out, dev.lse, out_ref, lse_ref, f"{kv}/{name}/{grid}")
 
 
 def test_empty_sequences(oracle_mod):
