@@ -46,6 +46,7 @@ _SIGNATURES = {
     "mfa_kv_append_fp8": ([_P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
     "mfa_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P], _I),
     "mfa_check_device_errors": ([_P, _I, _P], _I),
     "mfa_set_wait_budget_ns": ([_U64], None),
     "mfa_selftest_wait_timeout": ([_P, _U64, _P], _I),
@@ -151,6 +152,16 @@ def mfa_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, 
                                            _ptr(lse), float(scale), batch, max_pages, num_pages,
                                            max_len_hint, _ptr(workspace), workspace_bytes,
                                            _stream(stream)))
+
+
+def mfa_decode_attention_noalloc(q, k_cache, v_cache, page_table, seq_lens, out, lse, scale, batch, max_pages,
+                                 num_pages, max_len_hint, device_error_word=None, stream=None):
+    """Same as mfa_decode_attention, but the split scratch is the library's own
+    static device array (no workspace argument); see include/mfa.h."""
+    _check(load().mfa_decode_attention_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                               _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch,
+                                               max_pages, num_pages, max_len_hint, _ptr(device_error_word),
+                                               _stream(stream)))
 
 
 def mfa_check_device_errors(workspace, clear: bool = True, stream=None):

@@ -253,6 +253,11 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
 
 }  // namespace
 
+namespace mfa {
+void set_last_error_message(const char* msg) { g_last_error = msg; }
+uint64_t current_wait_budget_ns() { return g_wait_budget_ns.load(std::memory_order_relaxed); }
+}  // namespace mfa
+
 extern "C" {
 
 mfa_status_t mfa_plan_decode(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan) {

@@ -59,6 +59,10 @@ cudaError_t launch_decode_split_simt(const DecodeParams& p, bool fp8, cudaStream
 cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                    const CUtensorMap& q_map, cudaStream_t stream);
 size_t decode_split_tc_smem_bytes(int B);
+
+// Host-side services of mfa_api.cu for other entry points of the library.
+void set_last_error_message(const char* msg);
+uint64_t current_wait_budget_ns();
 cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t budget_ns, cudaStream_t stream);
 

@@ -165,6 +165,33 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       int batch, int max_pages, int num_pages, int max_len_hint,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of mfa_decode_attention (bf16 cache). The paper
+ * has no counterpart: it exists for callers that cannot give the library a
+ * workspace -- a plugin or foreign-function host that passes only tensors it
+ * already owns and no allocator, or a running serving loop that must not call
+ * cudaMalloc (which can synchronise the whole device).
+ * Inputs, outputs and their layouts are those of mfa_decode_attention. The
+ * split scratch is a fixed 24 MiB device array inside the library, present on
+ * every GPU that loads it until the process exits. The call itself allocates
+ * nothing.
+ *   - The first call on a device looks up the array's device address, with
+ *     that device current. Make this first call before any stream capture.
+ *   - Batches whose split results need more than 24 MiB
+ *     (mfa_plan_decode().workspace_bytes > 24 MiB) return MFA_ERR_WORKSPACE
+ *     with a message.
+ *   - All calls share the one array, so calls that may overlap on the GPU
+ *     (other streams or host threads) race and must be serialised by the
+ *     caller.
+ * device_error_word: optional [device] uint32 that receives the MFA_DEVERR_*
+ * bits of device faults (it is not cleared by the call). With NULL, faults go
+ * to a word in the shared array, which each call clears, and are not
+ * reported. */
+mfa_status_t mfa_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* page_table, const int32_t* seq_lens,
+                                          void* out, float* lse, float scale,
+                                          int batch, int max_pages, int num_pages, int max_len_hint,
+                                          uint32_t* device_error_word, void* stream);
+
 /* Synchronise `stream`, read the workspace error word and return the first
  * device fault it records (MFA_ERR_DEVICE_PAGE, _CAPACITY, _TIMEOUT) or MFA_OK.
  * `clear` != 0 resets the word afterwards. This call blocks the host. */
