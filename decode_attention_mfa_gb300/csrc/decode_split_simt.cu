@@ -57,6 +57,8 @@ __global__ void __launch_bounds__(kSimtThreads) decode_split_simt_kernel(DecodeP
   extern __shared__ int smem_i[];
   int* s_len = smem_i;
   int* s_prefix = smem_i + p.B;
+  pdl_wait_prior_grid();    // previous kernel (the KV append) complete
+  pdl_launch_dependents();  // the combine may be scheduled; it waits for this grid
   build_page_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, p.err, s_len, s_prefix);
   const long long P = s_prefix[p.B];
   const int c = blockIdx.x, G = p.grid;
@@ -143,11 +145,8 @@ __global__ void __launch_bounds__(kSimtThreads) decode_split_simt_kernel(DecodeP
 
 cudaError_t launch_decode_split_simt(const DecodeParams& p, bool fp8, cudaStream_t stream) {
   const size_t smem = sizeof(int) * (2 * (size_t)p.B + 1);
-  if (fp8)
-    decode_split_simt_kernel<true><<<p.grid, kSimtThreads, smem, stream>>>(p);
-  else
-    decode_split_simt_kernel<false><<<p.grid, kSimtThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  if (fp8) return launch_pdl(decode_split_simt_kernel<true>, dim3(p.grid), dim3(kSimtThreads), smem, stream, p);
+  return launch_pdl(decode_split_simt_kernel<false>, dim3(p.grid), dim3(kSimtThreads), smem, stream, p);
 }
 
 }  // namespace mfa

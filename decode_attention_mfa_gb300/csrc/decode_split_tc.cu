@@ -128,83 +128,135 @@ __device__ __forceinline__ bool seg_next(const int* s_prefix, const int* s_len, 
 }
 
 // ---------------------------------------------------------------- producer
+// Page ids of one sequence piece for the producer warp: a window of 64 ids
+// [base, base + 64) held as two registers per lane (lane i: ids base + i and
+// base + 32 + i), filled by coalesced warp loads and handed out by shuffle.
+// Requests go forward, except that V pages trail the K pages of the next tile
+// by two, so the window slides by 32 only when a request reaches base + 64.
+struct PageIds {
+  const int32_t* row;  // page_table row of the sequence
+  int pg1, base;       // valid pages end at pg1
+  int lo_ids, hi_ids;
+  __device__ int fetch(int pg, const DecodeParams& p) const {
+    int id = 0;
+    if (pg < pg1) {
+      id = __ldg(row + pg);
+      if (id < 0 || id >= p.num_pages) {
+        raise_error(p.err, MFA_DEVERR_PAGE);
+        id = 0;
+      }
+    }
+    return id;
+  }
+  __device__ void start(int pg0, const DecodeParams& p, int lane) {
+    base = pg0;
+    lo_ids = fetch(base + lane, p);
+    hi_ids = fetch(base + 32 + lane, p);
+  }
+  // all lanes call with the same pg, base <= pg
+  __device__ int get(int pg, const DecodeParams& p, int lane) {
+    while (pg >= base + 64) {
+      base += 32;
+      lo_ids = hi_ids;
+      hi_ids = fetch(base + 32 + lane, p);
+    }
+    const int idx = pg - base;
+    return idx < 32 ? __shfl_sync(0xffffffffu, lo_ids, idx) : __shfl_sync(0xffffffffu, hi_ids, idx - 32);
+  }
+};
+
+// The whole producer warp runs this loop (uniform control flow); lane 0
+// issues the copies.
 __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               const CUtensorMap* qmap, const Ctx& cx, const int* s_prefix, const int* s_len,
                               long long lo, long long hi) {
+  const int lane = threadIdx.x & 31;
   const uint64_t pol_stream = policy_evict_first();
   const uint64_t pol_keep = policy_evict_last();
+  const uint32_t q_base = cx.base + smem_layout(p.B).q;
   uint32_t cc = 0, seg_i = 0;
   Seg s;
   bool ok = seg_first(s_prefix, s_len, p.B, lo, hi, s);
-  auto page_id = [&](int b, int pg) -> int {
-    int id = __ldg(p.page_table + (size_t)b * p.max_pages + pg);
-    if (id < 0 || id >= p.num_pages) {
-      raise_error(p.err, MFA_DEVERR_PAGE);
-      id = 0;
-    }
-    return id;
+  auto wait_slot = [&](uint32_t& dst, uint32_t& bar) -> bool {
+    const uint32_t slot = cc % kSlots, n = cc / kSlots;
+    const bool r = cx.wait(kBarEmpty + slot, (n & 1) ^ 1);
+    __syncwarp();
+    dst = cx.base + slot * kSlotBytes;
+    bar = cx.bar(kBarFull + slot);
+    return r;
   };
-  // issue one chunk: K dim block d of tile (pages pa[, pb]) or V half hf of page pv
+  // K dim block d of a tile of pages pa (and pb >= 0)
   auto issue_k = [&](int d, int pa, int pb) -> bool {
-    const uint32_t slot = cc % kSlots, n = cc / kSlots;
-    if (!cx.wait(kBarEmpty + slot, (n & 1) ^ 1)) return false;
-    const uint32_t dst = cx.base + slot * kSlotBytes;
-    mbar_arrive_expect_tx(cx.bar(kBarFull + slot), pb >= 0 ? 16384u : 8192u);
-    tma_load_2d(dst, kmap, d * 64, pa * kPageSize, cx.bar(kBarFull + slot), pol_stream);
-    if (pb >= 0) tma_load_2d(dst + 8192, kmap, d * 64, pb * kPageSize, cx.bar(kBarFull + slot), pol_stream);
-    ++cc;
-    return true;
-  };
-  auto issue_v = [&](int hf, int pv) -> bool {
-    const uint32_t slot = cc % kSlots, n = cc / kSlots;
-    if (!cx.wait(kBarEmpty + slot, (n & 1) ^ 1)) return false;
-    const uint32_t dst = cx.base + slot * kSlotBytes;
-    mbar_arrive_expect_tx(cx.bar(kBarFull + slot), 16384u);
-    tma_load_2d(dst, vmap, hf * 128, pv * kPageSize, cx.bar(kBarFull + slot), pol_stream);
-    tma_load_2d(dst + 8192, vmap, hf * 128 + 64, pv * kPageSize, cx.bar(kBarFull + slot), pol_stream);
-    ++cc;
-    return true;
-  };
-  auto issue_k_tile = [&](const Seg& sg, int t) -> bool {
-    const int pga = sg.pg0 + 2 * t;
-    const int pa = page_id(sg.b, pga);
-    const int pb = (pga + 1 < sg.pg1) ? page_id(sg.b, pga + 1) : -1;
-    for (int d = 0; d < 4; ++d)
-      if (!issue_k(d, pa, pb)) return false;
-    return true;
-  };
-  auto issue_v_tile = [&](const Seg& sg, int t) -> bool {
-    const int pga = sg.pg0 + 2 * t;
-    const int np = (pga + 1 < sg.pg1) ? 2 : 1;
-    for (int i = 0; i < np; ++i) {
-      const int pv = page_id(sg.b, pga + i);
-      if (!issue_v(0, pv) || !issue_v(1, pv)) return false;
+    uint32_t dst, bar;
+    if (!wait_slot(dst, bar)) return false;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, pb >= 0 ? 16384u : 8192u);
+      tma_load_2d(dst, kmap, d * 64, pa * kPageSize, bar, pol_stream);
+      if (pb >= 0) tma_load_2d(dst + 8192, kmap, d * 64, pb * kPageSize, bar, pol_stream);
     }
+    ++cc;
+    return true;
+  };
+  // V dims [hf*128, hf*128 + 128) of page pv
+  auto issue_v = [&](int hf, int pv) -> bool {
+    uint32_t dst, bar;
+    if (!wait_slot(dst, bar)) return false;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, 16384u);
+      tma_load_2d(dst, vmap, hf * 128, pv * kPageSize, bar, pol_stream);
+      tma_load_2d(dst + 8192, vmap, hf * 128 + 64, pv * kPageSize, bar, pol_stream);
+    }
+    ++cc;
     return true;
   };
   uint32_t last_q_parity = 0;
   bool issued_q = false;
   while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
     if (*cx.abort) break;
+    PageIds ids;
+    ids.row = p.page_table + (size_t)s.b * p.max_pages;
+    ids.pg1 = s.pg1;
+    ids.start(s.pg0, p, lane);
     // Q of this sequence (free once every S MMA of the previous piece is done)
-    if (!cx.wait(kBarQEmpty, (seg_i & 1) ^ 1)) break;
-    mbar_arrive_expect_tx(cx.bar(kBarQFull), (uint32_t)kQBytes);
-    for (int d = 0; d < 4; ++d)
-      tma_load_2d(cx.base + smem_layout(p.B).q + d * 8192, qmap, d * 64, s.b * kHeads, cx.bar(kBarQFull), pol_keep);
+    const bool qfree = cx.wait(kBarQEmpty, (seg_i & 1) ^ 1);
+    __syncwarp();
+    if (!qfree) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(cx.bar(kBarQFull), (uint32_t)kQBytes);
+      for (int d = 0; d < 4; ++d)
+        tma_load_2d(q_base + d * 8192, qmap, d * 64, s.b * kHeads, cx.bar(kBarQFull), pol_keep);
+    }
     issued_q = true;
     last_q_parity = seg_i & 1;
     ++seg_i;
     const int T = (s.pg1 - s.pg0 + 1) / 2;
-    bool good = issue_k_tile(s, 0);
-    for (int t = 1; good && t < T; ++t) good = issue_k_tile(s, t) && issue_v_tile(s, t - 1);
-    if (good) good = issue_v_tile(s, T - 1);
+    bool good = true;
+    // chunk order: K(0), then K(t), V(t-1) for t = 1..T-1, then V(T-1)
+    for (int t = 0; good && t <= T; ++t) {
+      if (t < T) {
+        const int pga = s.pg0 + 2 * t;
+        const int pa = ids.get(pga, p, lane);
+        const int pb = (pga + 1 < s.pg1) ? ids.get(pga + 1, p, lane) : -1;
+        for (int d = 0; good && d < 4; ++d) good = issue_k(d, pa, pb);
+      }
+      if (good && t > 0) {
+        const int pgv = s.pg0 + 2 * (t - 1);
+        const int np = (pgv + 1 < s.pg1) ? 2 : 1;
+        for (int i = 0; good && i < np; ++i) {
+          const int pv = ids.get(pgv + i, p, lane);
+          good = issue_v(0, pv) && issue_v(1, pv);
+        }
+      }
+    }
     if (!good) break;
   }
-  // drain: every copy this thread issued must land before the CTA exits
-  const uint64_t drain_budget = cx.budget;
-  for (uint32_t k = (cc > (uint32_t)kSlots ? cc - kSlots : 0); k < cc; ++k)
-    (void)mbar_wait(cx.bar(kBarFull + k % kSlots), (k / kSlots) & 1, drain_budget, nullptr, p.err);
-  if (issued_q) (void)mbar_wait(cx.bar(kBarQFull), last_q_parity, drain_budget, nullptr, p.err);
+  // drain: every copy this warp issued must land before the CTA exits
+  if (lane == 0) {
+    for (uint32_t k = (cc > (uint32_t)kSlots ? cc - kSlots : 0); k < cc; ++k)
+      (void)mbar_wait(cx.bar(kBarFull + k % kSlots), (k / kSlots) & 1, cx.budget, nullptr, p.err);
+    if (issued_q) (void)mbar_wait(cx.bar(kBarQFull), last_q_parity, cx.budget, nullptr, p.err);
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- MMA issue
@@ -560,6 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     tc_fence_before();
   }
+  pdl_wait_prior_grid();    // the KV append (or previous step) must be complete before reading its results
+  pdl_launch_dependents();  // the combine kernel may be scheduled now (its prologue reads seq_lens); it
+                            // waits for this grid before it reads the partials
   build_page_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, p.err, s_len, s_prefix);  // ends with a barrier
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -571,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     softmax_role(p, cx, s_prefix, s_len, lo, hi, tmem, c, gbase);
   } else if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer_role(p, &kmap, &vmap, &qmap, cx, s_prefix, s_len, lo, hi);
+    producer_role(p, &kmap, &vmap, &qmap, cx, s_prefix, s_len, lo, hi);
   } else {
     mma_role(p, cx, s_prefix, s_len, lo, hi, tmem);
   }
@@ -596,8 +651,7 @@ cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& kma
     if (e != cudaSuccess) return e;
     configured_bytes = (int)smem;
   }
-  decode_split_tc_kernel<<<p.grid, kThreads, smem, stream>>>(p, kmap, vmap, qmap);
-  return cudaGetLastError();
+  return launch_pdl(decode_split_tc_kernel, dim3(p.grid), dim3(kThreads), smem, stream, p, kmap, vmap, qmap);
 }
 
 }  // namespace mfa

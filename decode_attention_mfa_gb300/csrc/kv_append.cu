@@ -17,19 +17,12 @@ namespace {
 
 constexpr int kAppendThreads = 256;  // 8 warps, one token row (K or V) per warp at a time
 
-// One 512-byte bf16 row: lane i holds elements [8i, 8i + 8).
-__device__ __forceinline__ void copy_row_bf16(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                                              int lane) {
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + lane);
-  reinterpret_cast<uint4*>(dst)[lane] = v;
-}
-
+// Rows are 512 bytes of bf16: lane i holds elements [8i, 8i + 8).
 // Quantise one bf16 row to E4M3 with scale = absmax / 448 (1 for a zero row).
 // Divisions are IEEE round-to-nearest; the conversion rounds to nearest even
 // and saturates to +-448.
-__device__ __forceinline__ void quantise_row_e4m3(const uint16_t* __restrict__ src, uint8_t* __restrict__ dst,
+__device__ __forceinline__ void quantise_row_e4m3(const uint4 raw, uint8_t* __restrict__ dst,
                                                   float* __restrict__ scale_out, int lane) {
-  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src) + lane);
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
   float x[8];
 #pragma unroll
@@ -59,50 +52,67 @@ __device__ __forceinline__ void quantise_row_e4m3(const uint16_t* __restrict__ s
   if (lane == 0) *scale_out = s;
 }
 
+constexpr int kMaxStagedPages = 64;  // page ids validated once and kept in shared memory
+
 __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendParams p) {
   __shared__ int s_start;
   __shared__ int s_bad;
+  __shared__ int s_pages[kMaxStagedPages];
   const int b = blockIdx.x;
-  if (threadIdx.x == 0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kAppendThreads / 32;
+  pdl_launch_dependents();  // the decode kernel may run its prologue meanwhile
+  // the row of this warp's first work item (token t = i / 2, K or V) is read
+  // while warp 0 looks up and checks where the tokens go
+  const int first = warp;
+  uint4 first_row = make_uint4(0u, 0u, 0u, 0u);
+  if (first < 2 * p.n_new) {
+    const uint16_t* src = ((first & 1) ? p.v_new : p.k_new) + ((size_t)b * p.n_new + (first >> 1)) * kHeadDim;
+    first_row = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+  }
+  if (warp == 0) {
     const int start = p.seq_lens[b];
     const long long cap = (long long)p.max_pages * kPageSize;
-    s_bad = 0;
-    if (start < 0 || (long long)start + p.n_new > cap) {
-      raise_error(p.err, MFA_DEVERR_CAPACITY);
-      s_bad = 1;
-    } else {
-      // validate every page id the new tokens land in before writing anything
-      for (int pg = start / kPageSize; pg <= (start + p.n_new - 1) / kPageSize; ++pg) {
+    bool bad_cap = start < 0 || (long long)start + p.n_new > cap;
+    bool bad_page = false;
+    if (!bad_cap) {
+      // every page id the new tokens land in is checked before anything is written
+      const int pg_first = start / kPageSize, pg_last = (start + p.n_new - 1) / kPageSize;
+      for (int pg = pg_first + lane; pg <= pg_last; pg += 32) {
         const int page = p.page_table[(size_t)b * p.max_pages + pg];
-        if (page < 0 || page >= p.num_pages) {
-          raise_error(p.err, MFA_DEVERR_PAGE);
-          s_bad = 1;
-          break;
-        }
+        if (page < 0 || page >= p.num_pages) bad_page = true;
+        if (pg - pg_first < kMaxStagedPages) s_pages[pg - pg_first] = page;
       }
+      bad_page = __any_sync(0xffffffffu, bad_page);
     }
-    s_start = start;
+    if (lane == 0) {
+      if (bad_cap) raise_error(p.err, MFA_DEVERR_CAPACITY);
+      if (bad_page) raise_error(p.err, MFA_DEVERR_PAGE);
+      s_bad = (bad_cap || bad_page) ? 1 : 0;
+      s_start = start;
+    }
   }
   __syncthreads();
   if (s_bad) return;
   const int start = s_start;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kWarps = kAppendThreads / 32;
-  // work item i: token t = i / 2, K (even) or V (odd)
+  const int pg_first = start / kPageSize;
   for (int i = warp; i < 2 * p.n_new; i += kWarps) {
     const int t = i >> 1;
     const bool is_v = i & 1;
     const int pos = start + t;
-    const int page = p.page_table[(size_t)b * p.max_pages + pos / kPageSize];
+    const int pg = pos / kPageSize;
+    const int page = (pg - pg_first < kMaxStagedPages) ? s_pages[pg - pg_first]
+                                                        : p.page_table[(size_t)b * p.max_pages + pg];
     const size_t slot = (size_t)page * kPageSize + (pos % kPageSize);
     const uint16_t* src = (is_v ? p.v_new : p.k_new) + ((size_t)b * p.n_new + t) * kHeadDim;
+    const uint4 row = (i == first) ? first_row : __ldg(reinterpret_cast<const uint4*>(src) + lane);
     if (p.fp8) {
       uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + slot * kHeadDim;
       float* sc = (is_v ? p.v_scale : p.k_scale) + slot;
-      quantise_row_e4m3(src, dst, sc, lane);
+      quantise_row_e4m3(row, dst, sc, lane);
     } else {
       uint16_t* dst = static_cast<uint16_t*>(is_v ? p.v_cache : p.k_cache) + slot * kHeadDim;
-      copy_row_bf16(src, dst, lane);
+      reinterpret_cast<uint4*>(dst)[lane] = row;
     }
   }
   __syncthreads();

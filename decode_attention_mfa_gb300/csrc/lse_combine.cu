@@ -25,7 +25,9 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
   extern __shared__ int smem_i[];
   int* s_len = smem_i;
   int* s_prefix = smem_i + p.B;
+  // seq_lens is final before the split kernel starts; the partials are not
   build_page_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, s_len, s_prefix);
+  pdl_wait_prior_grid();
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * (kCombineThreads / 32) + warp;
@@ -56,14 +58,27 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
       w = exp2f((__ldcg(p.part_lse + (size_t)(c + b) * kHeads + h) - mx) * kLog2e);
     den += w;
     const int n = min(32, c_last - base + 1);
-    for (int j = 0; j < n; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      if (wj == 0.0f) continue;
-      const float* src = p.part_o + ((size_t)(base + j + b) * kHeads + h) * kHeadDim;
-      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src) + lane);
-      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 128) + lane);
-      a0.x += wj * x0.x; a0.y += wj * x0.y; a0.z += wj * x0.z; a0.w += wj * x0.w;
-      a1.x += wj * x1.x; a1.y += wj * x1.y; a1.z += wj * x1.z; a1.w += wj * x1.w;
+    // four partials per round: their eight loads are in flight together; a slot
+    // of an empty CTA range (weight 0) is never read (it may hold stale data)
+    for (int j = 0; j < n; j += 4) {
+      float wj[4];
+      float4 x0[4], x1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        wj[u] = __shfl_sync(0xffffffffu, w, (j + u) & 31);
+        if (j + u >= n) wj[u] = 0.0f;
+        x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (wj[u] != 0.0f) {
+          const float* src = p.part_o + ((size_t)(base + j + u + b) * kHeads + h) * kHeadDim;
+          x0[u] = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+          x1[u] = __ldcg(reinterpret_cast<const float4*>(src + 128) + lane);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a0.x += wj[u] * x0[u].x; a0.y += wj[u] * x0[u].y; a0.z += wj[u] * x0[u].z; a0.w += wj[u] * x0[u].w;
+        a1.x += wj[u] * x1[u].x; a1.y += wj[u] * x1[u].y; a1.z += wj[u] * x1[u].z; a1.w += wj[u] * x1[u].w;
+      }
     }
   }
 #pragma unroll
@@ -85,8 +100,7 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
 cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream) {
   dim3 grid(kHeads / (kCombineThreads / 32), p.B);
   const size_t smem = sizeof(int) * (2 * (size_t)p.B + 1);
-  lse_combine_kernel<<<grid, kCombineThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(lse_combine_kernel, grid, dim3(kCombineThreads), smem, stream, p);
 }
 
 }  // namespace mfa

@@ -85,6 +85,16 @@ __device__ __forceinline__ int seq_of_page(const int* s_prefix, int B, long long
   return lo;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels of one decode step are launched with programmatic stream
+// serialisation: a kernel lets the next one be scheduled early
+// (launch_dependents) and the next one runs its prologue, then waits for the
+// previous grid's completion and memory (wait) before reading its results.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- smem / mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
