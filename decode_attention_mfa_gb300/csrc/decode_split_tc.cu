@@ -38,9 +38,9 @@ constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kSlots = 9;                 // 16 KB ring slots
+constexpr int kSlots = 7;                 // 16 KB ring slots
 constexpr int kSlotBytes = 16384;
-constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]
+constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]; two buffers
 constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads] bf16
 constexpr int kTmemCols = 256;            // S^T x2 (64 cols each) + O^T (2 x 64 cols)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -61,7 +61,7 @@ __host__ __device__ inline SmemLayout smem_layout(int B) {
   SmemLayout L;
   L.ring = 0;
   L.q = L.ring + kSlots * kSlotBytes;
-  L.p = L.q + kQBytes;
+  L.p = L.q + 2 * kQBytes;
   L.len = L.p + 2 * kPBytes;
   L.prefix = L.len + 4 * B;
   L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64]
@@ -76,9 +76,9 @@ __host__ __device__ inline SmemLayout smem_layout(int B) {
 enum : int {
   kBarFull = 0,                 // [kSlots]
   kBarEmpty = kBarFull + kSlots,  // [kSlots]
-  kBarQFull = kBarEmpty + kSlots,
-  kBarQEmpty,
-  kBarSFull,                    // [2]
+  kBarQFull = kBarEmpty + kSlots,  // [2]
+  kBarQEmpty = kBarQFull + 2,       // [2]
+  kBarSFull = kBarQEmpty + 2,       // [2]
   kBarSEmpty = kBarSFull + 2,   // [2]
   kBarPFull = kBarSEmpty + 2,   // [2]
   kBarPEmpty = kBarPFull + 2,   // [2]
@@ -209,7 +209,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++cc;
     return true;
   };
-  uint32_t last_q_parity = 0;
+  uint32_t last_q_parity = 0, last_qb = 0;
   bool issued_q = false;
   while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
     if (*cx.abort) break;
@@ -217,17 +217,21 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ids.row = p.page_table + (size_t)s.b * p.max_pages;
     ids.pg1 = s.pg1;
     ids.start(s.pg0, p, lane);
-    // Q of this sequence (free once every S MMA of the previous piece is done)
-    const bool qfree = cx.wait(kBarQEmpty, (seg_i & 1) ^ 1);
+    // Q of this sequence into buffer seg_i % 2 (free once every S MMA of the
+    // piece before the previous one is done, so the loads of this piece need
+    // not wait for the previous piece to finish)
+    const uint32_t qb = seg_i & 1;
+    const bool qfree = cx.wait(kBarQEmpty + qb, ((seg_i >> 1) & 1) ^ 1);
     __syncwarp();
     if (!qfree) break;
     if (lane == 0) {
-      mbar_arrive_expect_tx(cx.bar(kBarQFull), (uint32_t)kQBytes);
+      mbar_arrive_expect_tx(cx.bar(kBarQFull + qb), (uint32_t)kQBytes);
       for (int d = 0; d < 4; ++d)
-        tma_load_2d(q_base + d * 8192, qmap, d * 64, s.b * kHeads, cx.bar(kBarQFull), pol_keep);
+        tma_load_2d(q_base + qb * kQBytes + d * 8192, qmap, d * 64, s.b * kHeads, cx.bar(kBarQFull + qb), pol_keep);
     }
     issued_q = true;
-    last_q_parity = seg_i & 1;
+    last_q_parity = (seg_i >> 1) & 1;
+    last_qb = qb;
     ++seg_i;
     const int T = (s.pg1 - s.pg0 + 1) / 2;
     bool good = true;
@@ -254,7 +258,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   if (lane == 0) {
     for (uint32_t k = (cc > (uint32_t)kSlots ? cc - kSlots : 0); k < cc; ++k)
       (void)mbar_wait(cx.bar(kBarFull + k % kSlots), (k / kSlots) & 1, cx.budget, nullptr, p.err);
-    if (issued_q) (void)mbar_wait(cx.bar(kBarQFull), last_q_parity, cx.budget, nullptr, p.err);
+    if (issued_q) (void)mbar_wait(cx.bar(kBarQFull + last_qb), last_q_parity, cx.budget, nullptr, p.err);
   }
   __syncwarp();
 }
@@ -274,7 +278,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
     __syncwarp();
     return r;
   };
-  auto do_s = [&](int t_in_seg) -> bool {
+  auto do_s = [&](int t_in_seg, uint32_t qb) -> bool {
     const uint32_t buf = s_cnt & 1, n = s_cnt >> 1;
     if (!wait_all(kBarSEmpty + buf, (n & 1) ^ 1)) return false;
     const uint32_t d_tmem = tmem + buf * 64;
@@ -284,7 +288,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
       if (lane == 0) {
         tc_fence_after();
         const uint32_t a0 = cx.base + slot * kSlotBytes;
-        const uint32_t b0 = cx.base + L.q + d * 8192;
+        const uint32_t b0 = cx.base + L.q + qb * kQBytes + d * 8192;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc_mma(d_tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024), kIdescS,
@@ -346,13 +350,14 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
   };
 
   while (alive && ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
-    if (!wait_all(kBarQFull, seg_i & 1)) break;
+    const uint32_t qb = seg_i & 1;
+    if (!wait_all(kBarQFull + qb, (seg_i >> 1) & 1)) break;
     const int T = (s.pg1 - s.pg0 + 1) / 2;
-    alive = do_s(0);
-    if (alive && T == 1 && lane == 0) tc_commit(cx.bar(kBarQEmpty));
+    alive = do_s(0, qb);
+    if (alive && T == 1 && lane == 0) tc_commit(cx.bar(kBarQEmpty + qb));
     for (int t = 1; alive && t < T; ++t) {
-      alive = do_s(t);
-      if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(kBarQEmpty));
+      alive = do_s(t, qb);
+      if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(kBarQEmpty + qb));
       __syncwarp();
       if (alive) alive = do_pv(s, t - 1, t == 1);
     }
@@ -586,9 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(base + L.bars + 8 * (kBarFull + i), 1);
       mbar_init(base + L.bars + 8 * (kBarEmpty + i), 1);
     }
-    mbar_init(base + L.bars + 8 * kBarQFull, 1);
-    mbar_init(base + L.bars + 8 * kBarQEmpty, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(base + L.bars + 8 * (kBarQFull + i), 1);
+      mbar_init(base + L.bars + 8 * (kBarQEmpty + i), 1);
       mbar_init(base + L.bars + 8 * (kBarSFull + i), 1);
       mbar_init(base + L.bars + 8 * (kBarSEmpty + i), kSoftmaxThreads);
       mbar_init(base + L.bars + 8 * (kBarPFull + i), kSoftmaxThreads);
