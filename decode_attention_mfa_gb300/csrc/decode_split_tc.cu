@@ -1,5 +1,6 @@
-// decode_split_tc.cu -- split-KV MFA decode for a bf16 paged cache on the
-// 5th-generation tensor cores (tcgen05, TMEM accumulators) with TMA streaming.
+// decode_split_tc.cu -- split-KV MFA decode on the 5th-generation tensor cores
+// (tcgen05, TMEM accumulators) with TMA streaming, for a bf16 cache and for an
+// FP8-E4M3 cache with per-token fp32 scales.
 //
 // MFA ("Step-3 is Large yet Affordable", paper summary page, section 2 /
 // Table 1) gives all 64 query heads one shared K head and one shared V head
@@ -17,77 +18,126 @@
 // normalised partial result plus its natural-log LSE per sequence piece into
 // slot c + b); the LSE combine kernel merges the pieces.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (one CTA per SM):
 //   warps 0-3  softmax: TMEM lane = token of the tile; online softmax in fp32
 //              with a lazily updated reference maximum (only when a logit
-//              exceeds it by 2^8 are P, the row sums and O^T rescaled); then
-//              the epilogue (row-sum reduction, O^T / l, partial LSE).
-//   warp 4     producer: page-table walk, TMA loads of Q and of K/V chunks
-//              (16 KB: a 64-dim slice of a 2-page K tile, or a 128-dim slice
-//              of one V page) into a ring of shared-memory slots.
-//   warp 5     MMA issue (lane 0), TMEM allocation, zeroing of the unused
-//              rows of a partial last V page (0 * NaN would poison P.V).
+//              exceeds it by 2^8 are the row sums and O^T rescaled); then the
+//              epilogue (row-sum reduction, O^T / l, partial LSE).
+//   warp 4     producer: page-table walk and TMA loads.
+//   warp 5     MMA issue (lane 0) and TMEM allocation.
+//   warps 6-7  (E4M3 cache only) dequantisation.
+// bf16 cache: the producer loads 16 KB operand chunks (a 64-dim slice of a
+// 2-page K tile, or a 128-dim slice of one V page) straight into a ring of
+// shared-memory slots in the layouts the MMAs read; the MMA warp zeroes the
+// unused rows of a partial last V page (0 * NaN would poison P.V).
+// E4M3 cache ("Step-3 is Large yet Affordable", section 7: 8-bit KV): the
+// producer stages raw code pages (and each tile's per-token scales) and the
+// dequantisation warps turn them into f16 operand chunks of the same layouts
+// (E4M3 -> f16 is exact); the MMAs run as f16 x f16 with Q converted to f16.
+// The K scale multiplies the logits and the V scale is folded into P, both in
+// fp32 in the softmax warps (the row sums use the unscaled P).
 // Every mbarrier wait is bounded (wait budget); on expiry the kernel records
 // MFA_DEVERR_TIMEOUT, the roles stop issuing work and the CTA drains and exits.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "mfa_device.cuh"
 
 namespace mfa {
 namespace {
 
-constexpr int kThreads = 192;
+template <bool kFp8>
+struct Cfg;
+template <>
+struct Cfg<false> {
+  static constexpr int kThreads = 192;
+  static constexpr int kSlots = 7;       // 16 KB operand chunks
+  static constexpr int kStages = 0;      // raw code pages
+  static constexpr int kQBufs = 2;
+  static constexpr int kScaleSlots = 0;  // per-tile scale blocks
+  static constexpr int kAbFormat = 1;    // bf16 operands
+};
+template <>
+struct Cfg<true> {
+  static constexpr int kThreads = 256;
+  static constexpr int kSlots = 3;
+  static constexpr int kStages = 6;
+  static constexpr int kQBufs = 1;
+  static constexpr int kScaleSlots = 4;
+  static constexpr int kAbFormat = 0;    // f16 operands
+};
+
 constexpr int kSoftmaxThreads = 128;
+constexpr int kDequantThreads = 64;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kSlots = 7;                 // 16 KB ring slots
 constexpr int kSlotBytes = 16384;
-constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]; two buffers
-constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads] bf16
+constexpr int kStageBytes = 16384;        // one E4M3 page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
+constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]
+constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads], 16-bit
+constexpr int kScaleBytes = 1024;         // per tile: 128 K scales, then 128 V scales
 constexpr int kTmemCols = 256;            // S^T x2 (64 cols each) + O^T (2 x 64 cols)
+constexpr int kMaxBars = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units: P stays below 2^8
 
-// idesc: bf16 x bf16 -> fp32, M = 128, N = 64.
-constexpr uint32_t kIdescS = idesc_f16(128, 64, 1, 0, 0);  // A = K tile (K-major), B = Q (K-major)
-constexpr uint32_t kIdescO = idesc_f16(128, 64, 1, 1, 1);  // A = V^T (dim-major), B = P^T (head-major)
+template <bool kFp8>
+struct Bars {  // indices into the barrier array
+  using C = Cfg<kFp8>;
+  static constexpr int Full = 0;                     // [kSlots] operand chunk ready
+  static constexpr int Empty = Full + C::kSlots;     // [kSlots] operand chunk consumed
+  static constexpr int QFull = Empty + C::kSlots;    // [2] Q landed
+  static constexpr int QEmpty = QFull + 2;           // [2] every S MMA of the piece done
+  static constexpr int QReady = QEmpty + 2;          // [2] Q converted to f16 (E4M3 only)
+  static constexpr int SFull = QReady + 2;           // [2]
+  static constexpr int SEmpty = SFull + 2;           // [2]
+  static constexpr int PFull = SEmpty + 2;           // [2]
+  static constexpr int PEmpty = PFull + 2;           // [2]
+  static constexpr int OReady = PEmpty + 2;          // one completion per P.V
+  static constexpr int OFree = OReady + 1;           // one completion per epilogue
+  static constexpr int Drain = OFree + 1;
+  static constexpr int StFull = Drain + 1;           // [kStages] raw page landed
+  static constexpr int StEmpty = StFull + C::kStages;   // [kStages] raw page converted
+  static constexpr int ScFull = StEmpty + C::kStages;   // [kScaleSlots]
+  static constexpr int ScEmpty = ScFull + C::kScaleSlots;
+  static constexpr int Count = ScEmpty + C::kScaleSlots;
+  static_assert(Count <= kMaxBars, "barrier array too small");
+};
+
+template <bool kFp8>
+__host__ __device__ constexpr uint32_t idesc_s() {  // A = K tile (K-major), B = Q (K-major)
+  return idesc_f16(128, 64, Cfg<kFp8>::kAbFormat, 0, 0);
+}
+template <bool kFp8>
+__host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = P^T (head-major)
+  return idesc_f16(128, 64, Cfg<kFp8>::kAbFormat, 1, 1);
+}
 
 struct SmemLayout {
-  uint32_t ring, q, p;  // byte offsets from the 1024-aligned base
+  uint32_t ring, stage, q, p, scales;  // byte offsets from the 1024-aligned base
   uint32_t len, prefix, red, flags, bars, misc;
   uint32_t total;
 };
 
+template <bool kFp8>
 __host__ __device__ inline SmemLayout smem_layout(int B) {
+  using C = Cfg<kFp8>;
   SmemLayout L;
   L.ring = 0;
-  L.q = L.ring + kSlots * kSlotBytes;
-  L.p = L.q + 2 * kQBytes;
-  L.len = L.p + 2 * kPBytes;
+  L.stage = L.ring + C::kSlots * kSlotBytes;
+  L.q = L.stage + C::kStages * kStageBytes;
+  L.p = L.q + C::kQBufs * kQBytes;
+  L.scales = L.p + 2 * kPBytes;
+  L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
   L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64]
   L.flags = L.red + 6 * 64 * 4;                   // int flags[2][4]
   L.bars = (L.flags + 32 + 7) & ~7u;              // mbarriers
-  L.misc = L.bars + 8 * 48;                       // tmem base, abort flag
+  L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
   L.total = L.misc + 16;
   return L;
 }
-
-// Barrier indices inside the barrier array.
-enum : int {
-  kBarFull = 0,                 // [kSlots]
-  kBarEmpty = kBarFull + kSlots,  // [kSlots]
-  kBarQFull = kBarEmpty + kSlots,  // [2]
-  kBarQEmpty = kBarQFull + 2,       // [2]
-  kBarSFull = kBarQEmpty + 2,       // [2]
-  kBarSEmpty = kBarSFull + 2,   // [2]
-  kBarPFull = kBarSEmpty + 2,   // [2]
-  kBarPEmpty = kBarPFull + 2,   // [2]
-  kBarOReady = kBarPEmpty + 2,
-  kBarOFree,
-  kBarDrain,
-  kNumBars
-};
-static_assert(kNumBars <= 48, "barrier array too small");
 
 struct Ctx {
   uint32_t base;      // shared address of the aligned dynamic smem base
@@ -107,8 +157,7 @@ __device__ __forceinline__ void named_barrier_softmax() {
 struct Seg {
   int b, pg0, pg1, len;
 };
-__device__ __forceinline__ bool seg_first(const int* s_prefix, const int* s_len, int B, long long lo, long long hi,
-                                          Seg& s) {
+__device__ __forceinline__ bool seg_first(const int* s_prefix, int B, long long lo, long long hi, Seg& s) {
   if (lo >= hi) return false;
   s.b = seq_of_page(s_prefix, B, lo) - 1;
   return true;
@@ -126,6 +175,8 @@ __device__ __forceinline__ bool seg_next(const int* s_prefix, const int* s_len, 
   }
   return false;
 }
+__device__ __forceinline__ int tiles_of(const Seg& s) { return (s.pg1 - s.pg0 + 1) / 2; }
+__device__ __forceinline__ int pages_in_tile(const Seg& s, int t) { return (s.pg0 + 2 * t + 1 < s.pg1) ? 2 : 1; }
 
 // ---------------------------------------------------------------- producer
 // Page ids of one sequence piece for the producer warp: a window of 64 ids
@@ -166,26 +217,35 @@ struct PageIds {
 };
 
 // The whole producer warp runs this loop (uniform control flow); lane 0
-// issues the copies.
+// issues the copies. Per piece: Q, then the chunks of K(0), then for each
+// tile t >= 1 those of K(t) and V(t-1), then V(T-1) -- the order in which the
+// MMA warp consumes them (bf16), or in which the dequantisation warps convert
+// them (E4M3: raw pages, with each tile's scales next to its K pages).
+template <bool kFp8>
 __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               const CUtensorMap* qmap, const Ctx& cx, const int* s_prefix, const int* s_len,
                               long long lo, long long hi) {
+  using C = Cfg<kFp8>;
+  using Bb = Bars<kFp8>;
   const int lane = threadIdx.x & 31;
   const uint64_t pol_stream = policy_evict_first();
   const uint64_t pol_keep = policy_evict_last();
-  const uint32_t q_base = cx.base + smem_layout(p.B).q;
-  uint32_t cc = 0, seg_i = 0;
+  const SmemLayout L = smem_layout<kFp8>(p.B);
+  uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged pages (E4M3); pieces; tiles
   Seg s;
-  bool ok = seg_first(s_prefix, s_len, p.B, lo, hi, s);
+  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
+  constexpr int kRing = kFp8 ? C::kStages : C::kSlots;
+  constexpr int kRingFull = kFp8 ? Bb::StFull : Bb::Full;
+  constexpr int kRingEmpty = kFp8 ? Bb::StEmpty : Bb::Empty;
   auto wait_slot = [&](uint32_t& dst, uint32_t& bar) -> bool {
-    const uint32_t slot = cc % kSlots, n = cc / kSlots;
-    const bool r = cx.wait(kBarEmpty + slot, (n & 1) ^ 1);
+    const uint32_t slot = cc % kRing, n = cc / kRing;
+    const bool r = cx.wait(kRingEmpty + slot, (n & 1) ^ 1);
     __syncwarp();
-    dst = cx.base + slot * kSlotBytes;
-    bar = cx.bar(kBarFull + slot);
+    dst = cx.base + (kFp8 ? L.stage + slot * kStageBytes : L.ring + slot * kSlotBytes);
+    bar = cx.bar(kRingFull + slot);
     return r;
   };
-  // K dim block d of a tile of pages pa (and pb >= 0)
+  // bf16: K dim block d of a tile of pages pa (and pb >= 0)
   auto issue_k = [&](int d, int pa, int pb) -> bool {
     uint32_t dst, bar;
     if (!wait_slot(dst, bar)) return false;
@@ -197,7 +257,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++cc;
     return true;
   };
-  // V dims [hf*128, hf*128 + 128) of page pv
+  // bf16: V dims [hf*128, hf*128 + 128) of page pv
   auto issue_v = [&](int hf, int pv) -> bool {
     uint32_t dst, bar;
     if (!wait_slot(dst, bar)) return false;
@@ -209,6 +269,38 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++cc;
     return true;
   };
+  // E4M3: one whole raw page (two 128 B-wide boxes) of the K or V cache
+  auto stage_page = [&](const CUtensorMap* map, int pg) -> bool {
+    uint32_t dst, bar;
+    if (!wait_slot(dst, bar)) return false;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
+      tma_load_2d(dst, map, 0, pg * kPageSize, bar, pol_stream);
+      tma_load_2d(dst + 8192, map, 128, pg * kPageSize, bar, pol_stream);
+    }
+    ++cc;
+    return true;
+  };
+  // E4M3: the K and V scales of the tile's pages
+  auto stage_scales = [&](int pa, int pb) -> bool {
+    const uint32_t slot = sc_cnt % C::kScaleSlots, n = sc_cnt / C::kScaleSlots;
+    const bool r = cx.wait(Bb::ScEmpty + slot, (n & 1) ^ 1);
+    __syncwarp();
+    if (!r) return false;
+    if (lane == 0) {
+      const uint32_t dst = cx.base + L.scales + slot * kScaleBytes, bar = cx.bar(Bb::ScFull + slot);
+      const uint32_t per_page = kPageSize * sizeof(float);
+      mbar_arrive_expect_tx(bar, (pb >= 0 ? 4u : 2u) * per_page);
+      bulk_load(dst, p.k_scale + (size_t)pa * kPageSize, per_page, bar);
+      bulk_load(dst + 512, p.v_scale + (size_t)pa * kPageSize, per_page, bar);
+      if (pb >= 0) {
+        bulk_load(dst + per_page, p.k_scale + (size_t)pb * kPageSize, per_page, bar);
+        bulk_load(dst + 512 + per_page, p.v_scale + (size_t)pb * kPageSize, per_page, bar);
+      }
+    }
+    ++sc_cnt;
+    return true;
+  };
   uint32_t last_q_parity = 0, last_qb = 0;
   bool issued_q = false;
   while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
@@ -217,38 +309,45 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ids.row = p.page_table + (size_t)s.b * p.max_pages;
     ids.pg1 = s.pg1;
     ids.start(s.pg0, p, lane);
-    // Q of this sequence into buffer seg_i % 2 (free once every S MMA of the
-    // piece before the previous one is done, so the loads of this piece need
-    // not wait for the previous piece to finish)
-    const uint32_t qb = seg_i & 1;
-    const bool qfree = cx.wait(kBarQEmpty + qb, ((seg_i >> 1) & 1) ^ 1);
+    // Q of this sequence; its buffer is free once every S MMA of the piece that
+    // last used it is done (with two buffers the loads of this piece need not
+    // wait for the previous piece to finish)
+    const uint32_t qb = seg_i % C::kQBufs, qn = seg_i / C::kQBufs;
+    const bool qfree = cx.wait(Bb::QEmpty + qb, (qn & 1) ^ 1);
     __syncwarp();
     if (!qfree) break;
     if (lane == 0) {
-      mbar_arrive_expect_tx(cx.bar(kBarQFull + qb), (uint32_t)kQBytes);
+      const uint32_t q_dst = cx.base + L.q + qb * kQBytes;
+      mbar_arrive_expect_tx(cx.bar(Bb::QFull + qb), (uint32_t)kQBytes);
       for (int d = 0; d < 4; ++d)
-        tma_load_2d(q_base + qb * kQBytes + d * 8192, qmap, d * 64, s.b * kHeads, cx.bar(kBarQFull + qb), pol_keep);
+        tma_load_2d(q_dst + d * 8192, qmap, d * 64, s.b * kHeads, cx.bar(Bb::QFull + qb), pol_keep);
     }
     issued_q = true;
-    last_q_parity = (seg_i >> 1) & 1;
+    last_q_parity = qn & 1;
     last_qb = qb;
     ++seg_i;
-    const int T = (s.pg1 - s.pg0 + 1) / 2;
+    const int T = tiles_of(s);
     bool good = true;
-    // chunk order: K(0), then K(t), V(t-1) for t = 1..T-1, then V(T-1)
     for (int t = 0; good && t <= T; ++t) {
       if (t < T) {
         const int pga = s.pg0 + 2 * t;
         const int pa = ids.get(pga, p, lane);
-        const int pb = (pga + 1 < s.pg1) ? ids.get(pga + 1, p, lane) : -1;
-        for (int d = 0; good && d < 4; ++d) good = issue_k(d, pa, pb);
+        const int pb = (pages_in_tile(s, t) == 2) ? ids.get(pga + 1, p, lane) : -1;
+        if constexpr (kFp8) {
+          good = stage_page(kmap, pa) && (pb < 0 || stage_page(kmap, pb)) && stage_scales(pa, pb);
+        } else {
+          for (int d = 0; good && d < 4; ++d) good = issue_k(d, pa, pb);
+        }
       }
       if (good && t > 0) {
         const int pgv = s.pg0 + 2 * (t - 1);
-        const int np = (pgv + 1 < s.pg1) ? 2 : 1;
+        const int np = pages_in_tile(s, t - 1);
         for (int i = 0; good && i < np; ++i) {
           const int pv = ids.get(pgv + i, p, lane);
-          good = issue_v(0, pv) && issue_v(1, pv);
+          if constexpr (kFp8)
+            good = stage_page(vmap, pv);
+          else
+            good = issue_v(0, pv) && issue_v(1, pv);
         }
       }
     }
@@ -256,21 +355,167 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   }
   // drain: every copy this warp issued must land before the CTA exits
   if (lane == 0) {
-    for (uint32_t k = (cc > (uint32_t)kSlots ? cc - kSlots : 0); k < cc; ++k)
-      (void)mbar_wait(cx.bar(kBarFull + k % kSlots), (k / kSlots) & 1, cx.budget, nullptr, p.err);
-    if (issued_q) (void)mbar_wait(cx.bar(kBarQFull + last_qb), last_q_parity, cx.budget, nullptr, p.err);
+    for (uint32_t k = (cc > (uint32_t)kRing ? cc - kRing : 0); k < cc; ++k)
+      (void)mbar_wait(cx.bar(kRingFull + k % kRing), (k / kRing) & 1, cx.budget, nullptr, p.err);
+    if constexpr (kFp8) {
+      for (uint32_t k = (sc_cnt > (uint32_t)C::kScaleSlots ? sc_cnt - C::kScaleSlots : 0); k < sc_cnt; ++k)
+        (void)mbar_wait(cx.bar(Bb::ScFull + k % C::kScaleSlots), (k / C::kScaleSlots) & 1, cx.budget, nullptr,
+                        p.err);
+    }
+    if (issued_q) (void)mbar_wait(cx.bar(Bb::QFull + last_qb), last_q_parity, cx.budget, nullptr, p.err);
   }
   __syncwarp();
 }
 
+// ---------------------------------------------------------------- dequantisation (E4M3)
+// Raw pages arrive as two 128 B-wide boxes with the 128-byte swizzle: row r,
+// 16 B piece j of box h sits at h*8192 + r*128 + ((j ^ (r & 7)) << 4). Each
+// piece (16 codes) becomes two 16 B pieces of f16 in the operand layouts.
+__device__ __forceinline__ void codes16_to_f16(const uint4 raw, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i] >> (16 * k)) & 0xFFFFu),
+                                                        __NV_E4M3);
+      o[2 * i + k] = (uint32_t)h2.x | ((uint32_t)h2.y << 16);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t sw_piece(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+// Bf16 Q (TMA, 128-byte swizzle) -> f16 in place: same element positions.
+__device__ __forceinline__ void convert_q_to_f16(uint32_t q_addr, int tid) {
+  for (int i = tid; i < kQBytes / 16; i += kDequantThreads) {
+    const uint4 v = ld_shared_v4(q_addr + 16 * i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+      o[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    st_shared_v4(q_addr + 16 * i, make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
+__device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_prefix, const int* s_len,
+                             long long lo, long long hi) {
+  using C = Cfg<true>;
+  using Bb = Bars<true>;
+  const int tid = threadIdx.x - 6 * 32;  // 0..63
+  const SmemLayout L = smem_layout<true>(p.B);
+  uint32_t st = 0, cc = 0, seg_i = 0;    // staged pages consumed, operand chunks produced, pieces
+  Seg s;
+  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
+  auto stage_addr = [&](uint32_t k) { return cx.base + L.stage + (k % C::kStages) * kStageBytes; };
+  auto wait_stage = [&](uint32_t k) -> bool { return cx.wait(Bb::StFull + k % C::kStages, (k / C::kStages) & 1); };
+  auto release_stage = [&](uint32_t k) { mbar_arrive(cx.bar(Bb::StEmpty + k % C::kStages)); };
+  // claim the next operand slot; returns its address
+  auto begin_chunk = [&](uint32_t& dst) -> bool {
+    const uint32_t slot = cc % C::kSlots, n = cc / C::kSlots;
+    if (!cx.wait(Bb::Empty + slot, (n & 1) ^ 1)) return false;
+    dst = cx.base + L.ring + slot * kSlotBytes;
+    return true;
+  };
+  auto end_chunk = [&]() {
+    fence_proxy_async_smem();  // the MMA reads the chunk through the async proxy
+    mbar_arrive(cx.bar(Bb::Full + cc % C::kSlots));
+    ++cc;
+  };
+  while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
+    if (*cx.abort) return;
+    // Q of this piece: bf16 -> f16
+    if (!cx.wait(Bb::QFull, seg_i & 1)) return;
+    convert_q_to_f16(cx.base + L.q, tid);
+    fence_proxy_async_smem();
+    mbar_arrive(cx.bar(Bb::QReady));
+    ++seg_i;
+    const int T = tiles_of(s);
+    for (int t = 0; t <= T; ++t) {
+      if (t < T) {
+        // K(t): chunk d = dims [64d, 64d + 64) of the tile's 128 rows
+        const int np = pages_in_tile(s, t);
+        const uint32_t ka = st, kb = st + 1;
+        if (!wait_stage(ka) || (np == 2 && !wait_stage(kb))) return;
+        for (int d = 0; d < 4; ++d) {
+          uint32_t dst;
+          if (!begin_chunk(dst)) return;
+          for (int pi = 0; pi < np; ++pi) {
+            const uint32_t src = stage_addr(pi ? kb : ka) + (d >> 1) * 8192;
+            const int r = tid, orow = pi * 64 + tid;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j = (d & 1) * 4 + u;
+              uint4 lo16, hi16;
+              codes16_to_f16(ld_shared_v4(src + sw_piece(r, j)), lo16, hi16);
+              st_shared_v4(dst + sw_piece(orow, 2 * u), lo16);
+              st_shared_v4(dst + sw_piece(orow, 2 * u + 1), hi16);
+            }
+          }
+          end_chunk();
+        }
+        release_stage(ka);
+        if (np == 2) release_stage(kb);
+        st += np;
+      }
+      if (t > 0) {
+        // V(t-1): per page, chunk hf = dims [128hf, 128hf + 128) as two 64-dim blocks
+        const int np = pages_in_tile(s, t - 1);
+        const int pgv = s.pg0 + 2 * (t - 1);
+        for (int pi = 0; pi < np; ++pi) {
+          const uint32_t k = st + pi;
+          if (!wait_stage(k)) return;
+          const int nv = min(kPageSize, s.len - (pgv + pi) * kPageSize);  // valid rows of this page
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t dst;
+            if (!begin_chunk(dst)) return;
+            const uint32_t src = stage_addr(k) + hf * 8192;
+            const int r = tid;
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint4 lo16 = make_uint4(0u, 0u, 0u, 0u), hi16 = lo16;
+                if (r < nv) codes16_to_f16(ld_shared_v4(src + sw_piece(r, blk * 4 + u)), lo16, hi16);
+                st_shared_v4(dst + blk * 8192 + sw_piece(r, 2 * u), lo16);
+                st_shared_v4(dst + blk * 8192 + sw_piece(r, 2 * u + 1), hi16);
+              }
+            }
+            end_chunk();
+          }
+          release_stage(k);
+        }
+        st += np;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- MMA issue
+template <bool kFp8>
 __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_prefix, const int* s_len, long long lo,
                          long long hi, uint32_t tmem) {
+  using C = Cfg<kFp8>;
+  using Bb = Bars<kFp8>;
   const int lane = threadIdx.x & 31;
-  const SmemLayout L = smem_layout(p.B);
+  const SmemLayout L = smem_layout<kFp8>(p.B);
   uint32_t cc = 0, seg_i = 0, s_cnt = 0, p_cnt = 0;
   Seg s;
-  bool ok = seg_first(s_prefix, s_len, p.B, lo, hi, s);
+  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
   bool alive = true;
 
   auto wait_all = [&](int bar, uint32_t parity) -> bool {
@@ -278,51 +523,49 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
     __syncwarp();
     return r;
   };
-  auto do_s = [&](int t_in_seg, uint32_t qb) -> bool {
+  auto do_s = [&](uint32_t qb) -> bool {
     const uint32_t buf = s_cnt & 1, n = s_cnt >> 1;
-    if (!wait_all(kBarSEmpty + buf, (n & 1) ^ 1)) return false;
+    if (!wait_all(Bb::SEmpty + buf, (n & 1) ^ 1)) return false;
     const uint32_t d_tmem = tmem + buf * 64;
     for (int d = 0; d < 4; ++d) {
-      const uint32_t slot = cc % kSlots, ph = (cc / kSlots) & 1;
-      if (!wait_all(kBarFull + slot, ph)) return false;
+      const uint32_t slot = cc % C::kSlots, ph = (cc / C::kSlots) & 1;
+      if (!wait_all(Bb::Full + slot, ph)) return false;
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t a0 = cx.base + slot * kSlotBytes;
+        const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
         const uint32_t b0 = cx.base + L.q + qb * kQBytes + d * 8192;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma(d_tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024), kIdescS,
-                 (d | kk) != 0);
-        tc_commit(cx.bar(kBarEmpty + slot));
+          tc_mma(d_tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024),
+                 idesc_s<kFp8>(), (d | kk) != 0);
+        tc_commit(cx.bar(Bb::Empty + slot));
       }
       __syncwarp();
       ++cc;
     }
-    if (lane == 0) tc_commit(cx.bar(kBarSFull + buf));
+    if (lane == 0) tc_commit(cx.bar(Bb::SFull + buf));
     __syncwarp();
     ++s_cnt;
-    (void)t_in_seg;
     return true;
   };
   auto do_pv = [&](const Seg& sg, int t, bool first_of_seg) -> bool {
     const uint32_t buf = p_cnt & 1, n = p_cnt >> 1;
-    if (first_of_seg && !wait_all(kBarOFree, (seg_i & 1) ^ 1)) return false;
-    if (!wait_all(kBarPFull + buf, n & 1)) return false;
+    if (first_of_seg && !wait_all(Bb::OFree, (seg_i & 1) ^ 1)) return false;
+    if (!wait_all(Bb::PFull + buf, n & 1)) return false;
     const int pga = sg.pg0 + 2 * t;
-    const int np = (pga + 1 < sg.pg1) ? 2 : 1;
+    const int np = pages_in_tile(sg, t);
     for (int i = 0; i < np; ++i) {
       const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page
       for (int hf = 0; hf < 2; ++hf) {
-        const uint32_t slot = cc % kSlots, ph = (cc / kSlots) & 1;
-        if (!wait_all(kBarFull + slot, ph)) return false;
-        const uint32_t a0 = cx.base + slot * kSlotBytes;
-        if (nv < kPageSize) {
+        const uint32_t slot = cc % C::kSlots, ph = (cc / C::kSlots) & 1;
+        if (!wait_all(Bb::Full + slot, ph)) return false;
+        const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
+        if (!kFp8 && nv < kPageSize) {
           // rows [nv, 64) of both 64-dim blocks: 128 B each, 16 B per lane and step
           const int nbytes = (kPageSize - nv) * 128;
           for (int off = lane * 16; off < 2 * nbytes; off += 32 * 16) {
             const int blk = off / nbytes, r = off % nbytes;
-            const uint32_t addr = a0 + blk * 8192 + nv * 128 + r;
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+            st_shared_v4(a0 + blk * 8192 + nv * 128 + r, make_uint4(0u, 0u, 0u, 0u));
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -333,16 +576,17 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc_mma(tmem + 128 + hf * 64, smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
-                   smem_desc_sw128(bp + kk * 2048, 8192, 1024), kIdescO, !(first_of_seg && i == 0 && kk == 0));
-          tc_commit(cx.bar(kBarEmpty + slot));
+                   smem_desc_sw128(bp + kk * 2048, 8192, 1024), idesc_o<kFp8>(),
+                   !(first_of_seg && i == 0 && kk == 0));
+          tc_commit(cx.bar(Bb::Empty + slot));
         }
         __syncwarp();
         ++cc;
       }
     }
     if (lane == 0) {
-      tc_commit(cx.bar(kBarPEmpty + buf));
-      tc_commit(cx.bar(kBarOReady));
+      tc_commit(cx.bar(Bb::PEmpty + buf));
+      tc_commit(cx.bar(Bb::OReady));
     }
     __syncwarp();
     ++p_cnt;
@@ -350,14 +594,14 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
   };
 
   while (alive && ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
-    const uint32_t qb = seg_i & 1;
-    if (!wait_all(kBarQFull + qb, (seg_i >> 1) & 1)) break;
-    const int T = (s.pg1 - s.pg0 + 1) / 2;
-    alive = do_s(0, qb);
-    if (alive && T == 1 && lane == 0) tc_commit(cx.bar(kBarQEmpty + qb));
+    const uint32_t qb = seg_i % C::kQBufs, qn = seg_i / C::kQBufs;
+    if (!wait_all((kFp8 ? Bb::QReady : Bb::QFull) + qb, qn & 1)) break;
+    const int T = tiles_of(s);
+    alive = do_s(qb);
+    if (alive && T == 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
     for (int t = 1; alive && t < T; ++t) {
-      alive = do_s(t, qb);
-      if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(kBarQEmpty + qb));
+      alive = do_s(qb);
+      if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
       __syncwarp();
       if (alive) alive = do_pv(s, t - 1, t == 1);
     }
@@ -366,8 +610,8 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
   }
   // drain: wait for every MMA this thread issued before TMEM is released
   if (lane == 0) {
-    tc_commit(cx.bar(kBarDrain));
-    (void)mbar_wait(cx.bar(kBarDrain), 0, cx.budget, nullptr, p.err);
+    tc_commit(cx.bar(Bb::Drain));
+    (void)mbar_wait(cx.bar(Bb::Drain), 0, cx.budget, nullptr, p.err);
   }
   __syncwarp();
 }
@@ -404,12 +648,12 @@ __device__ __forceinline__ void warp_reduce_scatter_sum(float (&v)[64], int lane
   }
 }
 
-__device__ __forceinline__ void load_logits(uint32_t taddr, bool valid, float c2, float (&x)[64]) {
+__device__ __forceinline__ void load_logits(uint32_t taddr, bool valid, float mult, float (&x)[64]) {
   tmem_ld32(taddr, x);
   tmem_ld32(taddr + 32, x + 32);
   tc_wait_ld();
 #pragma unroll
-  for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * c2 : -INFINITY;
+  for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * mult : -INFINITY;
 }
 
 // O^T columns (this thread's TMEM lane, both 128-dim halves) times col_scale[h].
@@ -429,11 +673,25 @@ __device__ __forceinline__ void scale_o_columns(uint32_t taddr_o, const float* c
   tc_wait_st();
 }
 
+template <bool kFp8>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (kFp8) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+template <bool kFp8>
 __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_prefix, const int* s_len,
                              long long lo, long long hi, uint32_t tmem, int c, uint8_t* gbase) {
+  using C = Cfg<kFp8>;
+  using Bb = Bars<kFp8>;
   const int tid = threadIdx.x;  // 0..127: TMEM lane = token of the tile = dim of each O^T half
   const int warp = tid >> 5, lane = tid & 31;
-  const SmemLayout L = smem_layout(p.B);
+  const SmemLayout L = smem_layout<kFp8>(p.B);
   float* red = reinterpret_cast<float*>(gbase + L.red);  // [4][64] per-warp partial reductions
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
   float* alpha = mref + 64;                              // [64] rescale factors / 1/l, uniform
@@ -449,13 +707,13 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   uint32_t o_seen = 0;
   auto observe_pv = [&](uint32_t k) -> bool {
     while (o_seen <= k) {
-      if (!cx.wait(kBarOReady, o_seen & 1)) return false;
+      if (!cx.wait(Bb::OReady, o_seen & 1)) return false;
       ++o_seen;
     }
     return true;
   };
   Seg s;
-  bool ok = seg_first(s_prefix, s_len, p.B, lo, hi, s);
+  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
 
   while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
     if (tid < 64) mref[tid] = -INFINITY;
@@ -463,17 +721,28 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     float lp[64];  // this thread's share of the softmax denominators
 #pragma unroll
     for (int h = 0; h < 64; ++h) lp[h] = 0.0f;
-    const int T = (s.pg1 - s.pg0 + 1) / 2;
+    const int T = tiles_of(s);
     for (int t = 0; t < T; ++t) {
       const int tok0 = (s.pg0 + 2 * t) * kPageSize;
-      const int np = (s.pg0 + 2 * t + 1 < s.pg1) ? 2 : 1;
-      const bool valid = tid < min(np * kPageSize, s.len - tok0);
+      const bool valid = tid < min(pages_in_tile(s, t) * kPageSize, s.len - tok0);
+      // E4M3: this token's K and V scales (the tile's scale block, slot = tile count)
+      float kmul = c2, vmul = 1.0f;
+      if constexpr (kFp8) {
+        const uint32_t slot = p_cnt % C::kScaleSlots;
+        if (!cx.wait(Bb::ScFull + slot, (p_cnt / C::kScaleSlots) & 1)) return;
+        const float* sc = reinterpret_cast<const float*>(gbase + L.scales + slot * kScaleBytes);
+        if (valid) {
+          kmul = c2 * sc[tid];
+          vmul = sc[128 + tid];
+        }
+        mbar_arrive(cx.bar(Bb::ScEmpty + slot));
+      }
       const uint32_t sbuf = s_cnt & 1;
       const uint32_t taddr_s = tmem + lane_base + sbuf * 64;
-      if (!cx.wait(kBarSFull + sbuf, (s_cnt >> 1) & 1)) return;
+      if (!cx.wait(Bb::SFull + sbuf, (s_cnt >> 1) & 1)) return;
       tc_fence_after();
       float x[64];
-      load_logits(taddr_s, valid, c2, x);
+      load_logits(taddr_s, valid, kmul, x);
       bool mine = false;
 #pragma unroll
       for (int h = 0; h < 64; ++h) mine |= x[h] > mref[h] + kRescaleThreshold;
@@ -506,12 +775,12 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
           tc_fence_after();
           scale_o_columns(taddr_o, alpha);
         }
-        load_logits(taddr_s, valid, c2, x);
+        load_logits(taddr_s, valid, kmul, x);
       }
       tc_fence_before();
-      mbar_arrive(cx.bar(kBarSEmpty + sbuf));  // S^T buffer free for the tile after next
+      mbar_arrive(cx.bar(Bb::SEmpty + sbuf));  // S^T buffer free for the tile after next
       ++s_cnt;
-      // ---- P = exp2(x - mref): row sums in fp32, P^T row in bf16
+      // ---- P = exp2(x - mref): row sums in fp32; P^T row (times the V scale) in 16 bits
       uint32_t packed[32];
 #pragma unroll
       for (int h = 0; h < 64; h += 2) {
@@ -519,23 +788,19 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         const float p1 = exp2f(x[h + 1] - mref[h + 1]);
         lp[h] += p0;
         lp[h + 1] += p1;
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-        packed[h >> 1] = *reinterpret_cast<uint32_t*>(&b2);
+        packed[h >> 1] = kFp8 ? pack2<kFp8>(p0 * vmul, p1 * vmul) : pack2<kFp8>(p0, p1);
       }
       const uint32_t pbuf = p_cnt & 1;
       if (p_cnt > 0 && !observe_pv(p_cnt - 1)) return;
-      if (!cx.wait(kBarPEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
+      if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
       const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t addr = prow + ((j ^ (tid & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[4 * j]),
-                     "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]), "r"(packed[4 * j + 3])
-                     : "memory");
-      }
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(prow + ((j ^ (tid & 7)) << 4),
+                     make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]));
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(cx.bar(kBarPFull + pbuf));
+      mbar_arrive(cx.bar(Bb::PFull + pbuf));
       ++p_cnt;
       ++tile_i;
     }
@@ -568,40 +833,54 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       }
     }
     tc_fence_before();
-    mbar_arrive(cx.bar(kBarOFree));
+    mbar_arrive(cx.bar(Bb::OFree));
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kFp8>
+__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     decode_split_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap) {
+  using C = Cfg<kFp8>;
+  using Bb = Bars<kFp8>;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   const uint32_t raw = smem_u32(dyn_smem);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = dyn_smem + (base - raw);
-  const SmemLayout L = smem_layout(p.B);
+  const SmemLayout L = smem_layout<kFp8>(p.B);
   int* s_len = reinterpret_cast<int*>(gbase + L.len);
   int* s_prefix = reinterpret_cast<int*>(gbase + L.prefix);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.misc);
   int* abort_flag = reinterpret_cast<int*>(gbase + L.misc + 4);
   const int warp = threadIdx.x >> 5;
+  const uint32_t bars = base + L.bars;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(base + L.bars + 8 * (kBarFull + i), 1);
-      mbar_init(base + L.bars + 8 * (kBarEmpty + i), 1);
+    const uint32_t full_count = kFp8 ? kDequantThreads : 1;  // dequantisation warps or the TMA transaction
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(bars + 8 * (Bb::Full + i), full_count);
+      mbar_init(bars + 8 * (Bb::Empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(base + L.bars + 8 * (kBarQFull + i), 1);
-      mbar_init(base + L.bars + 8 * (kBarQEmpty + i), 1);
-      mbar_init(base + L.bars + 8 * (kBarSFull + i), 1);
-      mbar_init(base + L.bars + 8 * (kBarSEmpty + i), kSoftmaxThreads);
-      mbar_init(base + L.bars + 8 * (kBarPFull + i), kSoftmaxThreads);
-      mbar_init(base + L.bars + 8 * (kBarPEmpty + i), 1);
+      mbar_init(bars + 8 * (Bb::QFull + i), 1);
+      mbar_init(bars + 8 * (Bb::QEmpty + i), 1);
+      mbar_init(bars + 8 * (Bb::QReady + i), kDequantThreads);
+      mbar_init(bars + 8 * (Bb::SFull + i), 1);
+      mbar_init(bars + 8 * (Bb::SEmpty + i), kSoftmaxThreads);
+      mbar_init(bars + 8 * (Bb::PFull + i), kSoftmaxThreads);
+      mbar_init(bars + 8 * (Bb::PEmpty + i), 1);
     }
-    mbar_init(base + L.bars + 8 * kBarOReady, 1);
-    mbar_init(base + L.bars + 8 * kBarOFree, kSoftmaxThreads);
-    mbar_init(base + L.bars + 8 * kBarDrain, 1);
+    mbar_init(bars + 8 * Bb::OReady, 1);
+    mbar_init(bars + 8 * Bb::OFree, kSoftmaxThreads);
+    mbar_init(bars + 8 * Bb::Drain, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(bars + 8 * (Bb::StFull + i), 1);
+      mbar_init(bars + 8 * (Bb::StEmpty + i), kDequantThreads);
+    }
+    for (int i = 0; i < C::kScaleSlots; ++i) {
+      mbar_init(bars + 8 * (Bb::ScFull + i), 1);
+      mbar_init(bars + 8 * (Bb::ScEmpty + i), kSoftmaxThreads);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -626,14 +905,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long P = s_prefix[p.B];
   const int c = blockIdx.x;
   const long long lo = cta_page_lo(c, P, p.grid), hi = cta_page_lo(c + 1, P, p.grid);
-  Ctx cx{base, base + L.bars, abort_flag, p.err, p.wait_budget_ns};
+  Ctx cx{base, bars, abort_flag, p.err, p.wait_budget_ns};
 
   if (warp < 4) {
-    softmax_role(p, cx, s_prefix, s_len, lo, hi, tmem, c, gbase);
+    softmax_role<kFp8>(p, cx, s_prefix, s_len, lo, hi, tmem, c, gbase);
   } else if (warp == kProducerWarp) {
-    producer_role(p, &kmap, &vmap, &qmap, cx, s_prefix, s_len, lo, hi);
-  } else {
-    mma_role(p, cx, s_prefix, s_len, lo, hi, tmem);
+    producer_role<kFp8>(p, &kmap, &vmap, &qmap, cx, s_prefix, s_len, lo, hi);
+  } else if (warp == kMmaWarp) {
+    mma_role<kFp8>(p, cx, s_prefix, s_len, lo, hi, tmem);
+  } else if constexpr (kFp8) {
+    dequant_role(p, cx, s_prefix, s_len, lo, hi);
   }
   tc_fence_before();
   __syncthreads();
@@ -642,21 +923,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
 }
 
-}  // namespace
-
-size_t decode_split_tc_smem_bytes(int B) { return (size_t)smem_layout(B).total + 1024; }
-
-cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                   const CUtensorMap& qmap, cudaStream_t stream) {
-  const size_t smem = decode_split_tc_smem_bytes(p.B);
+template <bool kFp8>
+cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                      const CUtensorMap& qmap, cudaStream_t stream) {
+  const size_t smem = (size_t)smem_layout<kFp8>(p.B).total + 1024;
   static int configured_bytes = 0;  // largest opt-in set so far (per process; one device family)
   if ((int)smem > configured_bytes) {
     const cudaError_t e =
-        cudaFuncSetAttribute(decode_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(decode_split_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured_bytes = (int)smem;
   }
-  return launch_pdl(decode_split_tc_kernel, dim3(p.grid), dim3(kThreads), smem, stream, p, kmap, vmap, qmap);
+  return launch_pdl(decode_split_tc_kernel<kFp8>, dim3(p.grid), dim3(Cfg<kFp8>::kThreads), smem, stream, p, kmap,
+                    vmap, qmap);
+}
+
+}  // namespace
+
+size_t decode_split_tc_smem_bytes(int B) { return (size_t)smem_layout<false>(B).total + 1024; }
+size_t decode_split_tc_fp8_smem_bytes(int B) { return (size_t)smem_layout<true>(B).total + 1024; }
+
+cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                   const CUtensorMap& qmap, cudaStream_t stream) {
+  return launch_tc<false>(p, kmap, vmap, qmap, stream);
+}
+
+cudaError_t launch_decode_split_tc_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                       const CUtensorMap& qmap, cudaStream_t stream) {
+  return launch_tc<true>(p, kmap, vmap, qmap, stream);
 }
 
 }  // namespace mfa

@@ -124,6 +124,23 @@ mfa_status_t encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows)
   return MFA_OK;
 }
 
+// 2-D byte tensor [rows][256] (E4M3 codes) read in [64 rows x 128 bytes]
+// boxes with the 128-byte swizzle.
+mfa_status_t encode_rows_e4m3(CUtensorMap* map, const void* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  mfa_status_t st = get_encoder(&enc);
+  if (st != MFA_OK) return st;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+  const cuuint32_t box[2] = {128, 64};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MFA_OK;
+}
+
 // ------------------------------------------------------------ common checks
 mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* page_table, const int32_t* seq_lens, const void* out,
@@ -222,7 +239,8 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   mfa_status_t st = current_device(nullptr, &info);
   if (st != MFA_OK) return st;
   if (fp8 && (!k_scale || !v_scale)) return fail(MFA_ERR_INVALID_ARG, "null scale pointer");
-  if (fp8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return fail(MFA_ERR_INVALID_ARG, "misaligned scales");
+  if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
+    return fail(MFA_ERR_INVALID_ARG, "misaligned scales (16 bytes needed)");
   mfa_plan_t plan;
   st = check_decode_args(q, k_cache, v_cache, page_table, seq_lens, out, lse, batch, max_pages, num_pages,
                          max_len_hint, workspace, workspace_bytes, info.num_sms, &plan);
@@ -233,13 +251,15 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   cudaError_t e;
   if (g_prof_start && (e = cudaEventRecordWithFlags(g_prof_start, s, cudaEventRecordExternal)) != cudaSuccess)
     return cuda_fail(e, "profile event record");
+  CUtensorMap kmap, vmap, qmap;
+  const uint64_t rows = (uint64_t)num_pages * kPageSize;
+  if ((st = encode_rows_bf16(&qmap, q, (uint64_t)batch * kHeads)) != MFA_OK) return st;
   if (fp8) {
-    e = launch_decode_split_simt(p, true, s);
+    if ((st = encode_rows_e4m3(&kmap, k_cache, rows)) != MFA_OK || (st = encode_rows_e4m3(&vmap, v_cache, rows)) != MFA_OK)
+      return st;
+    e = launch_decode_split_tc_fp8(p, kmap, vmap, qmap, s);
   } else {
-    CUtensorMap kmap, vmap, qmap;
-    if ((st = encode_rows_bf16(&kmap, k_cache, (uint64_t)num_pages * kPageSize)) != MFA_OK ||
-        (st = encode_rows_bf16(&vmap, v_cache, (uint64_t)num_pages * kPageSize)) != MFA_OK ||
-        (st = encode_rows_bf16(&qmap, q, (uint64_t)batch * kHeads)) != MFA_OK)
+    if ((st = encode_rows_bf16(&kmap, k_cache, rows)) != MFA_OK || (st = encode_rows_bf16(&vmap, v_cache, rows)) != MFA_OK)
       return st;
     e = launch_decode_split_tc(p, kmap, vmap, qmap, s);
   }

@@ -77,7 +77,10 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_split_simt(const DecodeParams& p, bool fp8, cudaStream_t stream);
 cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                    const CUtensorMap& q_map, cudaStream_t stream);
+cudaError_t launch_decode_split_tc_fp8(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                       const CUtensorMap& q_map, cudaStream_t stream);
 size_t decode_split_tc_smem_bytes(int B);
+size_t decode_split_tc_fp8_smem_bytes(int B);
 
 // Host-side services of mfa_api.cu for other entry points of the library.
 void set_last_error_message(const char* msg);

@@ -155,9 +155,11 @@ mfa_status_t mfa_decode_attention(const void* q, const void* k_cache, const void
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* MFA decode attention over an FP8-E4M3 paged cache with per-token fp32
- * scales (k_scale, v_scale [num_pages][64], [device]). The cached value is
- * decode(code) * scale. Queries stay bf16. Everything else as
- * mfa_decode_attention. */
+ * scales (k_scale, v_scale [num_pages][64], [device], 16-byte aligned). The
+ * cached value is decode(code) * scale. Queries stay bf16. The tensor cores
+ * multiply in f16: q is rounded to f16 (exact for 2^-14 <= |q| < 65504) and
+ * P is scaled by the V scale before rounding to f16, which needs
+ * |v| < ~1e5. Everything else as mfa_decode_attention. */
 mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
                                       const float* k_scale, const float* v_scale,
                                       const int32_t* page_table, const int32_t* seq_lens,
