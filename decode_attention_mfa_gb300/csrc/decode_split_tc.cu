@@ -57,9 +57,11 @@ struct Cfg<false> {
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
 };
+constexpr int kDequantThreads = 64;      // E4M3: warps 6.. convert codes to f16
+
 template <>
 struct Cfg<true> {
-  static constexpr int kThreads = 256;
+  static constexpr int kThreads = 192 + kDequantThreads;
   static constexpr int kSlots = 3;
   static constexpr int kStages = 6;
   static constexpr int kQBufs = 1;
@@ -68,7 +70,6 @@ struct Cfg<true> {
 };
 
 constexpr int kSoftmaxThreads = 128;
-constexpr int kDequantThreads = 64;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kSlotBytes = 16384;
@@ -283,7 +284,8 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   };
   // E4M3: the K and V scales of the tile's pages
   auto stage_scales = [&](int pa, int pb) -> bool {
-    const uint32_t slot = sc_cnt % C::kScaleSlots, n = sc_cnt / C::kScaleSlots;
+    constexpr uint32_t kRingSc = C::kScaleSlots > 0 ? C::kScaleSlots : 1;
+    const uint32_t slot = sc_cnt % kRingSc, n = sc_cnt / kRingSc;
     const bool r = cx.wait(Bb::ScEmpty + slot, (n & 1) ^ 1);
     __syncwarp();
     if (!r) return false;
@@ -416,7 +418,7 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
                              long long lo, long long hi) {
   using C = Cfg<true>;
   using Bb = Bars<true>;
-  const int tid = threadIdx.x - 6 * 32;  // 0..63
+  const int tid = threadIdx.x - 6 * 32;  // 0 .. kDequantThreads - 1
   const SmemLayout L = smem_layout<true>(p.B);
   uint32_t st = 0, cc = 0, seg_i = 0;    // staged pages consumed, operand chunks produced, pieces
   Seg s;
@@ -454,16 +456,28 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
         for (int d = 0; d < 4; ++d) {
           uint32_t dst;
           if (!begin_chunk(dst)) return;
-          for (int pi = 0; pi < np; ++pi) {
+          // rows r = tid, tid + kDequantThreads, ... of the 128-row chunk (rows
+          // 64-127 come from the second page); a thread loads all its pieces
+          // before converting any
+          constexpr int kRows = 128 / kDequantThreads;
+          uint4 raw[4 * kRows];
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            const int row = tid + i * kDequantThreads, pi = row >> 6;
             const uint32_t src = stage_addr(pi ? kb : ka) + (d >> 1) * 8192;
-            const int r = tid, orow = pi * 64 + tid;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              raw[4 * i + u] = (pi < np) ? ld_shared_v4(src + sw_piece(row & 63, (d & 1) * 4 + u)) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int j = (d & 1) * 4 + u;
+              const int row = tid + i * kDequantThreads;
               uint4 lo16, hi16;
-              codes16_to_f16(ld_shared_v4(src + sw_piece(r, j)), lo16, hi16);
-              st_shared_v4(dst + sw_piece(orow, 2 * u), lo16);
-              st_shared_v4(dst + sw_piece(orow, 2 * u + 1), hi16);
+              codes16_to_f16(raw[4 * i + u], lo16, hi16);
+              st_shared_v4(dst + sw_piece(row, 2 * u), lo16);
+              st_shared_v4(dst + sw_piece(row, 2 * u + 1), hi16);
             }
           }
           end_chunk();
@@ -483,14 +497,25 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
           for (int hf = 0; hf < 2; ++hf) {
             uint32_t dst;
             if (!begin_chunk(dst)) return;
+            // units (64-dim block, row) = tid, tid + kDequantThreads, ...; rows past
+            // the sequence end become zeros
+            constexpr int kUnits = 128 / kDequantThreads;
             const uint32_t src = stage_addr(k) + hf * 8192;
-            const int r = tid;
+            uint4 raw[4 * kUnits];
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
+            for (int i = 0; i < kUnits; ++i) {
+              const int unit = tid + i * kDequantThreads, blk = unit >> 6, r = unit & 63;
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                raw[4 * i + u] = (r < nv) ? ld_shared_v4(src + sw_piece(r, blk * 4 + u)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < kUnits; ++i) {
+              const int unit = tid + i * kDequantThreads, blk = unit >> 6, r = unit & 63;
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                uint4 lo16 = make_uint4(0u, 0u, 0u, 0u), hi16 = lo16;
-                if (r < nv) codes16_to_f16(ld_shared_v4(src + sw_piece(r, blk * 4 + u)), lo16, hi16);
+                uint4 lo16, hi16;
+                codes16_to_f16(raw[4 * i + u], lo16, hi16);  // code 0 is +0
                 st_shared_v4(dst + blk * 8192 + sw_piece(r, 2 * u), lo16);
                 st_shared_v4(dst + blk * 8192 + sw_piece(r, 2 * u + 1), hi16);
               }
