@@ -13,10 +13,11 @@
 // an M=128 one on sm_103a), and softmax statistics are reduced across the 128
 // TMEM lanes.
 //
-// Work split: the same stream-K page partition as the CUDA-core path (CTA c
-// owns pages [c*P/G, (c+1)*P/G) of the concatenated sequences and writes one
-// normalised partial result plus its natural-log LSE per sequence piece into
-// slot c + b); the LSE combine kernel merges the pieces.
+// Work split: a stream-K partition of cost units (each non-empty sequence
+// costs its pages plus a fixed charge per piece, see build_cost_prefix); CTA
+// c owns units [c*C/G, (c+1)*C/G) and writes one normalised partial result
+// plus its natural-log LSE per sequence piece into slot c + b; the LSE
+// combine kernel merges the pieces.
 //
 // Warp roles (one CTA per SM):
 //   warps 0-3  softmax: TMEM lane = token of the tile; online softmax in fp32
@@ -158,19 +159,22 @@ __device__ __forceinline__ void named_barrier_softmax() {
 struct Seg {
   int b, pg0, pg1, len;
 };
-__device__ __forceinline__ bool seg_first(const int* s_prefix, int B, long long lo, long long hi, Seg& s) {
+__device__ __forceinline__ bool seg_first(const int* s_cost, int B, long long lo, long long hi, Seg& s) {
   if (lo >= hi) return false;
-  s.b = seq_of_page(s_prefix, B, lo) - 1;
+  s.b = seq_of_cost(s_cost, B, lo) - 1;
   return true;
 }
-__device__ __forceinline__ bool seg_next(const int* s_prefix, const int* s_len, int B, long long lo, long long hi,
-                                         Seg& s) {
-  for (int b = s.b + 1; b < B && s_prefix[b] < hi; ++b) {
-    const long long sp0 = s_prefix[b], sp1 = s_prefix[b + 1];
-    if (sp1 == sp0) continue;
+__device__ __forceinline__ bool seg_next(const int* s_cost, const int* s_len, int B, int piece_cost, long long lo,
+                                         long long hi, Seg& s) {
+  for (int b = s.b + 1; b < B && s_cost[b] < hi; ++b) {
+    const int np = pages_of_len(s_len[b]);
+    const long long first = (long long)s_cost[b] + piece_cost;  // cost position of page 0
+    const long long a = lo > first ? lo - first : 0;
+    const long long e = hi - first < np ? hi - first : np;
+    if (np == 0 || a >= e) continue;
     s.b = b;
-    s.pg0 = (int)((sp0 > lo ? sp0 : lo) - sp0);
-    s.pg1 = (int)((sp1 < hi ? sp1 : hi) - sp0);
+    s.pg0 = (int)a;
+    s.pg1 = (int)e;
     s.len = s_len[b];
     return true;
   }
@@ -224,7 +228,7 @@ struct PageIds {
 // them (E4M3: raw pages, with each tile's scales next to its K pages).
 template <bool kFp8>
 __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
-                              const CUtensorMap* qmap, const Ctx& cx, const int* s_prefix, const int* s_len,
+                              const CUtensorMap* qmap, const Ctx& cx, const int* s_cost, const int* s_len,
                               long long lo, long long hi) {
   using C = Cfg<kFp8>;
   using Bb = Bars<kFp8>;
@@ -234,7 +238,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   const SmemLayout L = smem_layout<kFp8>(p.B);
   uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged pages (E4M3); pieces; tiles
   Seg s;
-  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
+  bool ok = seg_first(s_cost, p.B, lo, hi, s);
   constexpr int kRing = kFp8 ? C::kStages : C::kSlots;
   constexpr int kRingFull = kFp8 ? Bb::StFull : Bb::Full;
   constexpr int kRingEmpty = kFp8 ? Bb::StEmpty : Bb::Empty;
@@ -305,7 +309,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   };
   uint32_t last_q_parity = 0, last_qb = 0;
   bool issued_q = false;
-  while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
+  while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
     if (*cx.abort) break;
     PageIds ids;
     ids.row = p.page_table + (size_t)s.b * p.max_pages;
@@ -414,7 +418,7 @@ __device__ __forceinline__ void convert_q_to_f16(uint32_t q_addr, int tid) {
   }
 }
 
-__device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_prefix, const int* s_len,
+__device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len,
                              long long lo, long long hi) {
   using C = Cfg<true>;
   using Bb = Bars<true>;
@@ -422,7 +426,7 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
   const SmemLayout L = smem_layout<true>(p.B);
   uint32_t st = 0, cc = 0, seg_i = 0;    // staged pages consumed, operand chunks produced, pieces
   Seg s;
-  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
+  bool ok = seg_first(s_cost, p.B, lo, hi, s);
   auto stage_addr = [&](uint32_t k) { return cx.base + L.stage + (k % C::kStages) * kStageBytes; };
   auto wait_stage = [&](uint32_t k) -> bool { return cx.wait(Bb::StFull + k % C::kStages, (k / C::kStages) & 1); };
   auto release_stage = [&](uint32_t k) { mbar_arrive(cx.bar(Bb::StEmpty + k % C::kStages)); };
@@ -438,7 +442,7 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
     mbar_arrive(cx.bar(Bb::Full + cc % C::kSlots));
     ++cc;
   };
-  while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
+  while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
     if (*cx.abort) return;
     // Q of this piece: bf16 -> f16
     if (!cx.wait(Bb::QFull, seg_i & 1)) return;
@@ -532,7 +536,7 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
 
 // ---------------------------------------------------------------- MMA issue
 template <bool kFp8>
-__device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_prefix, const int* s_len, long long lo,
+__device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len, long long lo,
                          long long hi, uint32_t tmem) {
   using C = Cfg<kFp8>;
   using Bb = Bars<kFp8>;
@@ -540,7 +544,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
   const SmemLayout L = smem_layout<kFp8>(p.B);
   uint32_t cc = 0, seg_i = 0, s_cnt = 0, p_cnt = 0;
   Seg s;
-  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
+  bool ok = seg_first(s_cost, p.B, lo, hi, s);
   bool alive = true;
 
   auto wait_all = [&](int bar, uint32_t parity) -> bool {
@@ -618,7 +622,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_pref
     return true;
   };
 
-  while (alive && ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
+  while (alive && ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
     const uint32_t qb = seg_i % C::kQBufs, qn = seg_i / C::kQBufs;
     if (!wait_all((kFp8 ? Bb::QReady : Bb::QFull) + qb, qn & 1)) break;
     const int T = tiles_of(s);
@@ -710,7 +714,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 
 template <bool kFp8>
-__device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_prefix, const int* s_len,
+__device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len,
                              long long lo, long long hi, uint32_t tmem, int c, uint8_t* gbase) {
   using C = Cfg<kFp8>;
   using Bb = Bars<kFp8>;
@@ -738,9 +742,9 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     return true;
   };
   Seg s;
-  bool ok = seg_first(s_prefix, p.B, lo, hi, s);
+  bool ok = seg_first(s_cost, p.B, lo, hi, s);
 
-  while (ok && seg_next(s_prefix, s_len, p.B, lo, hi, s)) {
+  while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
     if (tid < 64) mref[tid] = -INFINITY;
     named_barrier_softmax();
     float lp[64];  // this thread's share of the softmax denominators
@@ -874,7 +878,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   uint8_t* gbase = dyn_smem + (base - raw);
   const SmemLayout L = smem_layout<kFp8>(p.B);
   int* s_len = reinterpret_cast<int*>(gbase + L.len);
-  int* s_prefix = reinterpret_cast<int*>(gbase + L.prefix);
+  int* s_cost = reinterpret_cast<int*>(gbase + L.prefix);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.misc);
   int* abort_flag = reinterpret_cast<int*>(gbase + L.misc + 4);
   const int warp = threadIdx.x >> 5;
@@ -924,22 +928,22 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   pdl_wait_prior_grid();    // the KV append (or previous step) must be complete before reading its results
   pdl_launch_dependents();  // the combine kernel may be scheduled now (its prologue reads seq_lens); it
                             // waits for this grid before it reads the partials
-  build_page_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, p.err, s_len, s_prefix);  // ends with a barrier
+  build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, p.err, p.piece_cost, s_len, s_cost);  // ends with a barrier
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const long long P = s_prefix[p.B];
+  const long long units = s_cost[p.B];  // total cost units
   const int c = blockIdx.x;
-  const long long lo = cta_page_lo(c, P, p.grid), hi = cta_page_lo(c + 1, P, p.grid);
+  const long long lo = cta_cost_lo(c, units, p.grid), hi = cta_cost_lo(c + 1, units, p.grid);
   Ctx cx{base, bars, abort_flag, p.err, p.wait_budget_ns};
 
   if (warp < 4) {
-    softmax_role<kFp8>(p, cx, s_prefix, s_len, lo, hi, tmem, c, gbase);
+    softmax_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
   } else if (warp == kProducerWarp) {
-    producer_role<kFp8>(p, &kmap, &vmap, &qmap, cx, s_prefix, s_len, lo, hi);
+    producer_role<kFp8>(p, &kmap, &vmap, &qmap, cx, s_cost, s_len, lo, hi);
   } else if (warp == kMmaWarp) {
-    mma_role<kFp8>(p, cx, s_prefix, s_len, lo, hi, tmem);
+    mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
-    dequant_role(p, cx, s_prefix, s_len, lo, hi);
+    dequant_role(p, cx, s_cost, s_len, lo, hi);
   }
   tc_fence_before();
   __syncthreads();

@@ -17,36 +17,39 @@ constexpr int kCombineThreads = 256;  // 8 warps = 8 heads of one sequence
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-__device__ __forceinline__ bool cta_range_nonempty(int c, long long P, int G) {
-  return cta_page_lo(c, P, G) < cta_page_lo(c + 1, P, G);
+__device__ __forceinline__ bool cta_range_nonempty(int c, long long C, int G) {
+  return cta_cost_lo(c, C, G) < cta_cost_lo(c + 1, C, G);
 }
 
 __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodeParams p) {
   extern __shared__ int smem_i[];
   int* s_len = smem_i;
-  int* s_prefix = smem_i + p.B;
+  int* s_cost = smem_i + p.B;
   // seq_lens is final before the split kernel starts; the partials are not
-  build_page_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, s_len, s_prefix);
+  build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, p.piece_cost, s_len, s_cost);
   pdl_wait_prior_grid();
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * (kCombineThreads / 32) + warp;
-  const long long P = s_prefix[p.B];
+  const long long C = s_cost[p.B];
   const int G = p.grid;
-  const long long sp0 = s_prefix[b], sp1 = s_prefix[b + 1];
+  const int np = pages_of_len(s_len[b]);
   uint16_t* out = p.out + ((size_t)b * kHeads + h) * kHeadDim;
-  if (sp1 == sp0) {  // empty sequence
+  if (np == 0) {  // empty sequence
     reinterpret_cast<uint2*>(out)[lane] = make_uint2(0u, 0u);
     reinterpret_cast<uint2*>(out + 128)[lane] = make_uint2(0u, 0u);
     if (lane == 0) p.lse[(size_t)b * kHeads + h] = -INFINITY;
     return;
   }
-  const int c_first = cta_of_page(sp0, P, G);
-  const int c_last = cta_of_page(sp1 - 1, P, G);
+  // the CTAs holding the first and the last page of b; every CTA between
+  // them with a non-empty range holds a piece of b
+  const long long first = (long long)s_cost[b] + p.piece_cost;
+  const int c_first = cta_of_cost(first, C, G);
+  const int c_last = cta_of_cost(first + np - 1, C, G);
   // maximum of the partial LSEs
   float mx = -INFINITY;
   for (int c = c_first + lane; c <= c_last; c += 32)
-    if (cta_range_nonempty(c, P, G)) mx = fmaxf(mx, __ldcg(p.part_lse + (size_t)(c + b) * kHeads + h));
+    if (cta_range_nonempty(c, C, G)) mx = fmaxf(mx, __ldcg(p.part_lse + (size_t)(c + b) * kHeads + h));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
   for (int base = c_first; base <= c_last; base += 32) {
     const int c = base + lane;
     float w = 0.0f;
-    if (c <= c_last && cta_range_nonempty(c, P, G))
+    if (c <= c_last && cta_range_nonempty(c, C, G))
       w = exp2f((__ldcg(p.part_lse + (size_t)(c + b) * kHeads + h) - mx) * kLog2e);
     den += w;
     const int n = min(32, c_last - base + 1);

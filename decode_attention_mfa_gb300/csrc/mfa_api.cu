@@ -187,6 +187,7 @@ DecodeParams make_decode_params(const void* q, const void* k_cache, const void* 
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.grid = plan.grid_ctas;
+  p.piece_cost = kPieceCostPages;
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   return p;
 }

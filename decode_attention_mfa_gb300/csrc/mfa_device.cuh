@@ -39,12 +39,20 @@ __device__ __forceinline__ int clamp_len(int len, int cap_tokens, uint32_t* err)
   return len;
 }
 
-// Fill s_len[b] (clamped lengths) and s_prefix[b] = sum_{c<b} pages(c) for
-// b <= B, using every thread of the block. s_prefix has B + 1 entries.
+// Work partition of one decode step. Sequence b with n_b > 0 pages costs
+// n_b + piece_cost units (an empty one costs nothing): the fixed part stands
+// for what a sequence piece costs a CTA besides its pages (loading Q, the page
+// table row, writing the partial result). Page k of b sits at cost position
+// s_cost[b] + piece_cost + k; the first piece_cost positions of b hold no page.
+// The G CTAs split the C = s_cost[B] units into equal ranges and each works on
+// the pages whose positions fall in its range.
+//
+// Fill s_len[b] (clamped lengths) and s_cost[b] = sum_{c<b} cost(c) for
+// b <= B, using every thread of the block. s_cost has B + 1 entries.
 // Must be called by all threads of the block; ends with __syncthreads().
-__device__ __forceinline__ void build_page_prefix(const int32_t* __restrict__ seq_lens, int B,
-                                                  int cap_tokens, uint32_t* err, int* s_len,
-                                                  int* s_prefix) {
+__device__ __forceinline__ void build_cost_prefix(const int32_t* __restrict__ seq_lens, int B,
+                                                  int cap_tokens, uint32_t* err, int piece_cost, int* s_len,
+                                                  int* s_cost) {
   for (int b = threadIdx.x; b < B; b += blockDim.x) s_len[b] = clamp_len(__ldg(seq_lens + b), cap_tokens, err);
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -52,35 +60,36 @@ __device__ __forceinline__ void build_page_prefix(const int32_t* __restrict__ se
     int running = 0;
     for (int base = 0; base < B; base += 32) {
       const int b = base + lane;
-      const int v = (b < B) ? pages_of_len(s_len[b]) : 0;
+      const int np = (b < B) ? pages_of_len(s_len[b]) : 0;
+      const int v = np > 0 ? np + piece_cost : 0;
       int x = v;  // inclusive warp scan
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
       }
-      if (b < B) s_prefix[b] = running + x - v;
+      if (b < B) s_cost[b] = running + x - v;
       running += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (lane == 0) s_prefix[B] = running;
+    if (lane == 0) s_cost[B] = running;
   }
   __syncthreads();
 }
 
-// Range of CTA c over P total pages split into G equal parts.
-__host__ __device__ __forceinline__ long long cta_page_lo(int c, long long P, int G) {
-  return (long long)c * P / G;
+// Range start of CTA c over C cost units split into G equal parts.
+__host__ __device__ __forceinline__ long long cta_cost_lo(int c, long long C, int G) {
+  return (long long)c * C / G;
 }
-// The CTA whose range holds page p (0 <= p < P).
-__host__ __device__ __forceinline__ int cta_of_page(long long p, long long P, int G) {
-  return (int)(((p + 1) * (long long)G - 1) / P);
+// The CTA whose range holds cost position x (0 <= x < C).
+__host__ __device__ __forceinline__ int cta_of_cost(long long x, long long C, int G) {
+  return (int)(((x + 1) * (long long)G - 1) / C);
 }
-// Largest b in [0, B) with prefix[b] <= p (the sequence holding page p).
-__device__ __forceinline__ int seq_of_page(const int* s_prefix, int B, long long p) {
+// Largest b in [0, B) with s_cost[b] <= x (no sequence before it reaches x).
+__device__ __forceinline__ int seq_of_cost(const int* s_cost, int B, long long x) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if ((long long)s_prefix[mid] <= p) lo = mid; else hi = mid - 1;
+    if ((long long)s_cost[mid] <= x) lo = mid; else hi = mid - 1;
   }
   return lo;
 }

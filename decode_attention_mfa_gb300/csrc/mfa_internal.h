@@ -22,6 +22,11 @@ constexpr size_t kWsHeaderBytes = 256;
 constexpr size_t kPartialOBytes = (size_t)kHeads * kHeadDim * sizeof(float);
 constexpr size_t kPartialLseBytes = (size_t)kHeads * sizeof(float);
 
+// Work partition of the split kernel: besides its pages, every sequence piece
+// is charged this many page-equivalents (a CTA pays for loading Q and page
+// ids and for writing the partial result of each piece it holds).
+constexpr int kPieceCostPages = 2;
+
 struct AppendParams {
   const uint16_t* k_new;  // [B][n_new][256] bf16 bits
   const uint16_t* v_new;
@@ -51,6 +56,7 @@ struct DecodeParams {
   uint32_t* err;
   float scale;
   int B, max_pages, num_pages, grid;
+  int piece_cost;          // cost units charged per sequence piece (work partition)
   uint64_t wait_budget_ns;
 };
 
@@ -74,7 +80,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
-cudaError_t launch_decode_split_simt(const DecodeParams& p, bool fp8, cudaStream_t stream);
 cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                    const CUtensorMap& q_map, cudaStream_t stream);
 cudaError_t launch_decode_split_tc_fp8(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,

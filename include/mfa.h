@@ -86,11 +86,13 @@ typedef struct {
   size_t workspace_bytes;   /* bytes mfa_decode_attention* needs */
 } mfa_plan_t;
 
-/* Split-KV planning (host only). The split kernel divides the pages of all
- * sequences, P = sum_b ceil(L_b / 64), into `grid_ctas` = G contiguous,
- * equal ranges that cross sequence boundaries: CTA c owns pages
- * [floor(c*P/G), floor((c+1)*P/G)) and writes one partial result per
- * sequence b it touches, into slot c + b. `max_len_hint` is the expected
+/* Split-KV planning (host only). The split kernel lays the sequences end to
+ * end on a line of cost units: a sequence with n = ceil(L_b / 64) > 0 pages
+ * takes n + 2 units (two units charged per piece, then one per page), an
+ * empty one none. The C units are cut into `grid_ctas` = G contiguous, equal
+ * ranges that cross sequence boundaries: CTA c owns the pages whose units lie
+ * in [floor(c*C/G), floor((c+1)*C/G)) and writes one partial result per
+ * sequence b it holds pages of, into slot c + b. `max_len_hint` is the expected
  * maximum length and only sizes the grid; longer sequences are still handled.
  * `num_sms` <= 0 means the current device's SM count. Returns
  * MFA_ERR_INVALID_ARG for batch outside [1, MFA_MAX_BATCH] or a negative

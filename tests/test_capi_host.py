@@ -42,41 +42,53 @@ def test_plan_without_gpu(lib):
             capi.mfa_plan_decode(bad[0], bad[1], 152)
 
 
-def _cta_lo(c, P, G):
-    return c * P // G
+def _cta_lo(c, C, G):
+    return c * C // G
 
 
-def _cta_of_page(p, P, G):
-    return ((p + 1) * G - 1) // P
+def _cta_of_cost(x, C, G):
+    return ((x + 1) * G - 1) // C
 
 
-@pytest.mark.parametrize("seed", range(20))
+@pytest.mark.parametrize("seed", range(24))
 def test_partition_slots_are_unique_and_combine_finds_them(seed):
-    """Split scheme used by the split and combine kernels: CTA c owns pages
-    [c*P//G, (c+1)*P//G); its piece of sequence b goes to slot c + b. Slots
-    never collide, stay below G + B - 1, and the combine's CTA interval for b
-    is exactly the CTAs that own pages of b."""
+    """Split scheme used by the split and combine kernels: a sequence with
+    n > 0 pages costs n + piece_cost units, its page k sits at unit
+    cost_prefix[b] + piece_cost + k, and CTA c owns units [c*C//G,
+    (c+1)*C//G); its piece of sequence b goes to slot c + b. Every page is
+    owned by exactly one CTA, slots never collide and stay below G + B - 1,
+    and the combine's CTA interval for b is exactly the CTAs that own pages
+    of b."""
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 60))
     pages = rng.integers(0, 40, size=B) * (rng.random(B) < 0.9)
+    if seed % 4 == 0:
+        pages[:] = rng.integers(1, 3)  # many short sequences, more CTAs than pages
     G = int(rng.integers(1, 160))
-    P = int(pages.sum())
-    if P == 0:
+    piece_cost = int(rng.integers(0, 4))
+    cost = np.where(pages > 0, pages + piece_cost, 0)
+    C = int(cost.sum())
+    if C == 0:
         return
-    prefix = np.concatenate([[0], np.cumsum(pages)])
-    owners, slots = {}, set()
+    prefix = np.concatenate([[0], np.cumsum(cost)])
+    owners, slots, covered = {}, set(), np.zeros(B, dtype=np.int64)
     for c in range(G):
-        lo, hi = _cta_lo(c, P, G), _cta_lo(c + 1, P, G)
+        lo, hi = _cta_lo(c, C, G), _cta_lo(c + 1, C, G)
         for b in range(B):
-            if max(lo, prefix[b]) < min(hi, prefix[b + 1]):
+            first = prefix[b] + piece_cost
+            pg0, pg1 = max(lo - first, 0), min(hi - first, pages[b])
+            if pages[b] > 0 and pg0 < pg1:
+                covered[b] += pg1 - pg0
                 s = c + b
                 assert s not in slots and s < G + B - 1
                 slots.add(s)
                 owners.setdefault(b, []).append(c)
+    assert (covered == pages).all()
     for b in range(B):
         if pages[b] == 0:
             assert b not in owners
             continue
-        cf, cl = _cta_of_page(prefix[b], P, G), _cta_of_page(prefix[b + 1] - 1, P, G)
-        found = [c for c in range(cf, cl + 1) if _cta_lo(c, P, G) < _cta_lo(c + 1, P, G)]
+        first = prefix[b] + piece_cost
+        cf, cl = _cta_of_cost(first, C, G), _cta_of_cost(first + pages[b] - 1, C, G)
+        found = [c for c in range(cf, cl + 1) if _cta_lo(c, C, G) < _cta_lo(c + 1, C, G)]
         assert found == owners[b]
