@@ -52,9 +52,9 @@ struct Cfg;
 template <>
 struct Cfg<false> {
   static constexpr int kThreads = 192;
-  static constexpr int kSlots = 7;       // 16 KB operand chunks
+  static constexpr int kSlots = 9;       // 16 KB operand chunks
   static constexpr int kStages = 0;      // raw code pages
-  static constexpr int kQBufs = 2;
+  static constexpr int kQBufs = 1;
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
 };
@@ -96,8 +96,7 @@ struct Bars {  // indices into the barrier array
   static constexpr int SEmpty = SFull + 2;           // [2]
   static constexpr int PFull = SEmpty + 2;           // [2]
   static constexpr int PEmpty = PFull + 2;           // [2]
-  static constexpr int OReady = PEmpty + 2;          // one completion per P.V
-  static constexpr int OFree = OReady + 1;           // one completion per epilogue
+  static constexpr int OFree = PEmpty + 2;          // one completion per epilogue
   static constexpr int Drain = OFree + 1;
   static constexpr int StFull = Drain + 1;           // [kStages] raw page landed
   static constexpr int StEmpty = StFull + C::kStages;   // [kStages] raw page converted
@@ -123,9 +122,9 @@ struct SmemLayout {
 };
 
 template <bool kFp8>
-__host__ __device__ inline SmemLayout smem_layout(int B) {
+__host__ __device__ constexpr SmemLayout smem_layout(int B) {
   using C = Cfg<kFp8>;
-  SmemLayout L;
+  SmemLayout L{};
   L.ring = 0;
   L.stage = L.ring + C::kSlots * kSlotBytes;
   L.q = L.stage + C::kStages * kStageBytes;
@@ -140,6 +139,9 @@ __host__ __device__ inline SmemLayout smem_layout(int B) {
   L.total = L.misc + 16;
   return L;
 }
+constexpr uint32_t kMaxDynamicSmem = 227u * 1024u;  // per-block opt-in limit of sm_103a
+static_assert(smem_layout<false>(kMaxBatch).total + 1024 <= kMaxDynamicSmem, "bf16 layout exceeds shared memory");
+static_assert(smem_layout<true>(kMaxBatch).total + 1024 <= kMaxDynamicSmem, "E4M3 layout exceeds shared memory");
 
 struct Ctx {
   uint32_t base;      // shared address of the aligned dynamic smem base
@@ -615,7 +617,6 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
     }
     if (lane == 0) {
       tc_commit(cx.bar(Bb::PEmpty + buf));
-      tc_commit(cx.bar(Bb::OReady));
     }
     __syncwarp();
     ++p_cnt;
@@ -729,18 +730,12 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   const uint32_t taddr_o = tmem + lane_base + 128;
   const float c2 = p.scale * kLog2e;
   uint32_t s_cnt = 0, p_cnt = 0, tile_i = 0;
-  // o_ready completes once per P.V; a parity wait only tells the current phase
-  // from the previous one, so its completions are observed one by one, in
-  // order. Waiting for P.V(g-1) before handing over P(g) keeps the barrier at
-  // most one phase ahead of this count.
-  uint32_t o_seen = 0;
-  auto observe_pv = [&](uint32_t k) -> bool {
-    while (o_seen <= k) {
-      if (!cx.wait(Bb::OReady, o_seen & 1)) return false;
-      ++o_seen;
-    }
-    return true;
-  };
+  // P.V(g) completes phase g/2 of p_empty[g % 2]. Before P(g) is written the
+  // softmax has seen P.V(g-2) complete, and P.V(g+2) cannot start before P(g+2)
+  // exists, so when it waits for P.V(g) that barrier is at phase g/2 or just
+  // past it: the parity wait is exact. Completion of P.V(g) implies that of
+  // every earlier MMA (one issuing thread, commits track all prior MMAs).
+  auto wait_pv = [&](uint32_t g) -> bool { return cx.wait(Bb::PEmpty + (g & 1), (g >> 1) & 1); };
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
 
@@ -800,7 +795,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         }
         if (t > 0 && rescale_o) {
           // O^T holds the previous tiles: wait for their last P.V, then scale its columns
-          if (!observe_pv(p_cnt - 1)) return;
+          if (!wait_pv(p_cnt - 1)) return;
           tc_fence_after();
           scale_o_columns(taddr_o, alpha);
         }
@@ -820,7 +815,6 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         packed[h >> 1] = kFp8 ? pack2<kFp8>(p0 * vmul, p1 * vmul) : pack2<kFp8>(p0, p1);
       }
       const uint32_t pbuf = p_cnt & 1;
-      if (p_cnt > 0 && !observe_pv(p_cnt - 1)) return;
       if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
       const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
 #pragma unroll
@@ -834,7 +828,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       ++tile_i;
     }
     // ---- epilogue of this sequence piece: l = sum over the 128 lanes, O^T / l, LSE
-    if (!observe_pv(p_cnt - 1)) return;
+    if (!wait_pv(p_cnt - 1)) return;
     tc_fence_after();
     warp_reduce_scatter_sum(lp, lane);
     named_barrier_softmax();  // earlier readers of red/alpha are done
@@ -899,7 +893,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(bars + 8 * (Bb::PFull + i), kSoftmaxThreads);
       mbar_init(bars + 8 * (Bb::PEmpty + i), 1);
     }
-    mbar_init(bars + 8 * Bb::OReady, 1);
     mbar_init(bars + 8 * Bb::OFree, kSoftmaxThreads);
     mbar_init(bars + 8 * Bb::Drain, 1);
     for (int i = 0; i < C::kStages; ++i) {
