@@ -117,7 +117,7 @@ __host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = 
 
 struct SmemLayout {
   uint32_t ring, stage, q, p, scales;  // byte offsets from the 1024-aligned base
-  uint32_t len, prefix, red, flags, bars, misc;
+  uint32_t len, prefix, red, bars, misc;
   uint32_t total;
 };
 
@@ -133,8 +133,7 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
   L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64]
-  L.flags = L.red + 6 * 64 * 4;                   // int flags[2][4]
-  L.bars = (L.flags + 32 + 7) & ~7u;              // mbarriers
+  L.bars = L.red + 6 * 64 * 4;                    // mbarriers
   L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
   L.total = L.misc + 16;
   return L;
@@ -155,6 +154,23 @@ struct Ctx {
 
 __device__ __forceinline__ void named_barrier_softmax() {
   asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+}
+// The same barrier, returning the OR of `pred` over the softmax threads.
+__device__ __forceinline__ bool named_barrier_softmax_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(kSoftmaxThreads)
+      : "memory");
+  return r != 0;
+}
+// 2^x with the multi-function unit's approximation (relative error below
+// 2^-22; subnormal results flush to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Segment iteration shared by all roles: sequence b, pages [pg0, pg1) of it.
@@ -725,11 +741,10 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   float* red = reinterpret_cast<float*>(gbase + L.red);  // [4][64] per-warp partial reductions
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
   float* alpha = mref + 64;                              // [64] rescale factors / 1/l, uniform
-  int* flags = reinterpret_cast<int*>(gbase + L.flags);  // [2][4]
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
   const uint32_t taddr_o = tmem + lane_base + 128;
   const float c2 = p.scale * kLog2e;
-  uint32_t s_cnt = 0, p_cnt = 0, tile_i = 0;
+  uint32_t s_cnt = 0, p_cnt = 0;
   // P.V(g) completes phase g/2 of p_empty[g % 2]. Before P(g) is written the
   // softmax has seen P.V(g-2) complete, and P.V(g+2) cannot start before P(g+2)
   // exists, so when it waits for P.V(g) that barrier is at phase g/2 or just
@@ -771,11 +786,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
 #pragma unroll
       for (int h = 0; h < 64; ++h) mine |= x[h] > mref[h] + kRescaleThreshold;
       // ---- does any logit of the tile exceed its reference maximum by 2^8?
-      const int fl = tile_i & 1;
-      const bool wany = __any_sync(0xffffffffu, mine);
-      if (lane == 0) flags[fl * 4 + warp] = wany ? 1 : 0;
-      named_barrier_softmax();
-      if (flags[fl * 4 + 0] | flags[fl * 4 + 1] | flags[fl * 4 + 2] | flags[fl * 4 + 3]) {
+      if (named_barrier_softmax_or(mine)) {
         warp_reduce_scatter_max(x, lane);  // x is reloaded below
         red[warp * 64 + 2 * lane] = x[0];
         red[warp * 64 + 2 * lane + 1] = x[1];
@@ -783,17 +794,19 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         if (tid < 64) {
           const float m_old = mref[tid];
           const float m_new = fmaxf(m_old, fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid])));
-          alpha[tid] = (m_old == -INFINITY) ? 0.0f : exp2f(m_old - m_new);
+          alpha[tid] = ex2_approx(m_old - m_new);  // 0 while m_old = -inf
           mref[tid] = m_new;
         }
         named_barrier_softmax();
         bool rescale_o = false;
+        if (t > 0) {  // the first tile of a piece has nothing to rescale
 #pragma unroll
-        for (int h = 0; h < 64; ++h) {
-          lp[h] *= alpha[h];
-          rescale_o |= alpha[h] != 1.0f;
+          for (int h = 0; h < 64; ++h) {
+            lp[h] *= alpha[h];
+            rescale_o |= alpha[h] != 1.0f;
+          }
         }
-        if (t > 0 && rescale_o) {
+        if (rescale_o) {
           // O^T holds the previous tiles: wait for their last P.V, then scale its columns
           if (!wait_pv(p_cnt - 1)) return;
           tc_fence_after();
@@ -808,8 +821,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       uint32_t packed[32];
 #pragma unroll
       for (int h = 0; h < 64; h += 2) {
-        const float p0 = exp2f(x[h] - mref[h]);
-        const float p1 = exp2f(x[h + 1] - mref[h + 1]);
+        const float p0 = ex2_approx(x[h] - mref[h]);
+        const float p1 = ex2_approx(x[h + 1] - mref[h + 1]);
         lp[h] += p0;
         lp[h + 1] += p1;
         packed[h >> 1] = kFp8 ? pack2<kFp8>(p0 * vmul, p1 * vmul) : pack2<kFp8>(p0, p1);
@@ -825,11 +838,9 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       tc_fence_before();
       mbar_arrive(cx.bar(Bb::PFull + pbuf));
       ++p_cnt;
-      ++tile_i;
     }
-    // ---- epilogue of this sequence piece: l = sum over the 128 lanes, O^T / l, LSE
-    if (!wait_pv(p_cnt - 1)) return;
-    tc_fence_after();
+    // ---- epilogue of this sequence piece: l = sum over the 128 lanes and the
+    // LSE (final once the last P is out), then, after the last P.V, O^T / l
     warp_reduce_scatter_sum(lp, lane);
     named_barrier_softmax();  // earlier readers of red/alpha are done
     red[warp * 64 + 2 * lane] = lp[0];
@@ -842,6 +853,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       p.part_lse[slot * kHeads + tid] = (mref[tid] + log2f(l)) * kLn2;
     }
     named_barrier_softmax();
+    if (!wait_pv(p_cnt - 1)) return;
+    tc_fence_after();
     float* dst = p.part_o + slot * kHeads * kHeadDim;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
