@@ -52,9 +52,10 @@ struct Cfg;
 template <>
 struct Cfg<false> {
   static constexpr int kThreads = 192;
-  static constexpr int kSlots = 9;       // 16 KB operand chunks
+  static constexpr int kSlots = 7;       // 16 KB operand chunks
   static constexpr int kStages = 0;      // raw code pages
-  static constexpr int kQBufs = 1;
+  static constexpr int kQBufs = 2;
+  static constexpr bool kCrossPiece = true;  // one tile stream across sequence pieces
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
 };
@@ -66,6 +67,7 @@ struct Cfg<true> {
   static constexpr int kSlots = 3;
   static constexpr int kStages = 6;
   static constexpr int kQBufs = 1;
+  static constexpr bool kCrossPiece = false;  // per-piece order (a single Q buffer)
   static constexpr int kScaleSlots = 4;
   static constexpr int kAbFormat = 0;    // f16 operands
 };
@@ -78,7 +80,8 @@ constexpr int kStageBytes = 16384;        // one E4M3 page: 64 rows x 256 B (two
 constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]
 constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads], 16-bit
 constexpr int kScaleBytes = 1024;         // per tile: 128 K scales, then 128 V scales
-constexpr int kTmemCols = 256;            // S^T x2 (64 cols each) + O^T (2 x 64 cols)
+constexpr int kTmemCols = 512;            // S^T x2 (64 cols each) + O^T x2 (128 cols each)
+constexpr int kTmemO = 128;               // first O^T column; buffer o at kTmemO + 128 * o
 constexpr int kMaxBars = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -96,8 +99,8 @@ struct Bars {  // indices into the barrier array
   static constexpr int SEmpty = SFull + 2;           // [2]
   static constexpr int PFull = SEmpty + 2;           // [2]
   static constexpr int PEmpty = PFull + 2;           // [2]
-  static constexpr int OFree = PEmpty + 2;          // one completion per epilogue
-  static constexpr int Drain = OFree + 1;
+  static constexpr int OFree = PEmpty + 2;           // [2] one completion per epilogue of a piece using O^T buffer i
+  static constexpr int Drain = OFree + 2;
   static constexpr int StFull = Drain + 1;           // [kStages] raw page landed
   static constexpr int StEmpty = StFull + C::kStages;   // [kStages] raw page converted
   static constexpr int ScFull = StEmpty + C::kStages;   // [kScaleSlots]
@@ -132,8 +135,8 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
   L.scales = L.p + 2 * kPBytes;
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
-  L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64]
-  L.bars = L.red + 6 * 64 * 4;                    // mbarriers
+  L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64], inv_l[2][64]
+  L.bars = L.red + 8 * 64 * 4;                    // mbarriers
   L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
   L.total = L.misc + 16;
   return L;
@@ -325,6 +328,11 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++sc_cnt;
     return true;
   };
+  // bf16: V dims of both halves of the pages of a tile
+  auto issue_v_tile = [&](int pa, int pb) -> bool {
+    return issue_v(0, pa) && issue_v(1, pa) && (pb < 0 || (issue_v(0, pb) && issue_v(1, pb)));
+  };
+  int pend_a = -1, pend_b = -1;  // pages of the tile whose V is still to be issued (tile stream)
   uint32_t last_q_parity = 0, last_qb = 0;
   bool issued_q = false;
   while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
@@ -352,6 +360,20 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++seg_i;
     const int T = tiles_of(s);
     bool good = true;
+    if constexpr (C::kCrossPiece) {
+      // K(g), then V(g - 1) of the previous tile, which may belong to the
+      // previous piece: the next piece's first K tile is not queued behind the
+      // last V tile of the previous one
+      for (int t = 0; good && t < T; ++t) {
+        const int pga = s.pg0 + 2 * t;
+        const int pa = ids.get(pga, p, lane);
+        const int pb = (pages_in_tile(s, t) == 2) ? ids.get(pga + 1, p, lane) : -1;
+        for (int d = 0; good && d < 4; ++d) good = issue_k(d, pa, pb);
+        if (good && pend_a >= 0) good = issue_v_tile(pend_a, pend_b);
+        pend_a = pa;
+        pend_b = pb;
+      }
+    } else {
     for (int t = 0; good && t <= T; ++t) {
       if (t < T) {
         const int pga = s.pg0 + 2 * t;
@@ -375,8 +397,13 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
         }
       }
     }
-    if (!good) break;
+    }
+    if (!good) {
+      pend_a = -1;
+      break;
+    }
   }
+  if (C::kCrossPiece && pend_a >= 0) (void)issue_v_tile(pend_a, pend_b);
   // drain: every copy this warp issued must land before the CTA exits
   if (lane == 0) {
     for (uint32_t k = (cc > (uint32_t)kRing ? cc - kRing : 0); k < cc; ++k)
@@ -564,6 +591,9 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
   bool alive = true;
+  Seg pend_s{};        // tile stream: the tile whose P.V is still to be issued
+  int pend_t = -1;
+  uint32_t pend_piece = 0;
 
   auto wait_all = [&](int bar, uint32_t parity) -> bool {
     const bool r = cx.wait(bar, parity);  // every lane polls the same barrier
@@ -595,9 +625,14 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
     ++s_cnt;
     return true;
   };
-  auto do_pv = [&](const Seg& sg, int t, bool first_of_seg) -> bool {
+  // P.V of tile t of piece `piece` (sg)
+  auto do_pv = [&](const Seg& sg, int t, uint32_t piece) -> bool {
     const uint32_t buf = p_cnt & 1, n = p_cnt >> 1;
-    if (first_of_seg && !wait_all(Bb::OFree, (seg_i & 1) ^ 1)) return false;
+    const bool first_of_seg = t == 0;
+    // pieces alternate between the two O^T buffers; the first P.V of piece j
+    // overwrites the buffer of piece j - 2, whose epilogue must be done
+    const uint32_t obuf = piece & 1;
+    if (first_of_seg && !wait_all(Bb::OFree + obuf, ((piece >> 1) & 1) ^ 1)) return false;
     if (!wait_all(Bb::PFull + buf, n & 1)) return false;
     const int pga = sg.pg0 + 2 * t;
     const int np = pages_in_tile(sg, t);
@@ -622,7 +657,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
           const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma(tmem + 128 + hf * 64, smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
+            tc_mma(tmem + kTmemO + obuf * 128 + hf * 64, smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
                    smem_desc_sw128(bp + kk * 2048, 8192, 1024), idesc_o<kFp8>(),
                    !(first_of_seg && i == 0 && kk == 0));
           tc_commit(cx.bar(Bb::Empty + slot));
@@ -643,17 +678,31 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
     const uint32_t qb = seg_i % C::kQBufs, qn = seg_i / C::kQBufs;
     if (!wait_all((kFp8 ? Bb::QReady : Bb::QFull) + qb, qn & 1)) break;
     const int T = tiles_of(s);
-    alive = do_s(qb);
-    if (alive && T == 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
-    for (int t = 1; alive && t < T; ++t) {
+    if constexpr (C::kCrossPiece) {
+      // S(g), then P.V(g - 1), in the producer's order
+      for (int t = 0; alive && t < T; ++t) {
+        alive = do_s(qb);
+        if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
+        __syncwarp();
+        if (alive && pend_t >= 0) alive = do_pv(pend_s, pend_t, pend_piece);
+        pend_s = s;
+        pend_t = t;
+        pend_piece = seg_i;
+      }
+    } else {
       alive = do_s(qb);
-      if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
-      __syncwarp();
-      if (alive) alive = do_pv(s, t - 1, t == 1);
+      if (alive && T == 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
+      for (int t = 1; alive && t < T; ++t) {
+        alive = do_s(qb);
+        if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
+        __syncwarp();
+        if (alive) alive = do_pv(s, t - 1, seg_i);
+      }
+      if (alive) alive = do_pv(s, T - 1, seg_i);
     }
-    if (alive) alive = do_pv(s, T - 1, T == 1);
     ++seg_i;
   }
+  if (C::kCrossPiece && alive && pend_t >= 0) (void)do_pv(pend_s, pend_t, pend_piece);
   // drain: wait for every MMA this thread issued before TMEM is released
   if (lane == 0) {
     tc_commit(cx.bar(Bb::Drain));
@@ -740,9 +789,10 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   const SmemLayout L = smem_layout<kFp8>(p.B);
   float* red = reinterpret_cast<float*>(gbase + L.red);  // [4][64] per-warp partial reductions
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
-  float* alpha = mref + 64;                              // [64] rescale factors / 1/l, uniform
+  float* alpha = mref + 64;                              // [64] rescale factors, uniform
+  float* inv_l = alpha + 64;                             // [2][64] 1/l of the piece in O^T buffer i
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-  const uint32_t taddr_o = tmem + lane_base + 128;
+  const uint32_t taddr_o0 = tmem + lane_base + kTmemO;
   const float c2 = p.scale * kLog2e;
   uint32_t s_cnt = 0, p_cnt = 0;
   // P.V(g) completes phase g/2 of p_empty[g % 2]. Before P(g) is written the
@@ -751,10 +801,43 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   // past it: the parity wait is exact. Completion of P.V(g) implies that of
   // every earlier MMA (one issuing thread, commits track all prior MMAs).
   auto wait_pv = [&](uint32_t g) -> bool { return cx.wait(Bb::PEmpty + (g & 1), (g >> 1) & 1); };
+  // Pieces alternate between two O^T buffers. A piece's O^T / l is written
+  // out once the next piece's first P has been handed over (its last P.V was
+  // issued before that piece's first S), so the softmax warps go on to the
+  // next piece without waiting for the previous one's last P.V.
+  bool pend = false;
+  uint32_t pend_pv = 0, pend_obuf = 0;
+  size_t pend_slot = 0;
+  auto write_o = [&]() -> bool {
+    if (!wait_pv(pend_pv)) return false;
+    tc_fence_after();
+    const uint32_t ta = taddr_o0 + pend_obuf * 128;
+    const float* il = inv_l + pend_obuf * 64;
+    float* dst = p.part_o + pend_slot * kHeads * kHeadDim;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float o[32];
+        tmem_ld32(ta + hf * 64 + q * 32, o);
+        tc_wait_ld();
+        const int dim = hf * 128 + tid;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) dst[(q * 32 + h) * kHeadDim + dim] = o[h] * il[q * 32 + h];
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(cx.bar(Bb::OFree + pend_obuf));
+    pend = false;
+    return true;
+  };
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
+  uint32_t piece = 0;
 
   while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
+    const uint32_t obuf = piece & 1;
+    const uint32_t taddr_o = taddr_o0 + obuf * 128;
     if (tid < 64) mref[tid] = -INFINITY;
     named_barrier_softmax();
     float lp[64];  // this thread's share of the softmax denominators
@@ -838,9 +921,10 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       tc_fence_before();
       mbar_arrive(cx.bar(Bb::PFull + pbuf));
       ++p_cnt;
+      if (t == 0 && pend && !write_o()) return;
     }
     // ---- epilogue of this sequence piece: l = sum over the 128 lanes and the
-    // LSE (final once the last P is out), then, after the last P.V, O^T / l
+    // LSE (final once the last P is out); O^T / l follows later (write_o)
     warp_reduce_scatter_sum(lp, lane);
     named_barrier_softmax();  // earlier readers of red/alpha are done
     red[warp * 64 + 2 * lane] = lp[0];
@@ -849,28 +933,17 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const size_t slot = (size_t)c + s.b;
     if (tid < 64) {
       const float l = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
-      alpha[tid] = 1.0f / l;
+      inv_l[obuf * 64 + tid] = 1.0f / l;
       p.part_lse[slot * kHeads + tid] = (mref[tid] + log2f(l)) * kLn2;
     }
     named_barrier_softmax();
-    if (!wait_pv(p_cnt - 1)) return;
-    tc_fence_after();
-    float* dst = p.part_o + slot * kHeads * kHeadDim;
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float o[32];
-        tmem_ld32(taddr_o + hf * 64 + q * 32, o);
-        tc_wait_ld();
-        const int dim = hf * 128 + tid;
-#pragma unroll
-        for (int h = 0; h < 32; ++h) dst[(q * 32 + h) * kHeadDim + dim] = o[h] * alpha[q * 32 + h];
-      }
-    }
-    tc_fence_before();
-    mbar_arrive(cx.bar(Bb::OFree));
+    pend = true;
+    pend_pv = p_cnt - 1;
+    pend_obuf = obuf;
+    pend_slot = slot;
+    ++piece;
   }
+  if (pend) (void)write_o();
 }
 
 template <bool kFp8>
@@ -906,7 +979,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(bars + 8 * (Bb::PFull + i), kSoftmaxThreads);
       mbar_init(bars + 8 * (Bb::PEmpty + i), 1);
     }
-    mbar_init(bars + 8 * Bb::OFree, kSoftmaxThreads);
+    mbar_init(bars + 8 * (Bb::OFree + 0), kSoftmaxThreads);
+    mbar_init(bars + 8 * (Bb::OFree + 1), kSoftmaxThreads);
     mbar_init(bars + 8 * Bb::Drain, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bars + 8 * (Bb::StFull + i), 1);

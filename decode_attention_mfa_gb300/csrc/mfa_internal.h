@@ -25,7 +25,7 @@ constexpr size_t kPartialLseBytes = (size_t)kHeads * sizeof(float);
 // Work partition of the split kernel: besides its pages, every sequence piece
 // is charged this many page-equivalents (a CTA pays for loading Q and page
 // ids and for writing the partial result of each piece it holds).
-constexpr int kPieceCostPages = 2;
+constexpr int kPieceCostPages = 1;
 
 struct AppendParams {
   const uint16_t* k_new;  // [B][n_new][256] bf16 bits
