@@ -643,11 +643,12 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         if (!wait_all(Bb::Full + slot, ph)) return false;
         const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
         if (!kFp8 && nv < kPageSize) {
-          // rows [nv, 64) of both 64-dim blocks: 128 B each, 16 B per lane and step
+          // rows [nv, 64) of both 64-dim blocks (whole 128 B rows, so the
+          // swizzle does not matter): 16 B per lane and step
           const int nbytes = (kPageSize - nv) * 128;
-          for (int off = lane * 16; off < 2 * nbytes; off += 32 * 16) {
-            const int blk = off / nbytes, r = off % nbytes;
-            st_shared_v4(a0 + blk * 8192 + nv * 128 + r, make_uint4(0u, 0u, 0u, 0u));
+          for (int off = lane * 16; off < nbytes; off += 32 * 16) {
+            st_shared_v4(a0 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
+            st_shared_v4(a0 + 8192 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
           }
           fence_proxy_async_smem();
           __syncwarp();
