@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendParams 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kAppendThreads / 32;
   pdl_launch_dependents();  // the decode kernel may run its prologue meanwhile
+  pdl_wait_prior_grid();    // launched early too: whatever ran before must be complete and visible
   // the row of this warp's first work item (token t = i / 2, K or V) is read
   // while warp 0 looks up and checks where the tokens go
   const int first = warp;
@@ -122,8 +123,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendParams 
 }  // namespace
 
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
-  kv_append_kernel<<<p.B, kAppendThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(p.B), dim3(kAppendThreads), 0, stream, p);
 }
 
 }  // namespace mfa
