@@ -59,11 +59,20 @@ struct Cfg<false> {
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
 };
-constexpr int kDequantThreads = 64;      // E4M3: warps 6.. convert codes to f16
+// E4M3: warps 8-11 (a warpgroup) convert codes to f16; warps 6-7 idle. The
+// three warpgroups split the registers: the softmax warpgroup grows to
+// kRegSoftmax, the other two shrink to kRegOther (setmaxnreg), within the
+// 384 x 168 registers the block is launched with.
+constexpr int kDequantThreads = 128;
+constexpr int kDequantWarp0 = 8;
+constexpr int kRegSoftmax = 232;
+constexpr int kRegOther = 136;
+constexpr int kRegLaunch = 168;
+static_assert(128 * kRegSoftmax + 256 * kRegOther <= 384 * kRegLaunch, "register split exceeds the launch's registers");
 
 template <>
 struct Cfg<true> {
-  static constexpr int kThreads = 192 + kDequantThreads;
+  static constexpr int kThreads = 384;
   static constexpr int kSlots = 3;
   static constexpr int kStages = 6;
   static constexpr int kQBufs = 1;
@@ -467,7 +476,7 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
                              long long lo, long long hi) {
   using C = Cfg<true>;
   using Bb = Bars<true>;
-  const int tid = threadIdx.x - 6 * 32;  // 0 .. kDequantThreads - 1
+  const int tid = threadIdx.x - kDequantWarp0 * 32;  // 0 .. kDequantThreads - 1
   const SmemLayout L = smem_layout<true>(p.B);
   uint32_t st = 0, cc = 0, seg_i = 0;    // staged pages consumed, operand chunks produced, pieces
   Seg s;
@@ -1017,6 +1026,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const long long lo = cta_cost_lo(c, units, p.grid), hi = cta_cost_lo(c + 1, units, p.grid);
   Ctx cx{base, bars, abort_flag, p.err, p.wait_budget_ns};
 
+  if constexpr (kFp8) {  // whole warpgroups execute these
+    if (warp < 4)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
+    else
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther));
+  }
   if (warp < 4) {
     softmax_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
   } else if (warp == kProducerWarp) {
@@ -1024,7 +1039,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   } else if (warp == kMmaWarp) {
     mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
-    dequant_role(p, cx, s_cost, s_len, lo, hi);
+    if (warp >= kDequantWarp0) dequant_role(p, cx, s_cost, s_len, lo, hi);
   }
   tc_fence_before();
   __syncthreads();
@@ -1037,6 +1052,17 @@ template <bool kFp8>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, cudaStream_t stream) {
   const size_t smem = (size_t)smem_layout<kFp8>(p.B).total + 1024;
+  if constexpr (kFp8) {
+    // setmaxnreg.inc would wait forever if the block had fewer registers than the split
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+      cudaFuncAttributes fa;
+      const cudaError_t e = cudaFuncGetAttributes(&fa, decode_split_tc_kernel<kFp8>);
+      if (e != cudaSuccess) return e;
+      launch_regs = fa.numRegs;
+    }
+    if (launch_regs < kRegLaunch) return cudaErrorInvalidConfiguration;
+  }
   static int configured_bytes = 0;  // largest opt-in set so far (per process; one device family)
   if ((int)smem > configured_bytes) {
     const cudaError_t e =
