@@ -91,6 +91,7 @@ constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads], 16-bi
 constexpr int kScaleBytes = 1024;         // per tile: 128 K scales, then 128 V scales
 constexpr int kTmemCols = 512;            // S^T x2 (64 cols each) + O^T x2 (128 cols each)
 constexpr int kTmemO = 128;               // first O^T column; buffer o at kTmemO + 128 * o
+constexpr int kTmemK = 384;               // E4M3: the f16 K tile (A operand of S^T), 256 dims in 128 columns
 constexpr int kMaxBars = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -114,7 +115,9 @@ struct Bars {  // indices into the barrier array
   static constexpr int StEmpty = StFull + C::kStages;   // [kStages] raw page converted
   static constexpr int ScFull = StEmpty + C::kStages;   // [kScaleSlots]
   static constexpr int ScEmpty = ScFull + C::kScaleSlots;
-  static constexpr int Count = ScEmpty + C::kScaleSlots;
+  static constexpr int KFull = ScEmpty + C::kScaleSlots;  // E4M3: f16 K tile written to TMEM
+  static constexpr int KFree = KFull + 1;                 // E4M3: the S MMAs that read it are done
+  static constexpr int Count = KFree + 1;
   static_assert(Count <= kMaxBars, "barrier array too small");
 };
 
@@ -473,10 +476,13 @@ __device__ __forceinline__ void convert_q_to_f16(uint32_t q_addr, int tid) {
 }
 
 __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len,
-                             long long lo, long long hi) {
+                             long long lo, long long hi, uint32_t tmem) {
   using C = Cfg<true>;
   using Bb = Bars<true>;
   const int tid = threadIdx.x - kDequantWarp0 * 32;  // 0 .. kDequantThreads - 1
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quadrant
+  uint32_t kt = 0;                                              // K tiles written to TMEM
   const SmemLayout L = smem_layout<true>(p.B);
   uint32_t st = 0, cc = 0, seg_i = 0;    // staged pages consumed, operand chunks produced, pieces
   Seg s;
@@ -507,39 +513,42 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const int T = tiles_of(s);
     for (int t = 0; t <= T; ++t) {
       if (t < T) {
-        // K(t): chunk d = dims [64d, 64d + 64) of the tile's 128 rows
+        // K(t) goes to TMEM as the A operand of S^T: this thread writes token
+        // row r of the tile (its TMEM lane; rows 64-127 come from the second
+        // page), 256 dims as 128 columns of f16 pairs. Rows past the tile's
+        // pages keep whatever they held: their logits are masked.
         const int np = pages_in_tile(s, t);
         const uint32_t ka = st, kb = st + 1;
         if (!wait_stage(ka) || (np == 2 && !wait_stage(kb))) return;
-        for (int d = 0; d < 4; ++d) {
-          uint32_t dst;
-          if (!begin_chunk(dst)) return;
-          // rows r = tid, tid + kDequantThreads, ... of the 128-row chunk (rows
-          // 64-127 come from the second page); a thread loads all its pieces
-          // before converting any
-          constexpr int kRows = 128 / kDequantThreads;
-          uint4 raw[4 * kRows];
+        if (!cx.wait(Bb::KFree, (kt & 1) ^ 1)) return;  // the S MMAs of the previous tile are done
+        tc_fence_after();
+        const int r = 32 * (warp & 3) + lane, pi = r >> 6, rr = r & 63;
+        if (pi < np) {
+          const uint32_t src = stage_addr(pi ? kb : ka);
 #pragma unroll
-          for (int i = 0; i < kRows; ++i) {
-            const int row = tid + i * kDequantThreads, pi = row >> 6;
-            const uint32_t src = stage_addr(pi ? kb : ka) + (d >> 1) * 8192;
+          for (int h = 0; h < 2; ++h) {  // dims [128h, 128h + 128): one swizzled box of the staged page
+            uint4 raw[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              raw[4 * i + u] = (pi < np) ? ld_shared_v4(src + sw_piece(row & 63, (d & 1) * 4 + u)) : make_uint4(0u, 0u, 0u, 0u);
-          }
+            for (int j = 0; j < 8; ++j) raw[j] = ld_shared_v4(src + h * 8192 + sw_piece(rr, j));
 #pragma unroll
-          for (int i = 0; i < kRows; ++i) {
+            for (int q = 0; q < 2; ++q) {  // 32 columns (64 dims) per store
+              float cols[32];
+              uint32_t* u = reinterpret_cast<uint32_t*>(cols);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int row = tid + i * kDequantThreads;
-              uint4 lo16, hi16;
-              codes16_to_f16(raw[4 * i + u], lo16, hi16);
-              st_shared_v4(dst + sw_piece(row, 2 * u), lo16);
-              st_shared_v4(dst + sw_piece(row, 2 * u + 1), hi16);
+              for (int j = 0; j < 4; ++j) {
+                uint4 lo16, hi16;
+                codes16_to_f16(raw[4 * q + j], lo16, hi16);
+                u[8 * j + 0] = lo16.x; u[8 * j + 1] = lo16.y; u[8 * j + 2] = lo16.z; u[8 * j + 3] = lo16.w;
+                u[8 * j + 4] = hi16.x; u[8 * j + 5] = hi16.y; u[8 * j + 6] = hi16.z; u[8 * j + 7] = hi16.w;
+              }
+              tmem_st32(tmem + lane_base + kTmemK + h * 64 + q * 32, cols);
             }
           }
-          end_chunk();
         }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(cx.bar(Bb::KFull));
+        ++kt;
         release_stage(ka);
         if (np == 2) release_stage(kb);
         st += np;
@@ -613,6 +622,23 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
     const uint32_t buf = s_cnt & 1, n = s_cnt >> 1;
     if (!wait_all(Bb::SEmpty + buf, (n & 1) ^ 1)) return false;
     const uint32_t d_tmem = tmem + buf * 64;
+    if constexpr (kFp8) {
+      // A = the f16 K tile the dequantisation warps wrote to TMEM (one MMA per 16 dims)
+      if (!wait_all(Bb::KFull, s_cnt & 1)) return false;
+      if (lane == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t b0 = cx.base + L.q + qb * kQBytes + (k >> 2) * 8192 + (k & 3) * 32;
+          tc_mma_tmem_a(d_tmem, tmem + kTmemK + 8 * k, smem_desc_sw128(b0, 16, 1024), idesc_s<kFp8>(), k != 0);
+        }
+        tc_commit(cx.bar(Bb::KFree));
+        tc_commit(cx.bar(Bb::SFull + buf));
+      }
+      __syncwarp();
+      ++s_cnt;
+      return true;
+    }
     for (int d = 0; d < 4; ++d) {
       const uint32_t slot = cc % C::kSlots, ph = (cc / C::kSlots) & 1;
       if (!wait_all(Bb::Full + slot, ph)) return false;
@@ -1000,6 +1026,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(bars + 8 * (Bb::ScFull + i), 1);
       mbar_init(bars + 8 * (Bb::ScEmpty + i), kSoftmaxThreads);
     }
+    mbar_init(bars + 8 * Bb::KFull, kDequantThreads);
+    mbar_init(bars + 8 * Bb::KFree, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1039,7 +1067,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   } else if (warp == kMmaWarp) {
     mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
-    if (warp >= kDequantWarp0) dequant_role(p, cx, s_cost, s_len, lo, hi);
+    if (warp >= kDequantWarp0) dequant_role(p, cx, s_cost, s_len, lo, hi, tmem);
   }
   tc_fence_before();
   __syncthreads();
