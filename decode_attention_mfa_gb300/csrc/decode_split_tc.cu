@@ -59,20 +59,24 @@ struct Cfg<false> {
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
 };
-// E4M3: warps 8-11 (a warpgroup) convert codes to f16; warps 6-7 idle. The
-// three warpgroups split the registers: the softmax warpgroup grows to
-// kRegSoftmax, the other two shrink to kRegOther (setmaxnreg), within the
-// 384 x 168 registers the block is launched with.
-constexpr int kDequantThreads = 128;
+// E4M3: two warpgroups (warps 8-11 and 12-15) convert codes to f16; warps
+// 6-7 idle. The four warpgroups split the registers with setmaxnreg: the
+// softmax warpgroup grows to kRegSoftmax, the producer/MMA warpgroup shrinks
+// to kRegIssue and the dequantisation warpgroups to kRegDequant, within the
+// 512 x 128 registers the block is launched with.
+constexpr int kDequantThreads = 128;               // one dequantisation warpgroup
+constexpr int kDequantAll = 2 * kDequantThreads;   // both
 constexpr int kDequantWarp0 = 8;
-constexpr int kRegSoftmax = 232;
-constexpr int kRegOther = 136;
-constexpr int kRegLaunch = 168;
-static_assert(128 * kRegSoftmax + 256 * kRegOther <= 384 * kRegLaunch, "register split exceeds the launch's registers");
+constexpr int kRegSoftmax = 216;
+constexpr int kRegIssue = 96;
+constexpr int kRegDequant = 96;
+constexpr int kRegLaunch = 128;
+static_assert(128 * kRegSoftmax + 128 * kRegIssue + 256 * kRegDequant <= 512 * kRegLaunch,
+              "register split exceeds the launch's registers");
 
 template <>
 struct Cfg<true> {
-  static constexpr int kThreads = 384;
+  static constexpr int kThreads = 512;
   static constexpr int kSlots = 3;
   static constexpr int kStages = 6;
   static constexpr int kQBufs = 1;
@@ -462,7 +466,7 @@ __device__ __forceinline__ uint32_t sw_piece(int r, int j) { return (uint32_t)(r
 
 // Bf16 Q (TMA, 128-byte swizzle) -> f16 in place: same element positions.
 __device__ __forceinline__ void convert_q_to_f16(uint32_t q_addr, int tid) {
-  for (int i = tid; i < kQBytes / 16; i += kDequantThreads) {
+  for (int i = tid; i < kQBytes / 16; i += kDequantAll) {
     const uint4 v = ld_shared_v4(q_addr + 16 * i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
@@ -479,7 +483,9 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
                              long long lo, long long hi, uint32_t tmem) {
   using C = Cfg<true>;
   using Bb = Bars<true>;
-  const int tid = threadIdx.x - kDequantWarp0 * 32;  // 0 .. kDequantThreads - 1
+  const int all = threadIdx.x - kDequantWarp0 * 32;  // 0 .. kDequantAll - 1
+  const int g = all / kDequantThreads;               // this thread's warpgroup: 128-dim half it converts
+  const int tid = all % kDequantThreads;             // 0 .. kDequantThreads - 1
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quadrant
   uint32_t kt = 0;                                              // K tiles written to TMEM
@@ -506,7 +512,7 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
     if (*cx.abort) return;
     // Q of this piece: bf16 -> f16
     if (!cx.wait(Bb::QFull, seg_i & 1)) return;
-    convert_q_to_f16(cx.base + L.q, tid);
+    convert_q_to_f16(cx.base + L.q, all);
     fence_proxy_async_smem();
     mbar_arrive(cx.bar(Bb::QReady));
     ++seg_i;
@@ -515,8 +521,9 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
       if (t < T) {
         // K(t) goes to TMEM as the A operand of S^T: this thread writes token
         // row r of the tile (its TMEM lane; rows 64-127 come from the second
-        // page), 256 dims as 128 columns of f16 pairs. Rows past the tile's
-        // pages keep whatever they held: their logits are masked.
+        // page), 128 of its 256 dims (warpgroup g: dims [128g, 128g + 128))
+        // as 64 columns of f16 pairs. Rows past the tile's pages keep whatever
+        // they held: their logits are masked.
         const int np = pages_in_tile(s, t);
         const uint32_t ka = st, kb = st + 1;
         if (!wait_stage(ka) || (np == 2 && !wait_stage(kb))) return;
@@ -525,8 +532,8 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
         const int r = 32 * (warp & 3) + lane, pi = r >> 6, rr = r & 63;
         if (pi < np) {
           const uint32_t src = stage_addr(pi ? kb : ka);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {  // dims [128h, 128h + 128): one swizzled box of the staged page
+          {
+            const int h = g;  // dims [128h, 128h + 128): one swizzled box of the staged page
             uint4 raw[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) raw[j] = ld_shared_v4(src + h * 8192 + sw_piece(rr, j));
@@ -562,6 +569,10 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
           if (!wait_stage(k)) return;
           const int nv = min(kPageSize, s.len - (pgv + pi) * kPageSize);  // valid rows of this page
           for (int hf = 0; hf < 2; ++hf) {
+            if (hf != g) {  // the other warpgroup's chunk
+              ++cc;
+              continue;
+            }
             uint32_t dst;
             if (!begin_chunk(dst)) return;
             // units (64-dim block, row) = tid, tid + kDequantThreads, ...; rows past
@@ -1009,7 +1020,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars + 8 * (Bb::QFull + i), 1);
       mbar_init(bars + 8 * (Bb::QEmpty + i), 1);
-      mbar_init(bars + 8 * (Bb::QReady + i), kDequantThreads);
+      mbar_init(bars + 8 * (Bb::QReady + i), kDequantAll);
       mbar_init(bars + 8 * (Bb::SFull + i), 1);
       mbar_init(bars + 8 * (Bb::SEmpty + i), kSoftmaxThreads);
       mbar_init(bars + 8 * (Bb::PFull + i), kSoftmaxThreads);
@@ -1020,13 +1031,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(bars + 8 * Bb::Drain, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bars + 8 * (Bb::StFull + i), 1);
-      mbar_init(bars + 8 * (Bb::StEmpty + i), kDequantThreads);
+      mbar_init(bars + 8 * (Bb::StEmpty + i), kDequantAll);
     }
     for (int i = 0; i < C::kScaleSlots; ++i) {
       mbar_init(bars + 8 * (Bb::ScFull + i), 1);
       mbar_init(bars + 8 * (Bb::ScEmpty + i), kSoftmaxThreads);
     }
-    mbar_init(bars + 8 * Bb::KFull, kDequantThreads);
+    mbar_init(bars + 8 * Bb::KFull, kDequantAll);
     mbar_init(bars + 8 * Bb::KFree, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -1057,8 +1068,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   if constexpr (kFp8) {  // whole warpgroups execute these
     if (warp < 4)
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
+    else if (warp < kDequantWarp0)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegIssue));
     else
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegDequant));
   }
   if (warp < 4) {
     softmax_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
