@@ -133,14 +133,29 @@ def used_slots_equal(a, b, lengths, page_table):
     return np.array_equal(fa[slots].view(np.uint8), fb[slots].view(np.uint8))
 
 
-def compare(out_gpu, lse_gpu, out_ref, lse_ref, label=""):
-    """Tolerance check against the oracle; returns the error figures."""
+# Relative half-ulp of bf16 (8 significant bits): storing a value v in bf16
+# can move it by up to 2^-8 |v|, which exceeds MAX_ABS once |v| >= 2.56.
+BF16_HALF_ULP = 2.0 ** -8
+
+
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, label="", bf16_storage_slack=False):
+    """Tolerance check against the oracle; returns the error figures.
+
+    With `bf16_storage_slack` the absolute bound is applied element by element
+    as MAX_ABS + 2^-8 |ref|: the output is stored in bf16, so outputs of
+    magnitude >= 2.56 (short sequences, where out is a near-copy of a few V
+    rows) cannot be held to MAX_ABS even when computed exactly. The five
+    benchmark workloads average thousands of rows and use the plain bound."""
     o = out_gpu.float().cpu().numpy().astype(np.float64)
     l = lse_gpu.cpu().numpy().astype(np.float64)
     finite_ref = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(l), finite_ref), f"{label}: LSE finiteness differs"
     assert np.all(np.isfinite(o)), f"{label}: non-finite output"
-    max_abs = float(np.max(np.abs(o - out_ref))) if o.size else 0.0
+    if bf16_storage_slack and o.size:
+        excess = np.abs(o - out_ref) - BF16_HALF_ULP * np.abs(out_ref)
+        max_abs = float(np.max(excess))
+    else:
+        max_abs = float(np.max(np.abs(o - out_ref))) if o.size else 0.0
     denom = float(np.linalg.norm(out_ref))
     rel_l2 = float(np.linalg.norm(o - out_ref) / denom) if denom > 0 else float(np.linalg.norm(o))
     dl = float(np.max(np.abs(l[finite_ref] - lse_ref[finite_ref]))) if finite_ref.any() else 0.0

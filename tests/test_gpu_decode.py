@@ -114,6 +114,30 @@ def test_split_count_invariance(oracle_mod, kv):
         compare(dev.out, dev.lse, out_ref, lse_ref, f"{kv}/hint={hint}")
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_maximum_batch(oracle_mod, kv):
+    """The largest batch the ABI accepts (MFA_MAX_BATCH sequences): the largest
+    shared-memory layout of the split kernel and the widest combine grid.
+    Short ragged lengths (two start empty), one appended token per sequence."""
+    rng = np.random.default_rng(123)
+    lengths = [int(x) for x in rng.integers(0, 260, size=capi.MAX_BATCH)]
+    lengths[5] = lengths[700] = 0
+    w = wl.Workload("max_batch", len(lengths), ("list", tuple(lengths)), kv, True, 1, 13)
+    case = wl.make_case(w, lengths=lengths)
+    dev = DeviceCache(case, kv)
+    k_new = wl.draw_rows(len(lengths), wl.HEAD_DIM, [13, 1], 21).view(len(lengths), 1, wl.HEAD_DIM)
+    v_new = wl.draw_rows(len(lengths), wl.HEAD_DIM, [13, 2], 22).view(len(lengths), 1, wl.HEAD_DIM)
+    dev.append(k_new, v_new)
+    dev.attend()
+    dev.check_errors()
+    kc, vc, ks, vs, sl = oracle_caches(oracle_mod, case, kv)
+    oracle_mod.kv_append(wl.bits(k_new), wl.bits(v_new), kc, vc, case.page_table, sl, k_scale=ks, v_scale=vs)
+    assert np.array_equal(dev.seq_lens.cpu().numpy(), sl)
+    out_ref, lse_ref = oracle_mod.mfa_decode(wl.bits(case.q), kc, vc, case.page_table, sl, wl.SCALE,
+                                             k_scale=ks, v_scale=vs)
+    compare(dev.out, dev.lse, out_ref, lse_ref, f"{kv}/B={len(lengths)}", bf16_storage_slack=True)
+
+
 def test_bad_page_and_capacity_set_error_word():
     case = _case([200, 50], seed=10)
     dev = DeviceCache(case, "bf16")
