@@ -53,14 +53,17 @@ template <>
 struct Cfg<false> {
   static constexpr int kThreads = 192;
   static constexpr int kSlots = 7;       // 16 KB operand chunks
-  static constexpr int kStages = 0;      // raw code pages
+  static constexpr int kKStages = 0;     // raw code pages: K ring
+  static constexpr int kVStages = 0;     // raw code pages: V ring
+  static constexpr int kStages = 0;
   static constexpr int kQBufs = 2;
   static constexpr bool kCrossPiece = true;  // one tile stream across sequence pieces
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
 };
-// E4M3: two warpgroups (warps 8-11 and 12-15) convert codes to f16; warps
-// 6-7 idle. The four warpgroups split the registers with setmaxnreg: the
+// E4M3: warp 6 stages the V pages (warp 4 the K pages, scales and Q), warp 7
+// finds each piece's largest V scale; two warpgroups (warps 8-11 and 12-15)
+// convert the K tiles to f16 into TMEM (one 128-dim half each) and Q. The four warpgroups split the registers with setmaxnreg: the
 // softmax warpgroup grows to kRegSoftmax, the producer/MMA warpgroup shrinks
 // to kRegIssue and the dequantisation warpgroups to kRegDequant, within the
 // 512 x 128 registers the block is launched with.
@@ -77,8 +80,10 @@ static_assert(128 * kRegSoftmax + 128 * kRegIssue + 256 * kRegDequant <= 512 * k
 template <>
 struct Cfg<true> {
   static constexpr int kThreads = 512;
-  static constexpr int kSlots = 3;
-  static constexpr int kStages = 6;
+  static constexpr int kSlots = 0;        // V is read raw (8-bit MMA), K goes to TMEM: no operand ring
+  static constexpr int kKStages = 3;      // raw K pages (converted into TMEM)
+  static constexpr int kVStages = 5;      // raw V pages (the A operand of the 8-bit P.V MMAs)
+  static constexpr int kStages = kKStages + kVStages;
   static constexpr int kQBufs = 1;
   static constexpr bool kCrossPiece = false;  // per-piece order (a single Q buffer)
   static constexpr int kScaleSlots = 4;
@@ -87,6 +92,8 @@ struct Cfg<true> {
 
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
+constexpr int kVProducerWarp = 6;         // E4M3 only
+constexpr int kVRefWarp = 7;              // E4M3 only
 constexpr int kMmaWarp = 5;
 constexpr int kSlotBytes = 16384;
 constexpr int kStageBytes = 16384;        // one E4M3 page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
@@ -99,7 +106,15 @@ constexpr int kTmemK = 384;               // E4M3: the f16 K tile (A operand of 
 constexpr int kMaxBars = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f; // log2 units: P stays below 2^8
+// log2 units: P stays below 2^threshold between rescales. E4M3 keeps P within
+// 2^3 so that P's bulk sits in the normal range of the 8-bit P operand.
+template <bool kFp8>
+__host__ __device__ constexpr float rescale_threshold() { return kFp8 ? 3.0f : 8.0f; }
+// E4M3: the P operand is x = P * v_scale / vref * 2^5 <= 2^3 * 1 * 2^5 = 256 < 448
+// (vref = the piece's largest V scale), split into two E4M3 terms x1 + x2.
+constexpr float kPScale = 32.0f;
+constexpr int kPTerms = 2;
+constexpr int kPTermBytes = 128 * 64;     // one term: [128 tokens x 64 heads] E4M3
 
 template <bool kFp8>
 struct Bars {  // indices into the barrier array
@@ -121,7 +136,9 @@ struct Bars {  // indices into the barrier array
   static constexpr int ScEmpty = ScFull + C::kScaleSlots;
   static constexpr int KFull = ScEmpty + C::kScaleSlots;  // E4M3: f16 K tile written to TMEM
   static constexpr int KFree = KFull + 1;                 // E4M3: the S MMAs that read it are done
-  static constexpr int Count = KFree + 1;
+  static constexpr int VRefFull = KFree + 1;              // [2] E4M3: a piece's largest V scale is known
+  static constexpr int VRefEmpty = VRefFull + 2;          // [2] E4M3: the softmax has read it
+  static constexpr int Count = VRefEmpty + 2;
   static_assert(Count <= kMaxBars, "barrier array too small");
 };
 
@@ -132,6 +149,10 @@ __host__ __device__ constexpr uint32_t idesc_s() {  // A = K tile (K-major), B =
 template <bool kFp8>
 __host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = P^T (head-major)
   return idesc_f16(128, 64, Cfg<kFp8>::kAbFormat, 1, 1);
+}
+// kind::f8f6f4, A and B E4M3 (format 0), both dim/head-major, fp32 accumulate, M=128 N=64
+__host__ __device__ constexpr uint32_t idesc_o_e4m3() {
+  return (1u << 4) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 struct SmemLayout {
@@ -151,8 +172,8 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
   L.scales = L.p + 2 * kPBytes;
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
-  L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64], inv_l[2][64]
-  L.bars = L.red + 8 * 64 * 4;                    // mbarriers
+  L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64], inv_l[2][64], vref[2]
+  L.bars = (L.red + 8 * 64 * 4 + 8 + 7) & ~7u;    // mbarriers
   L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
   L.total = L.misc + 16;
   return L;
@@ -276,7 +297,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged pages (E4M3); pieces; tiles
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
-  constexpr int kRing = kFp8 ? C::kStages : C::kSlots;
+  constexpr int kRing = kFp8 ? C::kKStages : C::kSlots;  // E4M3: the K stage ring (V pages: warp 6)
   constexpr int kRingFull = kFp8 ? Bb::StFull : Bb::Full;
   constexpr int kRingEmpty = kFp8 ? Bb::StEmpty : Bb::Empty;
   auto wait_slot = [&](uint32_t& dst, uint32_t& bar) -> bool {
@@ -401,15 +422,12 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
           for (int d = 0; good && d < 4; ++d) good = issue_k(d, pa, pb);
         }
       }
-      if (good && t > 0) {
+      if (!kFp8 && good && t > 0) {
         const int pgv = s.pg0 + 2 * (t - 1);
         const int np = pages_in_tile(s, t - 1);
         for (int i = 0; good && i < np; ++i) {
           const int pv = ids.get(pgv + i, p, lane);
-          if constexpr (kFp8)
-            good = stage_page(vmap, pv);
-          else
-            good = issue_v(0, pv) && issue_v(1, pv);
+          good = issue_v(0, pv) && issue_v(1, pv);
         }
       }
     }
@@ -432,6 +450,98 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     if (issued_q) (void)mbar_wait(cx.bar(Bb::QFull + last_qb), last_q_parity, cx.budget, nullptr, p.err);
   }
   __syncwarp();
+}
+
+// E4M3: the V pages of every tile, in order, into the V stage ring (its own
+// warp, so K pages are never queued behind V pages waiting for P.V). A slot
+// is freed by the commit of the P.V MMAs that read it.
+__device__ void producer_v_role(const DecodeParams& p, const CUtensorMap* vmap, const Ctx& cx, const int* s_cost,
+                                const int* s_len, long long lo, long long hi) {
+  using C = Cfg<true>;
+  using Bb = Bars<true>;
+  const int lane = threadIdx.x & 31;
+  const uint64_t pol_stream = policy_evict_first();
+  const SmemLayout L = smem_layout<true>(p.B);
+  uint32_t vc = 0;  // V pages staged
+  Seg s;
+  bool ok = seg_first(s_cost, p.B, lo, hi, s);
+  bool good = true;
+  while (good && ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
+    if (*cx.abort) break;
+    PageIds ids;
+    ids.row = p.page_table + (size_t)s.b * p.max_pages;
+    ids.pg1 = s.pg1;
+    ids.start(s.pg0, p, lane);
+    for (int pg = s.pg0; good && pg < s.pg1; ++pg) {
+      const int id = ids.get(pg, p, lane);
+      const uint32_t slot = C::kKStages + vc % C::kVStages, n = vc / C::kVStages;
+      good = cx.wait(Bb::StEmpty + slot, (n & 1) ^ 1);
+      __syncwarp();
+      if (good && lane == 0) {
+        const uint32_t dst = cx.base + L.stage + slot * kStageBytes, bar = cx.bar(Bb::StFull + slot);
+        mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
+        tma_load_2d(dst, vmap, 0, id * kPageSize, bar, pol_stream);
+        tma_load_2d(dst + 8192, vmap, 128, id * kPageSize, bar, pol_stream);
+      }
+      if (good) ++vc;
+    }
+  }
+  // drain: every copy this warp issued must land before the CTA exits
+  if (lane == 0) {
+    for (uint32_t k = (vc > (uint32_t)C::kVStages ? vc - C::kVStages : 0); k < vc; ++k)
+      (void)mbar_wait(cx.bar(Bb::StFull + C::kKStages + k % C::kVStages), (k / C::kVStages) & 1, cx.budget, nullptr,
+                      p.err);
+  }
+  __syncwarp();
+}
+
+// E4M3: the largest V scale of each sequence piece (vref), published for the
+// softmax warps before they form the piece's first P (two slots, so this warp
+// works up to two pieces ahead).
+__device__ void vref_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len, long long lo,
+                          long long hi, float* s_vref) {
+  using Bb = Bars<true>;
+  const int lane = threadIdx.x & 31;
+  uint32_t piece = 0;
+  Seg s;
+  bool ok = seg_first(s_cost, p.B, lo, hi, s);
+  while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
+    if (*cx.abort) break;
+    const uint32_t slot = piece & 1, n = piece >> 1;
+    // lane i takes page g + i of each group of 32: its 64 scales in 16 vector loads
+    const int32_t* row = p.page_table + (size_t)s.b * p.max_pages;
+    float mx = 0.0f;
+    for (int g = s.pg0; g < s.pg1; g += 32) {
+      const int pg = g + lane;
+      if (pg < s.pg1) {
+        const int id = __ldg(row + pg);
+        if (id >= 0 && id < p.num_pages) {  // a bad id is reported by the producer warps
+          const int rows = min(kPageSize, s.len - pg * kPageSize);  // scales of unused rows are never read
+          const float4* sc = reinterpret_cast<const float4*>(p.v_scale + (size_t)id * kPageSize);
+          float4 v[16];
+#pragma unroll
+          for (int r4 = 0; r4 < 16; ++r4) v[r4] = (4 * r4 < rows) ? __ldg(sc + r4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int r4 = 0; r4 < 16; ++r4) {
+            if (4 * r4 + 0 < rows) mx = fmaxf(mx, v[r4].x);
+            if (4 * r4 + 1 < rows) mx = fmaxf(mx, v[r4].y);
+            if (4 * r4 + 2 < rows) mx = fmaxf(mx, v[r4].z);
+            if (4 * r4 + 3 < rows) mx = fmaxf(mx, v[r4].w);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (!cx.wait(Bb::VRefEmpty + slot, (n & 1) ^ 1)) break;
+    __syncwarp();
+    if (lane == 0) {
+      s_vref[slot] = mx > 0.0f ? mx : 1.0f;
+      mbar_arrive(cx.bar(Bb::VRefFull + slot));
+    }
+    __syncwarp();
+    ++piece;
+  }
 }
 
 // ---------------------------------------------------------------- dequantisation (E4M3)
@@ -490,24 +600,13 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quadrant
   uint32_t kt = 0;                                              // K tiles written to TMEM
   const SmemLayout L = smem_layout<true>(p.B);
-  uint32_t st = 0, cc = 0, seg_i = 0;    // staged pages consumed, operand chunks produced, pieces
+  uint32_t st = 0, seg_i = 0;            // K pages consumed, pieces
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
-  auto stage_addr = [&](uint32_t k) { return cx.base + L.stage + (k % C::kStages) * kStageBytes; };
-  auto wait_stage = [&](uint32_t k) -> bool { return cx.wait(Bb::StFull + k % C::kStages, (k / C::kStages) & 1); };
-  auto release_stage = [&](uint32_t k) { mbar_arrive(cx.bar(Bb::StEmpty + k % C::kStages)); };
-  // claim the next operand slot; returns its address
-  auto begin_chunk = [&](uint32_t& dst) -> bool {
-    const uint32_t slot = cc % C::kSlots, n = cc / C::kSlots;
-    if (!cx.wait(Bb::Empty + slot, (n & 1) ^ 1)) return false;
-    dst = cx.base + L.ring + slot * kSlotBytes;
-    return true;
-  };
-  auto end_chunk = [&]() {
-    fence_proxy_async_smem();  // the MMA reads the chunk through the async proxy
-    mbar_arrive(cx.bar(Bb::Full + cc % C::kSlots));
-    ++cc;
-  };
+  // the K stage ring (V pages never pass through these warps)
+  auto stage_addr = [&](uint32_t k) { return cx.base + L.stage + (k % C::kKStages) * kStageBytes; };
+  auto wait_stage = [&](uint32_t k) -> bool { return cx.wait(Bb::StFull + k % C::kKStages, (k / C::kKStages) & 1); };
+  auto release_stage = [&](uint32_t k) { mbar_arrive(cx.bar(Bb::StEmpty + k % C::kKStages)); };
   while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
     if (*cx.abort) return;
     // Q of this piece: bf16 -> f16
@@ -517,8 +616,8 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
     mbar_arrive(cx.bar(Bb::QReady));
     ++seg_i;
     const int T = tiles_of(s);
-    for (int t = 0; t <= T; ++t) {
-      if (t < T) {
+    for (int t = 0; t < T; ++t) {
+      {
         // K(t) goes to TMEM as the A operand of S^T: this thread writes token
         // row r of the tile (its TMEM lane; rows 64-127 come from the second
         // page), 128 of its 256 dims (warpgroup g: dims [128g, 128g + 128))
@@ -560,50 +659,6 @@ __device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_
         if (np == 2) release_stage(kb);
         st += np;
       }
-      if (t > 0) {
-        // V(t-1): per page, chunk hf = dims [128hf, 128hf + 128) as two 64-dim blocks
-        const int np = pages_in_tile(s, t - 1);
-        const int pgv = s.pg0 + 2 * (t - 1);
-        for (int pi = 0; pi < np; ++pi) {
-          const uint32_t k = st + pi;
-          if (!wait_stage(k)) return;
-          const int nv = min(kPageSize, s.len - (pgv + pi) * kPageSize);  // valid rows of this page
-          for (int hf = 0; hf < 2; ++hf) {
-            if (hf != g) {  // the other warpgroup's chunk
-              ++cc;
-              continue;
-            }
-            uint32_t dst;
-            if (!begin_chunk(dst)) return;
-            // units (64-dim block, row) = tid, tid + kDequantThreads, ...; rows past
-            // the sequence end become zeros
-            constexpr int kUnits = 128 / kDequantThreads;
-            const uint32_t src = stage_addr(k) + hf * 8192;
-            uint4 raw[4 * kUnits];
-#pragma unroll
-            for (int i = 0; i < kUnits; ++i) {
-              const int unit = tid + i * kDequantThreads, blk = unit >> 6, r = unit & 63;
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                raw[4 * i + u] = (r < nv) ? ld_shared_v4(src + sw_piece(r, blk * 4 + u)) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int i = 0; i < kUnits; ++i) {
-              const int unit = tid + i * kDequantThreads, blk = unit >> 6, r = unit & 63;
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                uint4 lo16, hi16;
-                codes16_to_f16(raw[4 * i + u], lo16, hi16);  // code 0 is +0
-                st_shared_v4(dst + blk * 8192 + sw_piece(r, 2 * u), lo16);
-                st_shared_v4(dst + blk * 8192 + sw_piece(r, 2 * u + 1), hi16);
-              }
-            }
-            end_chunk();
-          }
-          release_stage(k);
-        }
-        st += np;
-      }
     }
   }
 }
@@ -617,6 +672,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   const int lane = threadIdx.x & 31;
   const SmemLayout L = smem_layout<kFp8>(p.B);
   uint32_t cc = 0, seg_i = 0, s_cnt = 0, p_cnt = 0;
+  uint32_t vc = 0;  // E4M3: V pages consumed from the V stage ring
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
   bool alive = true;
@@ -682,6 +738,43 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
     if (!wait_all(Bb::PFull + buf, n & 1)) return false;
     const int pga = sg.pg0 + 2 * t;
     const int np = pages_in_tile(sg, t);
+    if constexpr (kFp8) {
+      // 8-bit P.V: A = the raw staged V page (dims x tokens, 128-byte swizzle,
+      // one 128-dim box per half), B = the P terms (tokens x heads, 64-byte
+      // swizzle); K = 32 tokens per MMA, two terms accumulated in place
+      for (int i = 0; i < np; ++i) {
+        const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page
+        const uint32_t vslot = C::kKStages + vc % C::kVStages;
+        if (!wait_all(Bb::StFull + vslot, (vc / C::kVStages) & 1)) return false;
+        const uint32_t vs = cx.base + L.stage + vslot * kStageBytes;
+        if (nv < kPageSize) {
+          // rows [nv, 64) of both boxes (whole 128 B rows): code 0x7F is NaN and 0 * NaN would poison P.V
+          const int nbytes = (kPageSize - nv) * 128;
+          for (int off = lane * 16; off < nbytes; off += 32 * 16) {
+            st_shared_v4(vs + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
+            st_shared_v4(vs + 8192 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 4096;  // token rows 64i.. of each term
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+              for (int tm = 0; tm < kPTerms; ++tm)
+                tc_mma_f8(tmem + kTmemO + obuf * 128 + hf * 64, smem_desc(vs + hf * 8192 + ks * 4096, 16, 1024, 2),
+                          smem_desc(bp + tm * kPTermBytes + ks * 2048, 16, 512, 4), idesc_o_e4m3(),
+                          !(first_of_seg && i == 0 && ks == 0 && tm == 0));
+          tc_commit(cx.bar(Bb::StEmpty + vslot));  // the V page's stage is free once these MMAs are done
+        }
+        __syncwarp();
+        ++vc;
+      }
+    } else {
     for (int i = 0; i < np; ++i) {
       const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page
       for (int hf = 0; hf < 2; ++hf) {
@@ -712,6 +805,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         __syncwarp();
         ++cc;
       }
+    }
     }
     if (lane == 0) {
       tc_commit(cx.bar(Bb::PEmpty + buf));
@@ -838,6 +932,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
   float* alpha = mref + 64;                              // [64] rescale factors, uniform
   float* inv_l = alpha + 64;                             // [2][64] 1/l of the piece in O^T buffer i
+  float* s_vref = inv_l + 128;                           // [2] E4M3: largest V scale of a piece
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
   const uint32_t taddr_o0 = tmem + lane_base + kTmemO;
   const float c2 = p.scale * kLog2e;
@@ -885,6 +980,15 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
     const uint32_t obuf = piece & 1;
     const uint32_t taddr_o = taddr_o0 + obuf * 128;
+    // E4M3: P enters the 8-bit P.V as P * v_scale * pscale (<= 256); O^T is
+    // then pscale times too large, which the epilogue undoes
+    float pscale = 1.0f;
+    if constexpr (kFp8) {
+      const uint32_t vslot = piece & 1;
+      if (!cx.wait(Bb::VRefFull + vslot, (piece >> 1) & 1)) return;
+      pscale = kPScale / s_vref[vslot];
+      mbar_arrive(cx.bar(Bb::VRefEmpty + vslot));
+    }
     if (tid < 64) mref[tid] = -INFINITY;
     named_barrier_softmax();
     float lp[64];  // this thread's share of the softmax denominators
@@ -902,7 +1006,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         const float* sc = reinterpret_cast<const float*>(gbase + L.scales + slot * kScaleBytes);
         if (valid) {
           kmul = c2 * sc[tid];
-          vmul = sc[128 + tid];
+          vmul = sc[128 + tid] * pscale;
         }
         mbar_arrive(cx.bar(Bb::ScEmpty + slot));
       }
@@ -914,7 +1018,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       load_logits(taddr_s, valid, kmul, x);
       bool mine = false;
 #pragma unroll
-      for (int h = 0; h < 64; ++h) mine |= x[h] > mref[h] + kRescaleThreshold;
+      for (int h = 0; h < 64; ++h) mine |= x[h] > mref[h] + rescale_threshold<kFp8>();
       // ---- does any logit of the tile exceed its reference maximum by 2^8?
       if (named_barrier_softmax_or(mine)) {
         warp_reduce_scatter_max(x, lane);  // x is reloaded below
@@ -948,22 +1052,54 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       mbar_arrive(cx.bar(Bb::SEmpty + sbuf));  // S^T buffer free for the tile after next
       ++s_cnt;
       // ---- P = exp2(x - mref): row sums in fp32; P^T row (times the V scale) in 16 bits
-      uint32_t packed[32];
+      uint32_t packed[32];  // bf16: this token's 64 P values; E4M3: 16 words per term
 #pragma unroll
       for (int h = 0; h < 64; h += 2) {
         const float p0 = ex2_approx(x[h] - mref[h]);
         const float p1 = ex2_approx(x[h + 1] - mref[h + 1]);
         lp[h] += p0;
         lp[h + 1] += p1;
-        packed[h >> 1] = kFp8 ? pack2<kFp8>(p0 * vmul, p1 * vmul) : pack2<kFp8>(p0, p1);
+        if constexpr (kFp8) {
+          // x = P * v_scale * 2^5 / vref in [0, 256], as x1 + x2 (E4M3): x2 rounds x - x1,
+          // formed in f16 (x1 is exact in f16, and so is the difference)
+          const __half2 xh = __floats2half2_rn(p0 * vmul, p1 * vmul);
+          const __nv_fp8x2_storage_t c1 =
+              __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&xh), __NV_SATFINITE, __NV_E4M3);
+          const __half2_raw d1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+          const __half2 rh = __hsub2(xh, *reinterpret_cast<const __half2*>(&d1));
+          const __nv_fp8x2_storage_t c2 =
+              __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rh), __NV_SATFINITE, __NV_E4M3);
+          const int w = h >> 2, sh = (h & 2) ? 16 : 0;  // two heads per 16 bits, four per word
+          if (sh == 0) {
+            packed[w] = (uint32_t)c1;
+            packed[16 + w] = (uint32_t)c2;
+          } else {
+            packed[w] |= (uint32_t)c1 << 16;
+            packed[16 + w] |= (uint32_t)c2 << 16;
+          }
+        } else {
+          packed[h >> 1] = pack2<kFp8>(p0, p1);
+        }
       }
       const uint32_t pbuf = p_cnt & 1;
       if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
-      const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
+      if constexpr (kFp8) {
+        // term tm, token row tid: 64 B, 16 B chunk j at ((j ^ ((row >> 1) & 3)) << 4) (64-byte swizzle)
+        const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 64;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        st_shared_v4(prow + ((j ^ (tid & 7)) << 4),
-                     make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]));
+        for (int tm = 0; tm < kPTerms; ++tm)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(prow + tm * kPTermBytes + ((j ^ ((tid >> 1) & 3)) << 4),
+                         make_uint4(packed[16 * tm + 4 * j], packed[16 * tm + 4 * j + 1], packed[16 * tm + 4 * j + 2],
+                                    packed[16 * tm + 4 * j + 3]));
+      } else {
+        const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(prow + ((j ^ (tid & 7)) << 4),
+                       make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]));
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(cx.bar(Bb::PFull + pbuf));
@@ -980,7 +1116,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const size_t slot = (size_t)c + s.b;
     if (tid < 64) {
       const float l = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
-      inv_l[obuf * 64 + tid] = 1.0f / l;
+      inv_l[obuf * 64 + tid] = 1.0f / (l * pscale);
       p.part_lse[slot * kHeads + tid] = (mref[tid] + log2f(l)) * kLn2;
     }
     named_barrier_softmax();
@@ -1031,7 +1167,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(bars + 8 * Bb::Drain, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bars + 8 * (Bb::StFull + i), 1);
-      mbar_init(bars + 8 * (Bb::StEmpty + i), kDequantAll);
+      // K pages are released by both dequantisation warpgroups, V pages by the P.V commit
+      mbar_init(bars + 8 * (Bb::StEmpty + i), i < C::kKStages ? kDequantAll : 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars + 8 * (Bb::VRefFull + i), 1);
+      mbar_init(bars + 8 * (Bb::VRefEmpty + i), kSoftmaxThreads);
     }
     for (int i = 0; i < C::kScaleSlots; ++i) {
       mbar_init(bars + 8 * (Bb::ScFull + i), 1);
@@ -1080,7 +1221,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   } else if (warp == kMmaWarp) {
     mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
-    if (warp >= kDequantWarp0) dequant_role(p, cx, s_cost, s_len, lo, hi, tmem);
+    if (warp == kVProducerWarp)
+      producer_v_role(p, &vmap, cx, s_cost, s_len, lo, hi);
+    else if (warp == kVRefWarp)
+      vref_role(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 8 * 64);
+    else if (warp >= kDequantWarp0)
+      dequant_role(p, cx, s_cost, s_len, lo, hi, tmem);
   }
   tc_fence_before();
   __syncthreads();
