@@ -26,17 +26,19 @@
 //              epilogue (row-sum reduction, O^T / l, partial LSE).
 //   warp 4     producer: page-table walk and TMA loads.
 //   warp 5     MMA issue (lane 0) and TMEM allocation.
-//   warps 6-7  (E4M3 cache only) dequantisation.
+//   warp 6     (E4M3 cache only) V page producer.
+//   warp 7     (E4M3 cache only) largest V scale of each piece.
 // bf16 cache: the producer loads 16 KB operand chunks (a 64-dim slice of a
 // 2-page K tile, or a 128-dim slice of one V page) straight into a ring of
 // shared-memory slots in the layouts the MMAs read; the MMA warp zeroes the
 // unused rows of a partial last V page (0 * NaN would poison P.V).
-// E4M3 cache ("Step-3 is Large yet Affordable", section 7: 8-bit KV): the
-// producer stages raw code pages (and each tile's per-token scales) and the
-// dequantisation warps turn them into f16 operand chunks of the same layouts
-// (E4M3 -> f16 is exact); the MMAs run as f16 x f16 with Q converted to f16.
-// The K scale multiplies the logits and the V scale is folded into P, both in
-// fp32 in the softmax warps (the row sums use the unscaled P).
+// E4M3 cache ("Step-3 is Large yet Affordable", section 7: 8-bit KV): both
+// products are 8-bit MMAs (kind::f8f6f4) on the raw code pages as TMA stages
+// them. Q enters S^T as two E4M3 terms (a per-head power-of-two scale, then
+// q = t1 + t2 holds every bf16 value down to 2^-10 of the scaled range); P
+// enters P.V as two E4M3 terms of P * v_scale, relative to the piece's
+// largest V scale. The K scale, the Q scale and the softmax scale multiply
+// the logits in fp32 in the softmax warps (the row sums use the unscaled P).
 // Every mbarrier wait is bounded (wait budget); on expiry the kernel records
 // MFA_DEVERR_TIMEOUT, the roles stop issuing work and the CTA drains and exits.
 #include <cuda_fp16.h>
@@ -61,33 +63,19 @@ struct Cfg<false> {
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
 };
-// E4M3: warp 6 stages the V pages (warp 4 the K pages, scales and Q), warp 7
-// finds each piece's largest V scale; two warpgroups (warps 8-11 and 12-15)
-// convert the K tiles to f16 into TMEM (one 128-dim half each) and Q. The four warpgroups split the registers with setmaxnreg: the
-// softmax warpgroup grows to kRegSoftmax, the producer/MMA warpgroup shrinks
-// to kRegIssue and the dequantisation warpgroups to kRegDequant, within the
-// 512 x 128 registers the block is launched with.
-constexpr int kDequantThreads = 128;               // one dequantisation warpgroup
-constexpr int kDequantAll = 2 * kDequantThreads;   // both
-constexpr int kDequantWarp0 = 8;
-constexpr int kRegSoftmax = 216;
-constexpr int kRegIssue = 96;
-constexpr int kRegDequant = 96;
-constexpr int kRegLaunch = 128;
-static_assert(128 * kRegSoftmax + 128 * kRegIssue + 256 * kRegDequant <= 512 * kRegLaunch,
-              "register split exceeds the launch's registers");
-
+// E4M3: warp 4 stages the K tiles and scales, warp 6 the V pages, warp 7
+// finds each piece's largest V scale; both products run as 8-bit MMAs on the
+// raw staged pages, so no code is converted on chip.
 template <>
 struct Cfg<true> {
-  static constexpr int kThreads = 512;
-  static constexpr int kSlots = 0;        // V is read raw (8-bit MMA), K goes to TMEM: no operand ring
-  static constexpr int kKStages = 3;      // raw K pages (converted into TMEM)
-  static constexpr int kVStages = 5;      // raw V pages (the A operand of the 8-bit P.V MMAs)
+  static constexpr int kThreads = 256;
+  static constexpr int kSlots = 0;        // K and V are read raw by 8-bit MMAs: no operand ring
+  static constexpr int kKStages = 2;      // raw K tiles (both pages of a tile, 32 KB): A of S^T
+  static constexpr int kVStages = 4;      // raw V pages (16 KB): A of P.V
   static constexpr int kStages = kKStages + kVStages;
-  static constexpr int kQBufs = 1;
+  static constexpr int kQBufs = 1;        // bf16 Q, split in place into two E4M3 terms
   static constexpr bool kCrossPiece = false;  // per-piece order (a single Q buffer)
   static constexpr int kScaleSlots = 4;
-  static constexpr int kAbFormat = 0;    // f16 operands
 };
 
 constexpr int kSoftmaxThreads = 128;
@@ -96,13 +84,15 @@ constexpr int kVProducerWarp = 6;         // E4M3 only
 constexpr int kVRefWarp = 7;              // E4M3 only
 constexpr int kMmaWarp = 5;
 constexpr int kSlotBytes = 16384;
-constexpr int kStageBytes = 16384;        // one E4M3 page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
+constexpr int kStageBytes = 16384;        // one E4M3 V page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
+constexpr int kKTileBytes = 32768;        // one E4M3 K tile: box h (dims [128h, 128h+128)) of 128 rows at 16 KB * h
+constexpr int kQTerms = 2;                // E4M3: Q as two E4M3 terms (per-head power-of-two scale)
+constexpr int kQTermBytes = 16384;        // one term: 2 boxes of [64 heads x 128 B], 128-byte swizzle
 constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]
 constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads], 16-bit
 constexpr int kScaleBytes = 1024;         // per tile: 128 K scales, then 128 V scales
 constexpr int kTmemCols = 512;            // S^T x2 (64 cols each) + O^T x2 (128 cols each)
 constexpr int kTmemO = 128;               // first O^T column; buffer o at kTmemO + 128 * o
-constexpr int kTmemK = 384;               // E4M3: the f16 K tile (A operand of S^T), 256 dims in 128 columns
 constexpr int kMaxBars = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -123,20 +113,18 @@ struct Bars {  // indices into the barrier array
   static constexpr int Empty = Full + C::kSlots;     // [kSlots] operand chunk consumed
   static constexpr int QFull = Empty + C::kSlots;    // [2] Q landed
   static constexpr int QEmpty = QFull + 2;           // [2] every S MMA of the piece done
-  static constexpr int QReady = QEmpty + 2;          // [2] Q converted to f16 (E4M3 only)
+  static constexpr int QReady = QEmpty + 2;          // [2] Q split into E4M3 terms (E4M3 only)
   static constexpr int SFull = QReady + 2;           // [2]
   static constexpr int SEmpty = SFull + 2;           // [2]
   static constexpr int PFull = SEmpty + 2;           // [2]
   static constexpr int PEmpty = PFull + 2;           // [2]
   static constexpr int OFree = PEmpty + 2;           // [2] one completion per epilogue of a piece using O^T buffer i
   static constexpr int Drain = OFree + 2;
-  static constexpr int StFull = Drain + 1;           // [kStages] raw page landed
-  static constexpr int StEmpty = StFull + C::kStages;   // [kStages] raw page converted
+  static constexpr int StFull = Drain + 1;           // [kStages] raw K tile / V page landed
+  static constexpr int StEmpty = StFull + C::kStages;   // [kStages] the MMAs reading it are done
   static constexpr int ScFull = StEmpty + C::kStages;   // [kScaleSlots]
   static constexpr int ScEmpty = ScFull + C::kScaleSlots;
-  static constexpr int KFull = ScEmpty + C::kScaleSlots;  // E4M3: f16 K tile written to TMEM
-  static constexpr int KFree = KFull + 1;                 // E4M3: the S MMAs that read it are done
-  static constexpr int VRefFull = KFree + 1;              // [2] E4M3: a piece's largest V scale is known
+  static constexpr int VRefFull = ScEmpty + C::kScaleSlots;  // [2] E4M3: a piece's largest V scale is known
   static constexpr int VRefEmpty = VRefFull + 2;          // [2] E4M3: the softmax has read it
   static constexpr int Count = VRefEmpty + 2;
   static_assert(Count <= kMaxBars, "barrier array too small");
@@ -150,6 +138,8 @@ template <bool kFp8>
 __host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = P^T (head-major)
   return idesc_f16(128, 64, Cfg<kFp8>::kAbFormat, 1, 1);
 }
+// kind::f8f6f4, A and B E4M3 (format 0), both K-major, fp32 accumulate, M=128 N=64
+__host__ __device__ constexpr uint32_t idesc_s_e4m3() { return (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24); }
 // kind::f8f6f4, A and B E4M3 (format 0), both dim/head-major, fp32 accumulate, M=128 N=64
 __host__ __device__ constexpr uint32_t idesc_o_e4m3() {
   return (1u << 4) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
@@ -166,14 +156,15 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
   using C = Cfg<kFp8>;
   SmemLayout L{};
   L.ring = 0;
-  L.stage = L.ring + C::kSlots * kSlotBytes;
-  L.q = L.stage + C::kStages * kStageBytes;
-  L.p = L.q + C::kQBufs * kQBytes;
+  L.stage = L.ring + C::kSlots * kSlotBytes;  // E4M3: K tiles, then V pages
+  L.q = L.stage + C::kKStages * kKTileBytes + C::kVStages * kStageBytes;
+  L.p = L.q + C::kQBufs * kQBytes;  // E4M3: the Q terms overwrite the bf16 Q (same 32 KB)
   L.scales = L.p + 2 * kPBytes;
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
-  L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;  // float red[4][64], mref[64], alpha[64], inv_l[2][64], vref[2]
-  L.bars = (L.red + 8 * 64 * 4 + 8 + 7) & ~7u;    // mbarriers
+  // float red[4][64], mref[64], alpha[64], inv_l[2][64], qinv[64], vref[2]
+  L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;
+  L.bars = (L.red + 9 * 64 * 4 + 8 + 7) & ~7u;    // mbarriers
   L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
   L.total = L.misc + 16;
   return L;
@@ -282,8 +273,8 @@ struct PageIds {
 // The whole producer warp runs this loop (uniform control flow); lane 0
 // issues the copies. Per piece: Q, then the chunks of K(0), then for each
 // tile t >= 1 those of K(t) and V(t-1), then V(T-1) -- the order in which the
-// MMA warp consumes them (bf16), or in which the dequantisation warps convert
-// them (E4M3: raw pages, with each tile's scales next to its K pages).
+// MMA warp consumes them (bf16). E4M3: Q, then per tile the raw K tile and
+// its scale block (the V pages come from warp 6).
 template <bool kFp8>
 __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               const CUtensorMap* qmap, const Ctx& cx, const int* s_cost, const int* s_len,
@@ -294,7 +285,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   const uint64_t pol_stream = policy_evict_first();
   const uint64_t pol_keep = policy_evict_last();
   const SmemLayout L = smem_layout<kFp8>(p.B);
-  uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged pages (E4M3); pieces; tiles
+  uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged K tiles (E4M3); pieces; tiles
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
   constexpr int kRing = kFp8 ? C::kKStages : C::kSlots;  // E4M3: the K stage ring (V pages: warp 6)
@@ -304,7 +295,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     const uint32_t slot = cc % kRing, n = cc / kRing;
     const bool r = cx.wait(kRingEmpty + slot, (n & 1) ^ 1);
     __syncwarp();
-    dst = cx.base + (kFp8 ? L.stage + slot * kStageBytes : L.ring + slot * kSlotBytes);
+    dst = cx.base + (kFp8 ? L.stage + slot * kKTileBytes : L.ring + slot * kSlotBytes);
     bar = cx.bar(kRingFull + slot);
     return r;
   };
@@ -332,14 +323,19 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++cc;
     return true;
   };
-  // E4M3: one whole raw page (two 128 B-wide boxes) of the K or V cache
-  auto stage_page = [&](const CUtensorMap* map, int pg) -> bool {
+  // E4M3: the raw K pages of a tile, as two K-major A operands of 128 rows
+  // (box h = dims [128h, 128h + 128): page pa's rows at 16 KB * h, pb's after them)
+  auto stage_k_tile = [&](int pa, int pb) -> bool {
     uint32_t dst, bar;
     if (!wait_slot(dst, bar)) return false;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
-      tma_load_2d(dst, map, 0, pg * kPageSize, bar, pol_stream);
-      tma_load_2d(dst + 8192, map, 128, pg * kPageSize, bar, pol_stream);
+      mbar_arrive_expect_tx(bar, pb >= 0 ? 32768u : 16384u);
+      tma_load_2d(dst, kmap, 0, pa * kPageSize, bar, pol_stream);
+      tma_load_2d(dst + 16384, kmap, 128, pa * kPageSize, bar, pol_stream);
+      if (pb >= 0) {
+        tma_load_2d(dst + 8192, kmap, 0, pb * kPageSize, bar, pol_stream);
+        tma_load_2d(dst + 24576, kmap, 128, pb * kPageSize, bar, pol_stream);
+      }
     }
     ++cc;
     return true;
@@ -417,7 +413,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
         const int pa = ids.get(pga, p, lane);
         const int pb = (pages_in_tile(s, t) == 2) ? ids.get(pga + 1, p, lane) : -1;
         if constexpr (kFp8) {
-          good = stage_page(kmap, pa) && (pb < 0 || stage_page(kmap, pb)) && stage_scales(pa, pb);
+          good = stage_k_tile(pa, pb) && stage_scales(pa, pb);
         } else {
           for (int d = 0; good && d < 4; ++d) good = issue_k(d, pa, pb);
         }
@@ -478,7 +474,8 @@ __device__ void producer_v_role(const DecodeParams& p, const CUtensorMap* vmap, 
       good = cx.wait(Bb::StEmpty + slot, (n & 1) ^ 1);
       __syncwarp();
       if (good && lane == 0) {
-        const uint32_t dst = cx.base + L.stage + slot * kStageBytes, bar = cx.bar(Bb::StFull + slot);
+        const uint32_t dst = cx.base + L.stage + C::kKStages * kKTileBytes + (vc % C::kVStages) * kStageBytes;
+        const uint32_t bar = cx.bar(Bb::StFull + slot);
         mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
         tma_load_2d(dst, vmap, 0, id * kPageSize, bar, pol_stream);
         tma_load_2d(dst + 8192, vmap, 128, id * kPageSize, bar, pol_stream);
@@ -544,25 +541,7 @@ __device__ void vref_role(const DecodeParams& p, const Ctx& cx, const int* s_cos
   }
 }
 
-// ---------------------------------------------------------------- dequantisation (E4M3)
-// Raw pages arrive as two 128 B-wide boxes with the 128-byte swizzle: row r,
-// 16 B piece j of box h sits at h*8192 + r*128 + ((j ^ (r & 7)) << 4). Each
-// piece (16 codes) becomes two 16 B pieces of f16 in the operand layouts.
-__device__ __forceinline__ void codes16_to_f16(const uint4 raw, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i] >> (16 * k)) & 0xFFFFu),
-                                                        __NV_E4M3);
-      o[2 * i + k] = (uint32_t)h2.x | ((uint32_t)h2.y << 16);
-    }
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
+// ---------------------------------------------------------------- shared-memory vectors
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -571,96 +550,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
-}
-__device__ __forceinline__ uint32_t sw_piece(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
-
-// Bf16 Q (TMA, 128-byte swizzle) -> f16 in place: same element positions.
-__device__ __forceinline__ void convert_q_to_f16(uint32_t q_addr, int tid) {
-  for (int i = tid; i < kQBytes / 16; i += kDequantAll) {
-    const uint4 v = ld_shared_v4(q_addr + 16 * i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-      o[k] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    st_shared_v4(q_addr + 16 * i, make_uint4(o[0], o[1], o[2], o[3]));
-  }
-}
-
-__device__ void dequant_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len,
-                             long long lo, long long hi, uint32_t tmem) {
-  using C = Cfg<true>;
-  using Bb = Bars<true>;
-  const int all = threadIdx.x - kDequantWarp0 * 32;  // 0 .. kDequantAll - 1
-  const int g = all / kDequantThreads;               // this thread's warpgroup: 128-dim half it converts
-  const int tid = all % kDequantThreads;             // 0 .. kDequantThreads - 1
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quadrant
-  uint32_t kt = 0;                                              // K tiles written to TMEM
-  const SmemLayout L = smem_layout<true>(p.B);
-  uint32_t st = 0, seg_i = 0;            // K pages consumed, pieces
-  Seg s;
-  bool ok = seg_first(s_cost, p.B, lo, hi, s);
-  // the K stage ring (V pages never pass through these warps)
-  auto stage_addr = [&](uint32_t k) { return cx.base + L.stage + (k % C::kKStages) * kStageBytes; };
-  auto wait_stage = [&](uint32_t k) -> bool { return cx.wait(Bb::StFull + k % C::kKStages, (k / C::kKStages) & 1); };
-  auto release_stage = [&](uint32_t k) { mbar_arrive(cx.bar(Bb::StEmpty + k % C::kKStages)); };
-  while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
-    if (*cx.abort) return;
-    // Q of this piece: bf16 -> f16
-    if (!cx.wait(Bb::QFull, seg_i & 1)) return;
-    convert_q_to_f16(cx.base + L.q, all);
-    fence_proxy_async_smem();
-    mbar_arrive(cx.bar(Bb::QReady));
-    ++seg_i;
-    const int T = tiles_of(s);
-    for (int t = 0; t < T; ++t) {
-      {
-        // K(t) goes to TMEM as the A operand of S^T: this thread writes token
-        // row r of the tile (its TMEM lane; rows 64-127 come from the second
-        // page), 128 of its 256 dims (warpgroup g: dims [128g, 128g + 128))
-        // as 64 columns of f16 pairs. Rows past the tile's pages keep whatever
-        // they held: their logits are masked.
-        const int np = pages_in_tile(s, t);
-        const uint32_t ka = st, kb = st + 1;
-        if (!wait_stage(ka) || (np == 2 && !wait_stage(kb))) return;
-        if (!cx.wait(Bb::KFree, (kt & 1) ^ 1)) return;  // the S MMAs of the previous tile are done
-        tc_fence_after();
-        const int r = 32 * (warp & 3) + lane, pi = r >> 6, rr = r & 63;
-        if (pi < np) {
-          const uint32_t src = stage_addr(pi ? kb : ka);
-          {
-            const int h = g;  // dims [128h, 128h + 128): one swizzled box of the staged page
-            uint4 raw[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) raw[j] = ld_shared_v4(src + h * 8192 + sw_piece(rr, j));
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {  // 32 columns (64 dims) per store
-              float cols[32];
-              uint32_t* u = reinterpret_cast<uint32_t*>(cols);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint4 lo16, hi16;
-                codes16_to_f16(raw[4 * q + j], lo16, hi16);
-                u[8 * j + 0] = lo16.x; u[8 * j + 1] = lo16.y; u[8 * j + 2] = lo16.z; u[8 * j + 3] = lo16.w;
-                u[8 * j + 4] = hi16.x; u[8 * j + 5] = hi16.y; u[8 * j + 6] = hi16.z; u[8 * j + 7] = hi16.w;
-              }
-              tmem_st32(tmem + lane_base + kTmemK + h * 64 + q * 32, cols);
-            }
-          }
-        }
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(cx.bar(Bb::KFull));
-        ++kt;
-        release_stage(ka);
-        if (np == 2) release_stage(kb);
-        st += np;
-      }
-    }
-  }
 }
 
 // ---------------------------------------------------------------- MMA issue
@@ -690,42 +579,52 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
     if (!wait_all(Bb::SEmpty + buf, (n & 1) ^ 1)) return false;
     const uint32_t d_tmem = tmem + buf * 64;
     if constexpr (kFp8) {
-      // A = the f16 K tile the dequantisation warps wrote to TMEM (one MMA per 16 dims)
-      if (!wait_all(Bb::KFull, s_cnt & 1)) return false;
+      // 8-bit S^T: A = the raw K tile (tokens x dims, K-major), B = a Q term
+      // (heads x dims, K-major); K = 32 dims per MMA, both terms in place
+      const uint32_t kslot = cc % C::kKStages;
+      if (!wait_all(Bb::StFull + kslot, (cc / C::kKStages) & 1)) return false;
       if (lane == 0) {
         tc_fence_after();
+        const uint32_t ka = cx.base + L.stage + kslot * kKTileBytes;
+        const uint32_t qa = cx.base + L.q + qb * kQBytes;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint32_t b0 = cx.base + L.q + qb * kQBytes + (k >> 2) * 8192 + (k & 3) * 32;
-          tc_mma_tmem_a(d_tmem, tmem + kTmemK + 8 * k, smem_desc_sw128(b0, 16, 1024), idesc_s<kFp8>(), k != 0);
-        }
-        tc_commit(cx.bar(Bb::KFree));
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+            for (int tm = 0; tm < kQTerms; ++tm)
+              tc_mma_f8(d_tmem, smem_desc(ka + h * 16384 + ks * 32, 16, 1024, 2),
+                        smem_desc(qa + tm * kQTermBytes + h * 8192 + ks * 32, 16, 1024, 2), idesc_s_e4m3(),
+                        (h | ks | tm) != 0);
+        tc_commit(cx.bar(Bb::StEmpty + kslot));
         tc_commit(cx.bar(Bb::SFull + buf));
       }
+      __syncwarp();
+      ++cc;
+      ++s_cnt;
+      return true;
+    } else {
+      for (int d = 0; d < 4; ++d) {
+        const uint32_t slot = cc % C::kSlots, ph = (cc / C::kSlots) & 1;
+        if (!wait_all(Bb::Full + slot, ph)) return false;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
+          const uint32_t b0 = cx.base + L.q + qb * kQBytes + d * 8192;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma(d_tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024),
+                   idesc_s<kFp8>(), (d | kk) != 0);
+          tc_commit(cx.bar(Bb::Empty + slot));
+        }
+        __syncwarp();
+        ++cc;
+      }
+      if (lane == 0) tc_commit(cx.bar(Bb::SFull + buf));
       __syncwarp();
       ++s_cnt;
       return true;
     }
-    for (int d = 0; d < 4; ++d) {
-      const uint32_t slot = cc % C::kSlots, ph = (cc / C::kSlots) & 1;
-      if (!wait_all(Bb::Full + slot, ph)) return false;
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
-        const uint32_t b0 = cx.base + L.q + qb * kQBytes + d * 8192;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma(d_tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024),
-                 idesc_s<kFp8>(), (d | kk) != 0);
-        tc_commit(cx.bar(Bb::Empty + slot));
-      }
-      __syncwarp();
-      ++cc;
-    }
-    if (lane == 0) tc_commit(cx.bar(Bb::SFull + buf));
-    __syncwarp();
-    ++s_cnt;
-    return true;
   };
   // P.V of tile t of piece `piece` (sg)
   auto do_pv = [&](const Seg& sg, int t, uint32_t piece) -> bool {
@@ -746,7 +645,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page
         const uint32_t vslot = C::kKStages + vc % C::kVStages;
         if (!wait_all(Bb::StFull + vslot, (vc / C::kVStages) & 1)) return false;
-        const uint32_t vs = cx.base + L.stage + vslot * kStageBytes;
+        const uint32_t vs = cx.base + L.stage + C::kKStages * kKTileBytes + (vc % C::kVStages) * kStageBytes;
         if (nv < kPageSize) {
           // rows [nv, 64) of both boxes (whole 128 B rows): code 0x7F is NaN and 0 * NaN would poison P.V
           const int nbytes = (kPageSize - nv) * 128;
@@ -884,12 +783,83 @@ __device__ __forceinline__ void warp_reduce_scatter_sum(float (&v)[64], int lane
   }
 }
 
-__device__ __forceinline__ void load_logits(uint32_t taddr, bool valid, float mult, float (&x)[64]) {
+// One S^T row times the token's multiplier and (E4M3) each head's 2^-e_h.
+template <bool kFp8>
+__device__ __forceinline__ void load_logits(uint32_t taddr, bool valid, float mult, const float* qinv,
+                                            float (&x)[64]) {
   tmem_ld32(taddr, x);
   tmem_ld32(taddr + 32, x + 32);
   tc_wait_ld();
 #pragma unroll
-  for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * mult : -INFINITY;
+  for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * mult * (kFp8 ? qinv[h] : 1.0f) : -INFINITY;
+}
+
+// E4M3: the bf16 Q of a piece (four 64-dim boxes of [64 heads x 128 B],
+// 128-byte swizzle, as TMA loaded it) becomes, in place, two E4M3 terms
+// t1 + t2 of Q_h * 2^e_h, each two 128-dim boxes of [64 heads x 128 B] in the
+// same swizzle. 2^e_h is the largest power of two with max_d |Q_hd| * 2^e_h
+// <= 448 (the E4M3 maximum); t1 rounds the scaled value, t2 the remainder,
+// which is exact unless it falls below the E4M3 normal range (absolute error
+// at most 2^-10 there). qinv[h] = 2^-e_h. Thread tid: head tid % 64, dims
+// [128 (tid / 64), +128). Ends with every thread's terms written and fenced
+// for the tensor cores (the caller then arrives on the ready barrier).
+__device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float* qinv, int tid) {
+  const int h = tid & 63, half = tid >> 6;
+  uint4 v[16];  // chunk j: dims [8j, 8j + 8) of this thread's half
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = ld_shared_v4(q_addr + (2 * half + (j >> 3)) * 8192 + h * 128 + (((j & 7) ^ (h & 7)) << 4));
+  float mx = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
+  }
+  red[half * 64 + h] = mx;
+  named_barrier_softmax();  // every thread has its Q values: the buffer may be overwritten
+  const float gm = fmaxf(red[h], red[64 + h]);
+  int e = 0;
+  if (gm > 0.0f && gm <= 3.0e38f) {
+    const uint32_t bits = __float_as_uint(gm);
+    const int E = (int)((bits >> 23) & 0xFFu) - 127;
+    e = ((bits & 0x7FFFFFu) <= 0x600000u ? 8 : 7) - E;  // gm * 2^e in (224, 448]
+    e = max(-126, min(126, e));
+  }
+  const float sq = __uint_as_float((uint32_t)(e + 127) << 23);
+  if (half == 0) qinv[h] = __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // output chunk k: dims [16k, 16k + 16) = input chunks 2k, 2k + 1
+    uint32_t t1[4], t2[4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint4 in = v[2 * k + u];
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {  // two output words of four codes each
+        uint32_t c1w = 0, c2w = 0;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t wd = w[2 * i + m];
+          const float2 a = make_float2(__uint_as_float(wd << 16) * sq, __uint_as_float(wd & 0xFFFF0000u) * sq);
+          const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+          const __half2_raw d1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&d1));
+          const __nv_fp8x2_storage_t c2 =
+              __nv_cvt_float2_to_fp8x2(make_float2(a.x - b.x, a.y - b.y), __NV_SATFINITE, __NV_E4M3);
+          c1w |= (uint32_t)c1 << (16 * m);
+          c2w |= (uint32_t)c2 << (16 * m);
+        }
+        t1[2 * u + i] = c1w;
+        t2[2 * u + i] = c2w;
+      }
+    }
+    const uint32_t o = half * 8192 + h * 128 + ((k ^ (h & 7)) << 4);
+    st_shared_v4(q_addr + o, make_uint4(t1[0], t1[1], t1[2], t1[3]));
+    st_shared_v4(q_addr + kQTermBytes + o, make_uint4(t2[0], t2[1], t2[2], t2[3]));
+  }
+  fence_proxy_async_smem();
 }
 
 // O^T columns (this thread's TMEM lane, both 128-dim halves) times col_scale[h].
@@ -932,7 +902,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
   float* alpha = mref + 64;                              // [64] rescale factors, uniform
   float* inv_l = alpha + 64;                             // [2][64] 1/l of the piece in O^T buffer i
-  float* s_vref = inv_l + 128;                           // [2] E4M3: largest V scale of a piece
+  float* qinv = inv_l + 128;                             // [64] E4M3: 2^-e_h of the piece's Q terms
+  float* s_vref = qinv + 64;                             // [2] E4M3: largest V scale of a piece
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
   const uint32_t taddr_o0 = tmem + lane_base + kTmemO;
   const float c2 = p.scale * kLog2e;
@@ -988,6 +959,11 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       if (!cx.wait(Bb::VRefFull + vslot, (piece >> 1) & 1)) return;
       pscale = kPScale / s_vref[vslot];
       mbar_arrive(cx.bar(Bb::VRefEmpty + vslot));
+      // Q of the piece -> E4M3 terms (the producer loaded it once the previous
+      // piece's S MMAs were done)
+      if (!cx.wait(Bb::QFull, piece & 1)) return;
+      split_q_e4m3(cx.base + L.q, red, qinv, tid);
+      mbar_arrive(cx.bar(Bb::QReady));
     }
     if (tid < 64) mref[tid] = -INFINITY;
     named_barrier_softmax();
@@ -1015,7 +991,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       if (!cx.wait(Bb::SFull + sbuf, (s_cnt >> 1) & 1)) return;
       tc_fence_after();
       float x[64];
-      load_logits(taddr_s, valid, kmul, x);
+      load_logits<kFp8>(taddr_s, valid, kmul, qinv, x);
       bool mine = false;
 #pragma unroll
       for (int h = 0; h < 64; ++h) mine |= x[h] > mref[h] + rescale_threshold<kFp8>();
@@ -1046,7 +1022,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
           tc_fence_after();
           scale_o_columns(taddr_o, alpha);
         }
-        load_logits(taddr_s, valid, kmul, x);
+        load_logits<kFp8>(taddr_s, valid, kmul, qinv, x);
       }
       tc_fence_before();
       mbar_arrive(cx.bar(Bb::SEmpty + sbuf));  // S^T buffer free for the tile after next
@@ -1148,15 +1124,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const uint32_t bars = base + L.bars;
 
   if (threadIdx.x == 0) {
-    const uint32_t full_count = kFp8 ? kDequantThreads : 1;  // dequantisation warps or the TMA transaction
     for (int i = 0; i < C::kSlots; ++i) {
-      mbar_init(bars + 8 * (Bb::Full + i), full_count);
+      mbar_init(bars + 8 * (Bb::Full + i), 1);
       mbar_init(bars + 8 * (Bb::Empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars + 8 * (Bb::QFull + i), 1);
       mbar_init(bars + 8 * (Bb::QEmpty + i), 1);
-      mbar_init(bars + 8 * (Bb::QReady + i), kDequantAll);
+      mbar_init(bars + 8 * (Bb::QReady + i), kSoftmaxThreads);
       mbar_init(bars + 8 * (Bb::SFull + i), 1);
       mbar_init(bars + 8 * (Bb::SEmpty + i), kSoftmaxThreads);
       mbar_init(bars + 8 * (Bb::PFull + i), kSoftmaxThreads);
@@ -1167,8 +1142,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(bars + 8 * Bb::Drain, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bars + 8 * (Bb::StFull + i), 1);
-      // K pages are released by both dequantisation warpgroups, V pages by the P.V commit
-      mbar_init(bars + 8 * (Bb::StEmpty + i), i < C::kKStages ? kDequantAll : 1);
+      mbar_init(bars + 8 * (Bb::StEmpty + i), 1);  // released by the commit of the MMAs that read it
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars + 8 * (Bb::VRefFull + i), 1);
@@ -1178,8 +1152,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       mbar_init(bars + 8 * (Bb::ScFull + i), 1);
       mbar_init(bars + 8 * (Bb::ScEmpty + i), kSoftmaxThreads);
     }
-    mbar_init(bars + 8 * Bb::KFull, kDequantAll);
-    mbar_init(bars + 8 * Bb::KFree, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1206,14 +1178,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const long long lo = cta_cost_lo(c, units, p.grid), hi = cta_cost_lo(c + 1, units, p.grid);
   Ctx cx{base, bars, abort_flag, p.err, p.wait_budget_ns};
 
-  if constexpr (kFp8) {  // whole warpgroups execute these
-    if (warp < 4)
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
-    else if (warp < kDequantWarp0)
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegIssue));
-    else
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegDequant));
-  }
   if (warp < 4) {
     softmax_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
   } else if (warp == kProducerWarp) {
@@ -1224,9 +1188,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     if (warp == kVProducerWarp)
       producer_v_role(p, &vmap, cx, s_cost, s_len, lo, hi);
     else if (warp == kVRefWarp)
-      vref_role(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 8 * 64);
-    else if (warp >= kDequantWarp0)
-      dequant_role(p, cx, s_cost, s_len, lo, hi, tmem);
+      vref_role(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 9 * 64);
   }
   tc_fence_before();
   __syncthreads();
@@ -1239,17 +1201,6 @@ template <bool kFp8>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, cudaStream_t stream) {
   const size_t smem = (size_t)smem_layout<kFp8>(p.B).total + 1024;
-  if constexpr (kFp8) {
-    // setmaxnreg.inc would wait forever if the block had fewer registers than the split
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
-      cudaFuncAttributes fa;
-      const cudaError_t e = cudaFuncGetAttributes(&fa, decode_split_tc_kernel<kFp8>);
-      if (e != cudaSuccess) return e;
-      launch_regs = fa.numRegs;
-    }
-    if (launch_regs < kRegLaunch) return cudaErrorInvalidConfiguration;
-  }
   static int configured_bytes = 0;  // largest opt-in set so far (per process; one device family)
   if ((int)smem > configured_bytes) {
     const cudaError_t e =
