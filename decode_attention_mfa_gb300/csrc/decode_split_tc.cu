@@ -62,6 +62,8 @@ struct Cfg<false> {
   static constexpr bool kCrossPiece = true;  // one tile stream across sequence pieces
   static constexpr int kScaleSlots = 0;  // per-tile scale blocks
   static constexpr int kAbFormat = 1;    // bf16 operands
+  static constexpr int kSCols = 64;      // TMEM columns of one S^T buffer: 64 heads
+  static constexpr int kOBufs = 2;       // O^T buffers (pieces alternate)
 };
 // E4M3: warp 4 stages the K tiles and scales, warp 6 the V pages, warp 7
 // finds each piece's largest V scale; both products run as 8-bit MMAs on the
@@ -76,6 +78,8 @@ struct Cfg<true> {
   static constexpr int kQBufs = 1;        // bf16 Q, split in place into two E4M3 terms
   static constexpr bool kCrossPiece = false;  // per-piece order (a single Q buffer)
   static constexpr int kScaleSlots = 4;
+  static constexpr int kSCols = 128;      // S^T against both Q terms: [term][head]
+  static constexpr int kOBufs = 1;        // O^T is [half][term][head] = 256 columns
 };
 
 constexpr int kSoftmaxThreads = 128;
@@ -86,13 +90,13 @@ constexpr int kMmaWarp = 5;
 constexpr int kSlotBytes = 16384;
 constexpr int kStageBytes = 16384;        // one E4M3 V page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
 constexpr int kKTileBytes = 32768;        // one E4M3 K tile: box h (dims [128h, 128h+128)) of 128 rows at 16 KB * h
-constexpr int kQTerms = 2;                // E4M3: Q as two E4M3 terms (per-head power-of-two scale)
-constexpr int kQTermBytes = 16384;        // one term: 2 boxes of [64 heads x 128 B], 128-byte swizzle
+constexpr int kQTermBytes = 8192;         // one term of one 128-dim box: [64 heads x 128 B], 128-byte swizzle
 constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]
 constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads], 16-bit
 constexpr int kScaleBytes = 1024;         // per tile: 128 K scales, then 128 V scales
-constexpr int kTmemCols = 512;            // S^T x2 (64 cols each) + O^T x2 (128 cols each)
-constexpr int kTmemO = 128;               // first O^T column; buffer o at kTmemO + 128 * o
+constexpr int kTmemCols = 512;            // S^T x2 + O^T (bf16: 2 x 64 + 2 x 128; E4M3: 2 x 128 + 256)
+template <bool kFp8>
+__host__ __device__ constexpr int tmem_o() { return 2 * Cfg<kFp8>::kSCols; }  // first O^T column; bf16 buffer o at +128 * o
 constexpr int kMaxBars = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -101,10 +105,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <bool kFp8>
 __host__ __device__ constexpr float rescale_threshold() { return kFp8 ? 3.0f : 8.0f; }
 // E4M3: the P operand is x = P * v_scale / vref * 2^5 <= 2^3 * 1 * 2^5 = 256 < 448
-// (vref = the piece's largest V scale), split into two E4M3 terms x1 + x2.
+// (vref = the piece's largest V scale), split into two E4M3 terms x1 + x2,
+// stored side by side per token: [x1 of heads 0-63 | x2 of heads 0-63].
 constexpr float kPScale = 32.0f;
-constexpr int kPTerms = 2;
-constexpr int kPTermBytes = 128 * 64;     // one term: [128 tokens x 64 heads] E4M3
 
 template <bool kFp8>
 struct Bars {  // indices into the barrier array
@@ -138,11 +141,11 @@ template <bool kFp8>
 __host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = P^T (head-major)
   return idesc_f16(128, 64, Cfg<kFp8>::kAbFormat, 1, 1);
 }
-// kind::f8f6f4, A and B E4M3 (format 0), both K-major, fp32 accumulate, M=128 N=64
-__host__ __device__ constexpr uint32_t idesc_s_e4m3() { return (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24); }
-// kind::f8f6f4, A and B E4M3 (format 0), both dim/head-major, fp32 accumulate, M=128 N=64
+// kind::f8f6f4, A and B E4M3 (format 0), both K-major, fp32 accumulate, M=128 N=128
+__host__ __device__ constexpr uint32_t idesc_s_e4m3() { return (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24); }
+// kind::f8f6f4, A and B E4M3 (format 0), both dim/head-major, fp32 accumulate, M=128 N=128
 __host__ __device__ constexpr uint32_t idesc_o_e4m3() {
-  return (1u << 4) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+  return (1u << 4) | (1u << 15) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 struct SmemLayout {
@@ -162,7 +165,7 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
   L.scales = L.p + 2 * kPBytes;
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
-  // float red[4][64], mref[64], alpha[64], inv_l[2][64], qinv[64], vref[2]
+  // float red[4][64], mref[64], alpha[64], inv_l[2][64], (unused)[64], vref[2]
   L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;
   L.bars = (L.red + 9 * 64 * 4 + 8 + 7) & ~7u;    // mbarriers
   L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
@@ -577,10 +580,11 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   auto do_s = [&](uint32_t qb) -> bool {
     const uint32_t buf = s_cnt & 1, n = s_cnt >> 1;
     if (!wait_all(Bb::SEmpty + buf, (n & 1) ^ 1)) return false;
-    const uint32_t d_tmem = tmem + buf * 64;
+    const uint32_t d_tmem = tmem + buf * C::kSCols;
     if constexpr (kFp8) {
-      // 8-bit S^T: A = the raw K tile (tokens x dims, K-major), B = a Q term
-      // (heads x dims, K-major); K = 32 dims per MMA, both terms in place
+      // 8-bit S^T: A = the raw K tile (tokens x dims, K-major), B = both Q
+      // terms stacked (128 rows [term][head] x dims, K-major): N = 128, so S^T
+      // holds K.t1^T in columns 0-63 and K.t2^T in 64-127; K = 32 dims per MMA
       const uint32_t kslot = cc % C::kKStages;
       if (!wait_all(Bb::StFull + kslot, (cc / C::kKStages) & 1)) return false;
       if (lane == 0) {
@@ -591,11 +595,8 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-            for (int tm = 0; tm < kQTerms; ++tm)
-              tc_mma_f8(d_tmem, smem_desc(ka + h * 16384 + ks * 32, 16, 1024, 2),
-                        smem_desc(qa + tm * kQTermBytes + h * 8192 + ks * 32, 16, 1024, 2), idesc_s_e4m3(),
-                        (h | ks | tm) != 0);
+            tc_mma_f8(d_tmem, smem_desc(ka + h * 16384 + ks * 32, 16, 1024, 2),
+                      smem_desc(qa + h * 16384 + ks * 32, 16, 1024, 2), idesc_s_e4m3(), (h | ks) != 0);
         tc_commit(cx.bar(Bb::StEmpty + kslot));
         tc_commit(cx.bar(Bb::SFull + buf));
       }
@@ -630,17 +631,18 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   auto do_pv = [&](const Seg& sg, int t, uint32_t piece) -> bool {
     const uint32_t buf = p_cnt & 1, n = p_cnt >> 1;
     const bool first_of_seg = t == 0;
-    // pieces alternate between the two O^T buffers; the first P.V of piece j
-    // overwrites the buffer of piece j - 2, whose epilogue must be done
-    const uint32_t obuf = piece & 1;
-    if (first_of_seg && !wait_all(Bb::OFree + obuf, ((piece >> 1) & 1) ^ 1)) return false;
+    // pieces cycle through the O^T buffers; the first P.V of piece j
+    // overwrites the buffer of piece j - kOBufs, whose epilogue must be done
+    const uint32_t obuf = piece % C::kOBufs;
+    if (first_of_seg && !wait_all(Bb::OFree + obuf, ((piece / C::kOBufs) & 1) ^ 1)) return false;
     if (!wait_all(Bb::PFull + buf, n & 1)) return false;
     const int pga = sg.pg0 + 2 * t;
     const int np = pages_in_tile(sg, t);
     if constexpr (kFp8) {
       // 8-bit P.V: A = the raw staged V page (dims x tokens, 128-byte swizzle,
-      // one 128-dim box per half), B = the P terms (tokens x heads, 64-byte
-      // swizzle); K = 32 tokens per MMA, two terms accumulated in place
+      // one 128-dim box per half), B = both P terms side by side (tokens x
+      // 128 [term][head], 128-byte swizzle): N = 128, so O^T half hf holds
+      // V^T.x1 in columns 0-63 and V^T.x2 in 64-127; K = 32 tokens per MMA
       for (int i = 0; i < np; ++i) {
         const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page
         const uint32_t vslot = C::kKStages + vc % C::kVStages;
@@ -658,16 +660,13 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         }
         if (lane == 0) {
           tc_fence_after();
-          const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 4096;  // token rows 64i.. of each term
+          const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;  // token rows 64i..
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks)
-#pragma unroll
-              for (int tm = 0; tm < kPTerms; ++tm)
-                tc_mma_f8(tmem + kTmemO + obuf * 128 + hf * 64, smem_desc(vs + hf * 8192 + ks * 4096, 16, 1024, 2),
-                          smem_desc(bp + tm * kPTermBytes + ks * 2048, 16, 512, 4), idesc_o_e4m3(),
-                          !(first_of_seg && i == 0 && ks == 0 && tm == 0));
+              tc_mma_f8(tmem + tmem_o<kFp8>() + hf * 128, smem_desc(vs + hf * 8192 + ks * 4096, 16, 1024, 2),
+                        smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3(), !(first_of_seg && i == 0 && ks == 0));
           tc_commit(cx.bar(Bb::StEmpty + vslot));  // the V page's stage is free once these MMAs are done
         }
         __syncwarp();
@@ -696,7 +695,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
           const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma(tmem + kTmemO + obuf * 128 + hf * 64, smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
+            tc_mma(tmem + tmem_o<kFp8>() + obuf * 128 + hf * 64, smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
                    smem_desc_sw128(bp + kk * 2048, 8192, 1024), idesc_o<kFp8>(),
                    !(first_of_seg && i == 0 && kk == 0));
           tc_commit(cx.bar(Bb::Empty + slot));
@@ -783,27 +782,59 @@ __device__ __forceinline__ void warp_reduce_scatter_sum(float (&v)[64], int lane
   }
 }
 
-// One S^T row times the token's multiplier and (E4M3) each head's 2^-e_h.
+// One S^T row times the token's multiplier (E4M3: the sum of the two Q
+// terms' columns); rows past the sequence read -inf (only a partial tile has
+// such rows).
 template <bool kFp8>
-__device__ __forceinline__ void load_logits(uint32_t taddr, bool valid, float mult, const float* qinv,
-                                            float (&x)[64]) {
-  tmem_ld32(taddr, x);
-  tmem_ld32(taddr + 32, x + 32);
-  tc_wait_ld();
+__device__ __forceinline__ void load_logits(uint32_t taddr, bool full, bool valid, float mult, float (&x)[64]) {
+  if constexpr (kFp8) {
 #pragma unroll
-  for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * mult * (kFp8 ? qinv[h] : 1.0f) : -INFINITY;
+    for (int q = 0; q < 2; ++q) {
+      float y[32];
+      tmem_ld32(taddr + q * 32, x + q * 32);
+      tmem_ld32(taddr + 64 + q * 32, y);
+      tc_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 32; ++h) x[q * 32 + h] += y[h];
+    }
+  } else {
+    tmem_ld32(taddr, x);
+    tmem_ld32(taddr + 32, x + 32);
+    tc_wait_ld();
+  }
+#pragma unroll
+  for (int h = 0; h < 64; ++h) x[h] *= mult;
+  if (!full) {
+#pragma unroll
+    for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] : -INFINITY;
+  }
+}
+// x[h] -= m[h] (m 16-byte aligned, uniform); returns the largest difference.
+__device__ __forceinline__ float sub_ref(float (&x)[64], const float* m) {
+  float dm = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 r = reinterpret_cast<const float4*>(m)[i];
+    x[4 * i] -= r.x;
+    x[4 * i + 1] -= r.y;
+    x[4 * i + 2] -= r.z;
+    x[4 * i + 3] -= r.w;
+    dm = fmaxf(dm, fmaxf(fmaxf(x[4 * i], x[4 * i + 1]), fmaxf(x[4 * i + 2], x[4 * i + 3])));
+  }
+  return dm;
 }
 
 // E4M3: the bf16 Q of a piece (four 64-dim boxes of [64 heads x 128 B],
 // 128-byte swizzle, as TMA loaded it) becomes, in place, two E4M3 terms
-// t1 + t2 of Q_h * 2^e_h, each two 128-dim boxes of [64 heads x 128 B] in the
-// same swizzle. 2^e_h is the largest power of two with max_d |Q_hd| * 2^e_h
-// <= 448 (the E4M3 maximum); t1 rounds the scaled value, t2 the remainder,
-// which is exact unless it falls below the E4M3 normal range (absolute error
-// at most 2^-10 there). qinv[h] = 2^-e_h. Thread tid: head tid % 64, dims
+// t1 + t2 of Q * 2^e: 128-dim box b (16 KB at 16 KB * b) holds t1 of the 64
+// heads, then t2 ([128 rows x 128 B], 128-byte swizzle). 2^e is the largest
+// power of two with max |Q| * 2^e <= 448 (the E4M3 maximum); t1 rounds the
+// scaled value, t2 the remainder, which is exact unless it falls below the
+// E4M3 normal range (absolute error at most 2^-10 there, i.e. 2^-18 of the
+// largest |Q|). Returns 2^-e. Thread tid: head tid % 64, dims
 // [128 (tid / 64), +128). Ends with every thread's terms written and fenced
 // for the tensor cores (the caller then arrives on the ready barrier).
-__device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float* qinv, int tid) {
+__device__ __forceinline__ float split_q_e4m3(uint32_t q_addr, float* red, int tid) {
   const int h = tid & 63, half = tid >> 6;
   uint4 v[16];  // chunk j: dims [8j, 8j + 8) of this thread's half
 #pragma unroll
@@ -817,9 +848,11 @@ __device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float*
     for (int k = 0; k < 4; ++k)
       mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
   }
-  red[half * 64 + h] = mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
   named_barrier_softmax();  // every thread has its Q values: the buffer may be overwritten
-  const float gm = fmaxf(red[h], red[64 + h]);
+  const float gm = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   int e = 0;
   if (gm > 0.0f && gm <= 3.0e38f) {
     const uint32_t bits = __float_as_uint(gm);
@@ -828,7 +861,6 @@ __device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float*
     e = max(-126, min(126, e));
   }
   const float sq = __uint_as_float((uint32_t)(e + 127) << 23);
-  if (half == 0) qinv[h] = __uint_as_float((uint32_t)(127 - e) << 23);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {  // output chunk k: dims [16k, 16k + 16) = input chunks 2k, 2k + 1
     uint32_t t1[4], t2[4];
@@ -855,25 +887,29 @@ __device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float*
         t2[2 * u + i] = c2w;
       }
     }
-    const uint32_t o = half * 8192 + h * 128 + ((k ^ (h & 7)) << 4);
+    const uint32_t o = half * 16384 + h * 128 + ((k ^ (h & 7)) << 4);
     st_shared_v4(q_addr + o, make_uint4(t1[0], t1[1], t1[2], t1[3]));
     st_shared_v4(q_addr + kQTermBytes + o, make_uint4(t2[0], t2[1], t2[2], t2[3]));
   }
   fence_proxy_async_smem();
+  return __uint_as_float((uint32_t)(127 - e) << 23);
 }
 
-// O^T columns (this thread's TMEM lane, both 128-dim halves) times col_scale[h].
+// O^T columns (this thread's TMEM lane, both 128-dim halves) times
+// col_scale[head]; E4M3: both terms' columns of each head.
+template <bool kFp8>
 __device__ __forceinline__ void scale_o_columns(uint32_t taddr_o, const float* col_scale) {
+  constexpr int kHalfCols = kFp8 ? 128 : 64;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kHalfCols / 32; ++q) {
       float o[32];
-      tmem_ld32(taddr_o + hf * 64 + q * 32, o);
+      tmem_ld32(taddr_o + hf * kHalfCols + q * 32, o);
       tc_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 32; ++h) o[h] *= col_scale[q * 32 + h];
-      tmem_st32(taddr_o + hf * 64 + q * 32, o);
+      for (int h = 0; h < 32; ++h) o[h] *= col_scale[(q & 1) * 32 + h];
+      tmem_st32(taddr_o + hf * kHalfCols + q * 32, o);
     }
   }
   tc_wait_st();
@@ -902,10 +938,9 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
   float* alpha = mref + 64;                              // [64] rescale factors, uniform
   float* inv_l = alpha + 64;                             // [2][64] 1/l of the piece in O^T buffer i
-  float* qinv = inv_l + 128;                             // [64] E4M3: 2^-e_h of the piece's Q terms
-  float* s_vref = qinv + 64;                             // [2] E4M3: largest V scale of a piece
+  float* s_vref = inv_l + 192;                           // [2] E4M3: largest V scale of a piece
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-  const uint32_t taddr_o0 = tmem + lane_base + kTmemO;
+  const uint32_t taddr_o0 = tmem + lane_base + tmem_o<kFp8>();
   const float c2 = p.scale * kLog2e;
   uint32_t s_cnt = 0, p_cnt = 0;
   // P.V(g) completes phase g/2 of p_empty[g % 2]. Before P(g) is written the
@@ -914,10 +949,11 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   // past it: the parity wait is exact. Completion of P.V(g) implies that of
   // every earlier MMA (one issuing thread, commits track all prior MMAs).
   auto wait_pv = [&](uint32_t g) -> bool { return cx.wait(Bb::PEmpty + (g & 1), (g >> 1) & 1); };
-  // Pieces alternate between two O^T buffers. A piece's O^T / l is written
-  // out once the next piece's first P has been handed over (its last P.V was
+  // Pieces cycle through the O^T buffers. A piece's O^T / l is written out
+  // once the next piece's first P has been handed over (its last P.V was
   // issued before that piece's first S), so the softmax warps go on to the
-  // next piece without waiting for the previous one's last P.V.
+  // next piece without waiting for the previous one's last P.V (with one
+  // buffer, E4M3, the next piece's first P.V waits for this).
   bool pend = false;
   uint32_t pend_pv = 0, pend_obuf = 0;
   size_t pend_slot = 0;
@@ -927,13 +963,22 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const uint32_t ta = taddr_o0 + pend_obuf * 128;
     const float* il = inv_l + pend_obuf * 64;
     float* dst = p.part_o + pend_slot * kHeads * kHeadDim;
+    constexpr int kHalfCols = kFp8 ? 128 : 64;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         float o[32];
-        tmem_ld32(ta + hf * 64 + q * 32, o);
-        tc_wait_ld();
+        tmem_ld32(ta + hf * kHalfCols + q * 32, o);
+        if constexpr (kFp8) {  // + the second P term's columns
+          float o2[32];
+          tmem_ld32(ta + hf * kHalfCols + 64 + q * 32, o2);
+          tc_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) o[h] += o2[h];
+        } else {
+          tc_wait_ld();
+        }
         const int dim = hf * 128 + tid;
 #pragma unroll
         for (int h = 0; h < 32; ++h) dst[(q * 32 + h) * kHeadDim + dim] = o[h] * il[q * 32 + h];
@@ -949,11 +994,11 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   uint32_t piece = 0;
 
   while (ok && seg_next(s_cost, s_len, p.B, p.piece_cost, lo, hi, s)) {
-    const uint32_t obuf = piece & 1;
+    const uint32_t obuf = piece % C::kOBufs;
     const uint32_t taddr_o = taddr_o0 + obuf * 128;
     // E4M3: P enters the 8-bit P.V as P * v_scale * pscale (<= 256); O^T is
     // then pscale times too large, which the epilogue undoes
-    float pscale = 1.0f;
+    float pscale = 1.0f, qinv = 1.0f;
     if constexpr (kFp8) {
       const uint32_t vslot = piece & 1;
       if (!cx.wait(Bb::VRefFull + vslot, (piece >> 1) & 1)) return;
@@ -962,7 +1007,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       // Q of the piece -> E4M3 terms (the producer loaded it once the previous
       // piece's S MMAs were done)
       if (!cx.wait(Bb::QFull, piece & 1)) return;
-      split_q_e4m3(cx.base + L.q, red, qinv, tid);
+      qinv = split_q_e4m3(cx.base + L.q, red, tid);
       mbar_arrive(cx.bar(Bb::QReady));
     }
     if (tid < 64) mref[tid] = -INFINITY;
@@ -973,7 +1018,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const int T = tiles_of(s);
     for (int t = 0; t < T; ++t) {
       const int tok0 = (s.pg0 + 2 * t) * kPageSize;
-      const bool valid = tid < min(pages_in_tile(s, t) * kPageSize, s.len - tok0);
+      const int rows = min(pages_in_tile(s, t) * kPageSize, s.len - tok0);  // valid rows of the tile
+      const bool full = rows == 128, valid = tid < rows;
       // E4M3: this token's K and V scales (the tile's scale block, slot = tile count)
       float kmul = c2, vmul = 1.0f;
       if constexpr (kFp8) {
@@ -981,22 +1027,21 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         if (!cx.wait(Bb::ScFull + slot, (p_cnt / C::kScaleSlots) & 1)) return;
         const float* sc = reinterpret_cast<const float*>(gbase + L.scales + slot * kScaleBytes);
         if (valid) {
-          kmul = c2 * sc[tid];
+          kmul = c2 * qinv * sc[tid];
           vmul = sc[128 + tid] * pscale;
         }
         mbar_arrive(cx.bar(Bb::ScEmpty + slot));
       }
       const uint32_t sbuf = s_cnt & 1;
-      const uint32_t taddr_s = tmem + lane_base + sbuf * 64;
+      const uint32_t taddr_s = tmem + lane_base + sbuf * C::kSCols;
       if (!cx.wait(Bb::SFull + sbuf, (s_cnt >> 1) & 1)) return;
       tc_fence_after();
       float x[64];
-      load_logits<kFp8>(taddr_s, valid, kmul, qinv, x);
-      bool mine = false;
-#pragma unroll
-      for (int h = 0; h < 64; ++h) mine |= x[h] > mref[h] + rescale_threshold<kFp8>();
-      // ---- does any logit of the tile exceed its reference maximum by 2^8?
+      load_logits<kFp8>(taddr_s, full, valid, kmul, x);
+      const bool mine = sub_ref(x, mref) > rescale_threshold<kFp8>();  // x = logit - reference from here
+      // ---- does any logit of the tile exceed its reference maximum by 2^threshold?
       if (named_barrier_softmax_or(mine)) {
+        load_logits<kFp8>(taddr_s, full, valid, kmul, x);
         warp_reduce_scatter_max(x, lane);  // x is reloaded below
         red[warp * 64 + 2 * lane] = x[0];
         red[warp * 64 + 2 * lane + 1] = x[1];
@@ -1020,9 +1065,10 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
           // O^T holds the previous tiles: wait for their last P.V, then scale its columns
           if (!wait_pv(p_cnt - 1)) return;
           tc_fence_after();
-          scale_o_columns(taddr_o, alpha);
+          scale_o_columns<kFp8>(taddr_o, alpha);
         }
-        load_logits<kFp8>(taddr_s, valid, kmul, qinv, x);
+        load_logits<kFp8>(taddr_s, full, valid, kmul, x);
+        (void)sub_ref(x, mref);
       }
       tc_fence_before();
       mbar_arrive(cx.bar(Bb::SEmpty + sbuf));  // S^T buffer free for the tile after next
@@ -1031,8 +1077,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       uint32_t packed[32];  // bf16: this token's 64 P values; E4M3: 16 words per term
 #pragma unroll
       for (int h = 0; h < 64; h += 2) {
-        const float p0 = ex2_approx(x[h] - mref[h]);
-        const float p1 = ex2_approx(x[h + 1] - mref[h + 1]);
+        const float p0 = ex2_approx(x[h]);
+        const float p1 = ex2_approx(x[h + 1]);
         lp[h] += p0;
         lp[h + 1] += p1;
         if constexpr (kFp8) {
@@ -1060,15 +1106,13 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       const uint32_t pbuf = p_cnt & 1;
       if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
       if constexpr (kFp8) {
-        // term tm, token row tid: 64 B, 16 B chunk j at ((j ^ ((row >> 1) & 3)) << 4) (64-byte swizzle)
-        const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 64;
+        // token row tid: 128 B = [x1 of heads 0-63 | x2 of heads 0-63], 16 B
+        // chunk j at ((j ^ (row & 7)) << 4) (128-byte swizzle)
+        const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
 #pragma unroll
-        for (int tm = 0; tm < kPTerms; ++tm)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            st_shared_v4(prow + tm * kPTermBytes + ((j ^ ((tid >> 1) & 3)) << 4),
-                         make_uint4(packed[16 * tm + 4 * j], packed[16 * tm + 4 * j + 1], packed[16 * tm + 4 * j + 2],
-                                    packed[16 * tm + 4 * j + 3]));
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(prow + ((j ^ (tid & 7)) << 4),
+                       make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]));
       } else {
         const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
 #pragma unroll
