@@ -165,7 +165,7 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
   L.scales = L.p + 2 * kPBytes;
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
-  // float red[4][64], mref[64], alpha[64], inv_l[2][64], (unused)[64], vref[2]
+  // float red[4][64], mref[64], alpha[64], inv_l[2][64], qinv[64], vref[2]
   L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;
   L.bars = (L.red + 9 * 64 * 4 + 8 + 7) & ~7u;    // mbarriers
   L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
@@ -782,11 +782,15 @@ __device__ __forceinline__ void warp_reduce_scatter_sum(float (&v)[64], int lane
   }
 }
 
-// One S^T row times the token's multiplier (E4M3: the sum of the two Q
-// terms' columns); rows past the sequence read -inf (only a partial tile has
-// such rows).
+// One S^T row as log2-domain logits minus the reference maxima:
+//   x[h] = S[h] * colmul[h] * mult - m[h]
+// (E4M3: S is the sum of the two Q terms' columns and colmul the heads'
+// 2^-e_h; bf16: colmul = 1); m = nullptr gives the plain logits. Rows past
+// the sequence read -inf (only a partial tile has such rows). Returns the
+// largest x. colmul and m are 16-byte aligned and uniform.
 template <bool kFp8>
-__device__ __forceinline__ void load_logits(uint32_t taddr, bool full, bool valid, float mult, float (&x)[64]) {
+__device__ __forceinline__ float load_logits(uint32_t taddr, bool full, bool valid, float mult, const float* colmul,
+                                             const float* m, float (&x)[64]) {
   if constexpr (kFp8) {
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -803,38 +807,36 @@ __device__ __forceinline__ void load_logits(uint32_t taddr, bool full, bool vali
     tc_wait_ld();
   }
 #pragma unroll
-  for (int h = 0; h < 64; ++h) x[h] *= mult;
+  for (int i = 0; i < 16; ++i) {
+    const float4 r = m ? reinterpret_cast<const float4*>(m)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    x[4 * i] = fmaf(x[4 * i], mult, -r.x);
+    x[4 * i + 1] = fmaf(x[4 * i + 1], mult, -r.y);
+    x[4 * i + 2] = fmaf(x[4 * i + 2], mult, -r.z);
+    x[4 * i + 3] = fmaf(x[4 * i + 3], mult, -r.w);
+  }
   if (!full) {
 #pragma unroll
     for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] : -INFINITY;
   }
-}
-// x[h] -= m[h] (m 16-byte aligned, uniform); returns the largest difference.
-__device__ __forceinline__ float sub_ref(float (&x)[64], const float* m) {
   float dm = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 r = reinterpret_cast<const float4*>(m)[i];
-    x[4 * i] -= r.x;
-    x[4 * i + 1] -= r.y;
-    x[4 * i + 2] -= r.z;
-    x[4 * i + 3] -= r.w;
+  for (int i = 0; i < 16; ++i)
     dm = fmaxf(dm, fmaxf(fmaxf(x[4 * i], x[4 * i + 1]), fmaxf(x[4 * i + 2], x[4 * i + 3])));
-  }
   return dm;
 }
 
 // E4M3: the bf16 Q of a piece (four 64-dim boxes of [64 heads x 128 B],
 // 128-byte swizzle, as TMA loaded it) becomes, in place, two E4M3 terms
-// t1 + t2 of Q * 2^e: 128-dim box b (16 KB at 16 KB * b) holds t1 of the 64
-// heads, then t2 ([128 rows x 128 B], 128-byte swizzle). 2^e is the largest
-// power of two with max |Q| * 2^e <= 448 (the E4M3 maximum); t1 rounds the
-// scaled value, t2 the remainder, which is exact unless it falls below the
-// E4M3 normal range (absolute error at most 2^-10 there, i.e. 2^-18 of the
-// largest |Q|). Returns 2^-e. Thread tid: head tid % 64, dims
-// [128 (tid / 64), +128). Ends with every thread's terms written and fenced
-// for the tensor cores (the caller then arrives on the ready barrier).
-__device__ __forceinline__ float split_q_e4m3(uint32_t q_addr, float* red, int tid) {
+// t1 + t2 of Q_h * 2^e_h: 128-dim box b (16 KB at 16 KB * b) holds t1 of the
+// 64 heads, then t2 ([128 rows x 128 B], 128-byte swizzle). 2^e_h is the
+// largest power of two with max_d |Q_hd| * 2^e_h <= 448 (the E4M3 maximum);
+// t1 rounds the scaled value, t2 the remainder, which is exact unless it
+// falls below the E4M3 normal range (absolute error at most 2^-10 there,
+// i.e. 2^-18 of the head's largest |Q|). qinv[h] = 2^-e_h. Thread tid: head
+// tid % 64, dims [128 (tid / 64), +128). Ends with every thread's terms
+// written and fenced for the tensor cores (the caller then arrives on the
+// ready barrier).
+__device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float* qinv, int tid) {
   const int h = tid & 63, half = tid >> 6;
   uint4 v[16];  // chunk j: dims [8j, 8j + 8) of this thread's half
 #pragma unroll
@@ -861,6 +863,7 @@ __device__ __forceinline__ float split_q_e4m3(uint32_t q_addr, float* red, int t
     e = max(-126, min(126, e));
   }
   const float sq = __uint_as_float((uint32_t)(e + 127) << 23);
+  if (tid == 0) qinv[0] = __uint_as_float((uint32_t)(127 - e) << 23);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {  // output chunk k: dims [16k, 16k + 16) = input chunks 2k, 2k + 1
     uint32_t t1[4], t2[4];
@@ -892,7 +895,6 @@ __device__ __forceinline__ float split_q_e4m3(uint32_t q_addr, float* red, int t
     st_shared_v4(q_addr + kQTermBytes + o, make_uint4(t2[0], t2[1], t2[2], t2[3]));
   }
   fence_proxy_async_smem();
-  return __uint_as_float((uint32_t)(127 - e) << 23);
 }
 
 // O^T columns (this thread's TMEM lane, both 128-dim halves) times
@@ -938,7 +940,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
   float* alpha = mref + 64;                              // [64] rescale factors, uniform
   float* inv_l = alpha + 64;                             // [2][64] 1/l of the piece in O^T buffer i
-  float* s_vref = inv_l + 192;                           // [2] E4M3: largest V scale of a piece
+  float* qinv = inv_l + 128;                             // [64] E4M3: 2^-e_h of the piece's Q terms
+  float* s_vref = qinv + 64;                             // [2] E4M3: largest V scale of a piece
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
   const uint32_t taddr_o0 = tmem + lane_base + tmem_o<kFp8>();
   const float c2 = p.scale * kLog2e;
@@ -998,7 +1001,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const uint32_t taddr_o = taddr_o0 + obuf * 128;
     // E4M3: P enters the 8-bit P.V as P * v_scale * pscale (<= 256); O^T is
     // then pscale times too large, which the epilogue undoes
-    float pscale = 1.0f, qinv = 1.0f;
+    float pscale = 1.0f;
     if constexpr (kFp8) {
       const uint32_t vslot = piece & 1;
       if (!cx.wait(Bb::VRefFull + vslot, (piece >> 1) & 1)) return;
@@ -1007,7 +1010,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       // Q of the piece -> E4M3 terms (the producer loaded it once the previous
       // piece's S MMAs were done)
       if (!cx.wait(Bb::QFull, piece & 1)) return;
-      qinv = split_q_e4m3(cx.base + L.q, red, tid);
+      split_q_e4m3(cx.base + L.q, red, qinv, tid);
       mbar_arrive(cx.bar(Bb::QReady));
     }
     if (tid < 64) mref[tid] = -INFINITY;
@@ -1027,7 +1030,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         if (!cx.wait(Bb::ScFull + slot, (p_cnt / C::kScaleSlots) & 1)) return;
         const float* sc = reinterpret_cast<const float*>(gbase + L.scales + slot * kScaleBytes);
         if (valid) {
-          kmul = c2 * qinv * sc[tid];
+          kmul = c2 * qinv[0] * sc[tid];
           vmul = sc[128 + tid] * pscale;
         }
         mbar_arrive(cx.bar(Bb::ScEmpty + slot));
@@ -1037,11 +1040,11 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       if (!cx.wait(Bb::SFull + sbuf, (s_cnt >> 1) & 1)) return;
       tc_fence_after();
       float x[64];
-      load_logits<kFp8>(taddr_s, full, valid, kmul, x);
-      const bool mine = sub_ref(x, mref) > rescale_threshold<kFp8>();  // x = logit - reference from here
+      // x = logit - reference maximum (log2 units)
+      const bool mine = load_logits<kFp8>(taddr_s, full, valid, kmul, qinv, mref, x) > rescale_threshold<kFp8>();
       // ---- does any logit of the tile exceed its reference maximum by 2^threshold?
       if (named_barrier_softmax_or(mine)) {
-        load_logits<kFp8>(taddr_s, full, valid, kmul, x);
+        (void)load_logits<kFp8>(taddr_s, full, valid, kmul, qinv, nullptr, x);
         warp_reduce_scatter_max(x, lane);  // x is reloaded below
         red[warp * 64 + 2 * lane] = x[0];
         red[warp * 64 + 2 * lane + 1] = x[1];
@@ -1067,58 +1070,53 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
           tc_fence_after();
           scale_o_columns<kFp8>(taddr_o, alpha);
         }
-        load_logits<kFp8>(taddr_s, full, valid, kmul, x);
-        (void)sub_ref(x, mref);
+        (void)load_logits<kFp8>(taddr_s, full, valid, kmul, qinv, mref, x);
       }
       tc_fence_before();
       mbar_arrive(cx.bar(Bb::SEmpty + sbuf));  // S^T buffer free for the tile after next
       ++s_cnt;
-      // ---- P = exp2(x - mref): row sums in fp32; P^T row (times the V scale) in 16 bits
-      uint32_t packed[32];  // bf16: this token's 64 P values; E4M3: 16 words per term
-#pragma unroll
-      for (int h = 0; h < 64; h += 2) {
-        const float p0 = ex2_approx(x[h]);
-        const float p1 = ex2_approx(x[h + 1]);
-        lp[h] += p0;
-        lp[h + 1] += p1;
-        if constexpr (kFp8) {
-          // x = P * v_scale * 2^5 / vref in [0, 256], as x1 + x2 (E4M3): x2 rounds x - x1,
-          // formed in f16 (x1 is exact in f16, and so is the difference)
-          const __half2 xh = __floats2half2_rn(p0 * vmul, p1 * vmul);
-          const __nv_fp8x2_storage_t c1 =
-              __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&xh), __NV_SATFINITE, __NV_E4M3);
-          const __half2_raw d1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
-          const __half2 rh = __hsub2(xh, *reinterpret_cast<const __half2*>(&d1));
-          const __nv_fp8x2_storage_t c2 =
-              __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rh), __NV_SATFINITE, __NV_E4M3);
-          const int w = h >> 2, sh = (h & 2) ? 16 : 0;  // two heads per 16 bits, four per word
-          if (sh == 0) {
-            packed[w] = (uint32_t)c1;
-            packed[16 + w] = (uint32_t)c2;
-          } else {
-            packed[w] |= (uint32_t)c1 << 16;
-            packed[16 + w] |= (uint32_t)c2 << 16;
-          }
-        } else {
-          packed[h >> 1] = pack2<kFp8>(p0, p1);
-        }
-      }
+      // ---- P = exp2(x - mref): row sums in fp32; this token's P^T row (times
+      // the V scale) into the P buffer, 16 B chunk j at ((j ^ (row & 7)) << 4)
+      // (128-byte swizzle) as soon as it is formed. bf16: chunk j = heads
+      // [8j, 8j + 8); E4M3: the row is [x1 of heads 0-63 | x2 of heads 0-63],
+      // chunk j = x1 and chunk 4 + j = x2 of heads [16j, 16j + 16).
       const uint32_t pbuf = p_cnt & 1;
       if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
-      if constexpr (kFp8) {
-        // token row tid: 128 B = [x1 of heads 0-63 | x2 of heads 0-63], 16 B
-        // chunk j at ((j ^ (row & 7)) << 4) (128-byte swizzle)
-        const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
+      const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
+      constexpr int kHeadsPerChunk = kFp8 ? 16 : 8;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_shared_v4(prow + ((j ^ (tid & 7)) << 4),
-                       make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]));
-      } else {
-        const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
+      for (int j = 0; j < 64 / kHeadsPerChunk; ++j) {
+        uint32_t w1[4], w2[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_shared_v4(prow + ((j ^ (tid & 7)) << 4),
-                       make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]));
+        for (int k = 0; k < kHeadsPerChunk / 2; ++k) {
+          const int h = j * kHeadsPerChunk + 2 * k;
+          const float p0 = ex2_approx(x[h]);
+          const float p1 = ex2_approx(x[h + 1]);
+          lp[h] += p0;
+          lp[h + 1] += p1;
+          if constexpr (kFp8) {
+            // x = P * v_scale * 2^5 / vref in [0, 256], as x1 + x2 (E4M3): x2 rounds x - x1,
+            // formed in f16 (x1 is exact in f16, and so is the difference)
+            const __half2 xh = __floats2half2_rn(p0 * vmul, p1 * vmul);
+            const __nv_fp8x2_storage_t c1 =
+                __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&xh), __NV_SATFINITE, __NV_E4M3);
+            const __half2_raw d1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+            const __half2 rh = __hsub2(xh, *reinterpret_cast<const __half2*>(&d1));
+            const __nv_fp8x2_storage_t c2 =
+                __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rh), __NV_SATFINITE, __NV_E4M3);
+            if ((k & 1) == 0) {  // two heads per 16 bits, four per word
+              w1[k >> 1] = (uint32_t)c1;
+              w2[k >> 1] = (uint32_t)c2;
+            } else {
+              w1[k >> 1] |= (uint32_t)c1 << 16;
+              w2[k >> 1] |= (uint32_t)c2 << 16;
+            }
+          } else {
+            w1[k] = pack2<kFp8>(p0, p1);
+          }
+        }
+        st_shared_v4(prow + ((j ^ (tid & 7)) << 4), make_uint4(w1[0], w1[1], w1[2], w1[3]));
+        if constexpr (kFp8) st_shared_v4(prow + (((4 + j) ^ (tid & 7)) << 4), make_uint4(w2[0], w2[1], w2[2], w2[3]));
       }
       fence_proxy_async_smem();
       tc_fence_before();

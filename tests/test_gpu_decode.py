@@ -115,6 +115,22 @@ def test_split_count_invariance(oracle_mod, kv):
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_query_heads_of_very_different_norms(oracle_mod, kv):
+    """Head h of Q scaled by 2^-(h % 13) (a 4096x spread), four heads by 8
+    (peaked softmax): the E4M3 path splits Q into E4M3 terms under one
+    power-of-two scale per piece, so small heads sit far below the largest."""
+    case = _case([700, 129, 2000], seed=31, kv=kv)
+    mult = torch.tensor([2.0 ** -(h % 13) for h in range(wl.HEADS)], dtype=torch.float32)
+    mult[[3, 17, 40, 63]] = 8.0
+    case.q.copy_((case.q.float() * mult[None, :, None]).to(torch.bfloat16))
+    dev = DeviceCache(case, kv)
+    dev.attend()
+    dev.check_errors()
+    out_ref, lse_ref = _oracle(oracle_mod, case, kv)
+    compare(dev.out, dev.lse, out_ref, lse_ref, f"{kv}/head-norm spread")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_maximum_batch(oracle_mod, kv):
     """The largest batch the ABI accepts (MFA_MAX_BATCH sequences): the largest
     shared-memory layout of the split kernel and the widest combine grid.
