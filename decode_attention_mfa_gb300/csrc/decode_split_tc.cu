@@ -19,15 +19,16 @@
 // plus its natural-log LSE per sequence piece into slot c + b; the LSE
 // combine kernel merges the pieces.
 //
-// Warp roles (one CTA per SM):
-//   warps 0-3  softmax: TMEM lane = token of the tile; online softmax in fp32
-//              with a lazily updated reference maximum (only when a logit
-//              exceeds it by 2^8 are the row sums and O^T rescaled); then the
-//              epilogue (row-sum reduction, O^T / l, partial LSE).
-//   warp 4     producer: page-table walk and TMA loads.
-//   warp 5     MMA issue (lane 0) and TMEM allocation.
-//   warp 6     (E4M3 cache only) V page producer.
-//   warp 7     (E4M3 cache only) largest V scale of each piece.
+// Warp roles (one CTA per SM; G = 1 softmax warpgroup for bf16, 2 for E4M3):
+//   warps 0..4G-1  softmax: warpgroup g owns heads [64g/G, 64(g+1)/G); TMEM
+//                  lane = token of the tile; online softmax in fp32 with a
+//                  lazily updated reference maximum (only when a logit exceeds
+//                  it by 2^threshold are the row sums and O^T rescaled); then
+//                  the epilogue (row-sum reduction, O^T / l, partial LSE).
+//   warp 4G        producer: page-table walk and TMA loads.
+//   warp 4G+1      MMA issue (lane 0) and TMEM allocation.
+//   warp 4G+2      (E4M3 cache only) V page producer.
+//   warp 4G+3      (E4M3 cache only) largest V scale of each piece.
 // bf16 cache: the producer loads 16 KB operand chunks (a 64-dim slice of a
 // 2-page K tile, or a 128-dim slice of one V page) straight into a ring of
 // shared-memory slots in the layouts the MMAs read; the MMA warp zeroes the
@@ -53,7 +54,7 @@ template <bool kFp8>
 struct Cfg;
 template <>
 struct Cfg<false> {
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 192;   // softmax warpgroup, producer, MMA
   static constexpr int kSlots = 7;       // 16 KB operand chunks
   static constexpr int kKStages = 0;     // raw code pages: K ring
   static constexpr int kVStages = 0;     // raw code pages: V ring
@@ -64,13 +65,16 @@ struct Cfg<false> {
   static constexpr int kAbFormat = 1;    // bf16 operands
   static constexpr int kSCols = 64;      // TMEM columns of one S^T buffer: 64 heads
   static constexpr int kOBufs = 2;       // O^T buffers (pieces alternate)
+  static constexpr int kGroups = 1;      // softmax warpgroups (each owns 64 / kGroups heads)
+  static constexpr int kSoftmaxThreads = 128 * kGroups;
+  static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
 };
-// E4M3: warp 4 stages the K tiles and scales, warp 6 the V pages, warp 7
-// finds each piece's largest V scale; both products run as 8-bit MMAs on the
-// raw staged pages, so no code is converted on chip.
+// E4M3: the producer stages the K tiles and scales, a second producer warp
+// the V pages, and one warp finds each piece's largest V scale; both products
+// run as 8-bit MMAs on the raw staged pages, so no code is converted on chip.
 template <>
 struct Cfg<true> {
-  static constexpr int kThreads = 256;
+  static constexpr int kThreads = 384;    // two softmax warpgroups, then 4 single-warp roles
   static constexpr int kSlots = 0;        // K and V are read raw by 8-bit MMAs: no operand ring
   static constexpr int kKStages = 2;      // raw K tiles (both pages of a tile, 32 KB): A of S^T
   static constexpr int kVStages = 4;      // raw V pages (16 KB): A of P.V
@@ -80,13 +84,12 @@ struct Cfg<true> {
   static constexpr int kScaleSlots = 4;
   static constexpr int kSCols = 128;      // S^T against both Q terms: [term][head]
   static constexpr int kOBufs = 1;        // O^T is [half][term][head] = 256 columns
+  static constexpr int kGroups = 2;       // softmax warpgroups: heads 0-31 and 32-63
+  static constexpr int kSoftmaxThreads = 128 * kGroups;
+  static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
+  static constexpr int kVProducerWarp = kProducerWarp + 2, kVRefWarp = kProducerWarp + 3;
 };
 
-constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerWarp = 4;
-constexpr int kVProducerWarp = 6;         // E4M3 only
-constexpr int kVRefWarp = 7;              // E4M3 only
-constexpr int kMmaWarp = 5;
 constexpr int kSlotBytes = 16384;
 constexpr int kStageBytes = 16384;        // one E4M3 V page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
 constexpr int kKTileBytes = 32768;        // one E4M3 K tile: box h (dims [128h, 128h+128)) of 128 rows at 16 KB * h
@@ -186,18 +189,22 @@ struct Ctx {
   __device__ bool wait(int i, uint32_t parity) const { return mbar_wait(bar(i), parity, budget, abort, err); }
 };
 
-__device__ __forceinline__ void named_barrier_softmax() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-}
-// The same barrier, returning the OR of `pred` over the softmax threads.
-__device__ __forceinline__ bool named_barrier_softmax_or(bool pred) {
+// Named barriers of the softmax warps: 1 + g for warpgroup g (128 threads),
+// 3 for all of them.
+__device__ __forceinline__ void barrier_group(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
+// The group barrier, returning the OR of `pred` over the group's threads.
+__device__ __forceinline__ bool barrier_group_or(int g, bool pred) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)pred), "n"(kSoftmaxThreads)
+      : "r"((uint32_t)pred), "r"(1 + g)
       : "memory");
   return r != 0;
+}
+template <int kThreadsAll>
+__device__ __forceinline__ void barrier_softmax_all() {
+  asm volatile("bar.sync 3, %0;" ::"n"(kThreadsAll) : "memory");
 }
 // 2^x with the multi-function unit's approximation (relative error below
 // 2^-22; subnormal results flush to zero, 2^-inf = 0).
@@ -751,63 +758,54 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
 }
 
 // ---------------------------------------------------------------- softmax
-// Per-thread: row t of S^T (token t of the tile), 64 head columns.
-__device__ __forceinline__ void warp_reduce_scatter_max(float (&v)[64], int lane) {
-  // after the 5 steps lane l holds the maxima of columns 2l and 2l+1 over the warp
+// Warpgroup g of the softmax warps owns heads [h0, h0 + kHpt), h0 = g * kHpt
+// (kHpt = 64 / groups); its thread r (0..127) owns TMEM lane r: token r of
+// the tile in S^T, dim r of each 128-dim half of O^T. The row statistics of
+// different heads never meet, so each group keeps its own reference maxima,
+// rescale decisions and named barrier.
+
+// Butterfly reduce-scatter over the warp: afterwards lane l holds the result
+// for columns (N / 32) * l + i, i < N / 32, in v[i].
+template <int N, bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
+  static_assert(N % 32 == 0, "columns");
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
-    const int half = 32 >> step;
+    const int half = (N / 2) >> step;
     const int o = 16 >> step;
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
       const float keep = up ? v[i + half] : v[i];
       const float send = up ? v[i] : v[i + half];
-      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
-    }
-  }
-}
-__device__ __forceinline__ void warp_reduce_scatter_sum(float (&v)[64], int lane) {
-#pragma unroll
-  for (int step = 0; step < 5; ++step) {
-    const int half = 32 >> step;
-    const int o = 16 >> step;
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float keep = up ? v[i + half] : v[i];
-      const float send = up ? v[i] : v[i + half];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      const float other = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, other) : keep + other;
     }
   }
 }
 
-// One S^T row as log2-domain logits minus the reference maxima:
-//   x[h] = S[h] * colmul[h] * mult - m[h]
-// (E4M3: S is the sum of the two Q terms' columns and colmul the heads'
-// 2^-e_h; bf16: colmul = 1); m = nullptr gives the plain logits. Rows past
-// the sequence read -inf (only a partial tile has such rows). Returns the
-// largest x. colmul and m are 16-byte aligned and uniform.
-template <bool kFp8>
-__device__ __forceinline__ float load_logits(uint32_t taddr, bool full, bool valid, float mult, const float* colmul,
-                                             const float* m, float (&x)[64]) {
-  if constexpr (kFp8) {
+// kHpt columns of one S^T row (taddr: the group's first column) as
+// log2-domain logits minus the reference maxima: x[h] = S[h] * mult - m[h]
+// (E4M3: S is the sum of the two Q terms' columns, 64 apart); m = nullptr
+// gives the plain logits. Rows past the sequence read -inf (only a partial
+// tile has such rows). Returns the largest x. m is 16-byte aligned, uniform.
+template <bool kFp8, int kHpt>
+__device__ __forceinline__ float load_logits(uint32_t taddr, bool full, bool valid, float mult, const float* m,
+                                             float (&x)[kHpt]) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+  for (int q = 0; q < kHpt / 32; ++q) {
+    tmem_ld32(taddr + q * 32, x + q * 32);
+    if constexpr (kFp8) {
       float y[32];
-      tmem_ld32(taddr + q * 32, x + q * 32);
       tmem_ld32(taddr + 64 + q * 32, y);
       tc_wait_ld();
 #pragma unroll
       for (int h = 0; h < 32; ++h) x[q * 32 + h] += y[h];
     }
-  } else {
-    tmem_ld32(taddr, x);
-    tmem_ld32(taddr + 32, x + 32);
-    tc_wait_ld();
   }
+  if constexpr (!kFp8) tc_wait_ld();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < kHpt / 4; ++i) {
     const float4 r = m ? reinterpret_cast<const float4*>(m)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     x[4 * i] = fmaf(x[4 * i], mult, -r.x);
     x[4 * i + 1] = fmaf(x[4 * i + 1], mult, -r.y);
@@ -816,35 +814,41 @@ __device__ __forceinline__ float load_logits(uint32_t taddr, bool full, bool val
   }
   if (!full) {
 #pragma unroll
-    for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] : -INFINITY;
+    for (int h = 0; h < kHpt; ++h) x[h] = valid ? x[h] : -INFINITY;
   }
   float dm = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
+  for (int i = 0; i < kHpt / 4; ++i)
     dm = fmaxf(dm, fmaxf(fmaxf(x[4 * i], x[4 * i + 1]), fmaxf(x[4 * i + 2], x[4 * i + 3])));
   return dm;
 }
 
 // E4M3: the bf16 Q of a piece (four 64-dim boxes of [64 heads x 128 B],
 // 128-byte swizzle, as TMA loaded it) becomes, in place, two E4M3 terms
-// t1 + t2 of Q_h * 2^e_h: 128-dim box b (16 KB at 16 KB * b) holds t1 of the
-// 64 heads, then t2 ([128 rows x 128 B], 128-byte swizzle). 2^e_h is the
-// largest power of two with max_d |Q_hd| * 2^e_h <= 448 (the E4M3 maximum);
-// t1 rounds the scaled value, t2 the remainder, which is exact unless it
-// falls below the E4M3 normal range (absolute error at most 2^-10 there,
-// i.e. 2^-18 of the head's largest |Q|). qinv[h] = 2^-e_h. Thread tid: head
-// tid % 64, dims [128 (tid / 64), +128). Ends with every thread's terms
-// written and fenced for the tensor cores (the caller then arrives on the
-// ready barrier).
-__device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float* qinv, int tid) {
-  const int h = tid & 63, half = tid >> 6;
-  uint4 v[16];  // chunk j: dims [8j, 8j + 8) of this thread's half
+// t1 + t2 of Q * 2^e: 128-dim box b (16 KB at 16 KB * b) holds t1 of the 64
+// heads, then t2 ([128 rows x 128 B], 128-byte swizzle). 2^e is the largest
+// power of two with max |Q| * 2^e <= 448 (the E4M3 maximum); t1 rounds the
+// scaled value, t2 the remainder, which is exact unless it falls below the
+// E4M3 normal range (absolute error at most 2^-10 there, i.e. 2^-18.8 of the
+// largest |Q|: elements down to 2^-10.8 of it are held exactly). Run by all
+// kThreadsAll softmax threads: thread t takes head t % 64 and dims
+// [D (t / 64), +D), D = 256 / (kThreadsAll / 64). scratch: one float per
+// warp. Returns 2^-e. Ends with every thread's terms written and fenced for
+// the tensor cores (the caller then arrives on the ready barrier).
+template <int kThreadsAll>
+__device__ __forceinline__ float split_q_e4m3(uint32_t q_addr, float* scratch, int tid) {
+  constexpr int kParts = kThreadsAll / 64, kDims = kHeadDim / kParts, kIn = kDims / 8;
+  static_assert(kDims % 16 == 0, "16-dim output chunks");
+  const int h = tid & 63, part = tid >> 6, d0 = part * kDims;
+  uint4 v[kIn];  // input chunk j: dims [d0 + 8j, +8) in bf16 box (d0 + 8j) / 64
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    v[j] = ld_shared_v4(q_addr + (2 * half + (j >> 3)) * 8192 + h * 128 + (((j & 7) ^ (h & 7)) << 4));
+  for (int j = 0; j < kIn; ++j) {
+    const int d = d0 + 8 * j;
+    v[j] = ld_shared_v4(q_addr + (d >> 6) * 8192 + h * 128 + ((((d & 63) >> 3) ^ (h & 7)) << 4));
+  }
   float mx = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < kIn; ++j) {
     const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
     for (int k = 0; k < 4; ++k)
@@ -852,9 +856,11 @@ __device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float*
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((tid & 31) == 0) red[tid >> 5] = mx;
-  named_barrier_softmax();  // every thread has its Q values: the buffer may be overwritten
-  const float gm = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  if ((tid & 31) == 0) scratch[tid >> 5] = mx;
+  barrier_softmax_all<kThreadsAll>();  // every thread has its Q values: the buffer may be overwritten
+  float gm = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kThreadsAll / 32; ++w) gm = fmaxf(gm, scratch[w]);
   int e = 0;
   if (gm > 0.0f && gm <= 3.0e38f) {
     const uint32_t bits = __float_as_uint(gm);
@@ -863,9 +869,8 @@ __device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float*
     e = max(-126, min(126, e));
   }
   const float sq = __uint_as_float((uint32_t)(e + 127) << 23);
-  if (tid == 0) qinv[0] = __uint_as_float((uint32_t)(127 - e) << 23);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // output chunk k: dims [16k, 16k + 16) = input chunks 2k, 2k + 1
+  for (int k = 0; k < kDims / 16; ++k) {  // output chunk: dims [d0 + 16k, +16) = input chunks 2k, 2k + 1
     uint32_t t1[4], t2[4];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -890,28 +895,34 @@ __device__ __forceinline__ void split_q_e4m3(uint32_t q_addr, float* red, float*
         t2[2 * u + i] = c2w;
       }
     }
-    const uint32_t o = half * 16384 + h * 128 + ((k ^ (h & 7)) << 4);
+    const int d = d0 + 16 * k;
+    const uint32_t o = (d >> 7) * 16384 + h * 128 + ((((d & 127) >> 4) ^ (h & 7)) << 4);
     st_shared_v4(q_addr + o, make_uint4(t1[0], t1[1], t1[2], t1[3]));
     st_shared_v4(q_addr + kQTermBytes + o, make_uint4(t2[0], t2[1], t2[2], t2[3]));
   }
   fence_proxy_async_smem();
+  return __uint_as_float((uint32_t)(127 - e) << 23);
 }
 
-// O^T columns (this thread's TMEM lane, both 128-dim halves) times
-// col_scale[head]; E4M3: both terms' columns of each head.
-template <bool kFp8>
-__device__ __forceinline__ void scale_o_columns(uint32_t taddr_o, const float* col_scale) {
+// The group's O^T columns (this thread's TMEM lane, both 128-dim halves)
+// times col_scale[head - h0]; E4M3: both terms' columns of each head.
+template <bool kFp8, int kHpt>
+__device__ __forceinline__ void scale_o_columns(uint32_t taddr_o, int h0, const float* col_scale) {
   constexpr int kHalfCols = kFp8 ? 128 : 64;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-    for (int q = 0; q < kHalfCols / 32; ++q) {
-      float o[32];
-      tmem_ld32(taddr_o + hf * kHalfCols + q * 32, o);
-      tc_wait_ld();
+    for (int tm = 0; tm < (kFp8 ? 2 : 1); ++tm) {
 #pragma unroll
-      for (int h = 0; h < 32; ++h) o[h] *= col_scale[(q & 1) * 32 + h];
-      tmem_st32(taddr_o + hf * kHalfCols + q * 32, o);
+      for (int q = 0; q < kHpt / 32; ++q) {
+        const uint32_t a = taddr_o + hf * kHalfCols + tm * 64 + h0 + q * 32;
+        float o[32];
+        tmem_ld32(a, o);
+        tc_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h) o[h] *= col_scale[q * 32 + h];
+        tmem_st32(a, o);
+      }
     }
   }
   tc_wait_st();
@@ -933,16 +944,19 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
                              long long lo, long long hi, uint32_t tmem, int c, uint8_t* gbase) {
   using C = Cfg<kFp8>;
   using Bb = Bars<kFp8>;
-  const int tid = threadIdx.x;  // 0..127: TMEM lane = token of the tile = dim of each O^T half
-  const int warp = tid >> 5, lane = tid & 31;
+  constexpr int kHpt = 64 / C::kGroups;  // heads per thread
+  const int g = threadIdx.x >> 7;        // head group
+  const int row = threadIdx.x & 127;     // TMEM lane = token of the tile = dim of each O^T half
+  const int quad = row >> 5, lane = row & 31;
+  const int h0 = g * kHpt;
   const SmemLayout L = smem_layout<kFp8>(p.B);
   float* red = reinterpret_cast<float*>(gbase + L.red);  // [4][64] per-warp partial reductions
   float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
   float* alpha = mref + 64;                              // [64] rescale factors, uniform
   float* inv_l = alpha + 64;                             // [2][64] 1/l of the piece in O^T buffer i
-  float* qinv = inv_l + 128;                             // [64] E4M3: 2^-e_h of the piece's Q terms
-  float* s_vref = qinv + 64;                             // [2] E4M3: largest V scale of a piece
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  float* qscratch = inv_l + 128;                         // [8] E4M3: per-warp max |Q|
+  float* s_vref = qscratch + 64;                         // [2] E4M3: largest V scale of a piece
+  const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const uint32_t taddr_o0 = tmem + lane_base + tmem_o<kFp8>();
   const float c2 = p.scale * kLog2e;
   uint32_t s_cnt = 0, p_cnt = 0;
@@ -951,7 +965,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   // exists, so when it waits for P.V(g) that barrier is at phase g/2 or just
   // past it: the parity wait is exact. Completion of P.V(g) implies that of
   // every earlier MMA (one issuing thread, commits track all prior MMAs).
-  auto wait_pv = [&](uint32_t g) -> bool { return cx.wait(Bb::PEmpty + (g & 1), (g >> 1) & 1); };
+  auto wait_pv = [&](uint32_t gi) -> bool { return cx.wait(Bb::PEmpty + (gi & 1), (gi >> 1) & 1); };
   // Pieces cycle through the O^T buffers. A piece's O^T / l is written out
   // once the next piece's first P has been handed over (its last P.V was
   // issued before that piece's first S), so the softmax warps go on to the
@@ -964,25 +978,25 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     if (!wait_pv(pend_pv)) return false;
     tc_fence_after();
     const uint32_t ta = taddr_o0 + pend_obuf * 128;
-    const float* il = inv_l + pend_obuf * 64;
-    float* dst = p.part_o + pend_slot * kHeads * kHeadDim;
+    const float* il = inv_l + pend_obuf * 64 + h0;
+    float* dst = p.part_o + (pend_slot * kHeads + h0) * kHeadDim;
     constexpr int kHalfCols = kFp8 ? 128 : 64;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < kHpt / 32; ++q) {
         float o[32];
-        tmem_ld32(ta + hf * kHalfCols + q * 32, o);
+        tmem_ld32(ta + hf * kHalfCols + h0 + q * 32, o);
         if constexpr (kFp8) {  // + the second P term's columns
           float o2[32];
-          tmem_ld32(ta + hf * kHalfCols + 64 + q * 32, o2);
+          tmem_ld32(ta + hf * kHalfCols + 64 + h0 + q * 32, o2);
           tc_wait_ld();
 #pragma unroll
           for (int h = 0; h < 32; ++h) o[h] += o2[h];
         } else {
           tc_wait_ld();
         }
-        const int dim = hf * 128 + tid;
+        const int dim = hf * 128 + row;
 #pragma unroll
         for (int h = 0; h < 32; ++h) dst[(q * 32 + h) * kHeadDim + dim] = o[h] * il[q * 32 + h];
       }
@@ -1000,8 +1014,9 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const uint32_t obuf = piece % C::kOBufs;
     const uint32_t taddr_o = taddr_o0 + obuf * 128;
     // E4M3: P enters the 8-bit P.V as P * v_scale * pscale (<= 256); O^T is
-    // then pscale times too large, which the epilogue undoes
-    float pscale = 1.0f;
+    // then pscale times too large, which the epilogue undoes. Q enters S^T
+    // as 2^e Q, undone by qinv in the token multiplier.
+    float pscale = 1.0f, qinv = 1.0f;
     if constexpr (kFp8) {
       const uint32_t vslot = piece & 1;
       if (!cx.wait(Bb::VRefFull + vslot, (piece >> 1) & 1)) return;
@@ -1010,19 +1025,19 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       // Q of the piece -> E4M3 terms (the producer loaded it once the previous
       // piece's S MMAs were done)
       if (!cx.wait(Bb::QFull, piece & 1)) return;
-      split_q_e4m3(cx.base + L.q, red, qinv, tid);
+      qinv = split_q_e4m3<C::kSoftmaxThreads>(cx.base + L.q, qscratch, threadIdx.x);
       mbar_arrive(cx.bar(Bb::QReady));
     }
-    if (tid < 64) mref[tid] = -INFINITY;
-    named_barrier_softmax();
-    float lp[64];  // this thread's share of the softmax denominators
+    if (row < kHpt) mref[h0 + row] = -INFINITY;
+    barrier_group(g);
+    float lp[kHpt];  // this thread's share of the softmax denominators
 #pragma unroll
-    for (int h = 0; h < 64; ++h) lp[h] = 0.0f;
+    for (int h = 0; h < kHpt; ++h) lp[h] = 0.0f;
     const int T = tiles_of(s);
     for (int t = 0; t < T; ++t) {
       const int tok0 = (s.pg0 + 2 * t) * kPageSize;
       const int rows = min(pages_in_tile(s, t) * kPageSize, s.len - tok0);  // valid rows of the tile
-      const bool full = rows == 128, valid = tid < rows;
+      const bool full = rows == 128, valid = row < rows;
       // E4M3: this token's K and V scales (the tile's scale block, slot = tile count)
       float kmul = c2, vmul = 1.0f;
       if constexpr (kFp8) {
@@ -1030,47 +1045,48 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         if (!cx.wait(Bb::ScFull + slot, (p_cnt / C::kScaleSlots) & 1)) return;
         const float* sc = reinterpret_cast<const float*>(gbase + L.scales + slot * kScaleBytes);
         if (valid) {
-          kmul = c2 * qinv[0] * sc[tid];
-          vmul = sc[128 + tid] * pscale;
+          kmul = c2 * qinv * sc[row];
+          vmul = sc[128 + row] * pscale;
         }
         mbar_arrive(cx.bar(Bb::ScEmpty + slot));
       }
       const uint32_t sbuf = s_cnt & 1;
-      const uint32_t taddr_s = tmem + lane_base + sbuf * C::kSCols;
+      const uint32_t taddr_s = tmem + lane_base + sbuf * C::kSCols + h0;
       if (!cx.wait(Bb::SFull + sbuf, (s_cnt >> 1) & 1)) return;
       tc_fence_after();
-      float x[64];
+      float x[kHpt];
       // x = logit - reference maximum (log2 units)
-      const bool mine = load_logits<kFp8>(taddr_s, full, valid, kmul, qinv, mref, x) > rescale_threshold<kFp8>();
-      // ---- does any logit of the tile exceed its reference maximum by 2^threshold?
-      if (named_barrier_softmax_or(mine)) {
-        (void)load_logits<kFp8>(taddr_s, full, valid, kmul, qinv, nullptr, x);
-        warp_reduce_scatter_max(x, lane);  // x is reloaded below
-        red[warp * 64 + 2 * lane] = x[0];
-        red[warp * 64 + 2 * lane + 1] = x[1];
-        named_barrier_softmax();
-        if (tid < 64) {
-          const float m_old = mref[tid];
-          const float m_new = fmaxf(m_old, fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid])));
-          alpha[tid] = ex2_approx(m_old - m_new);  // 0 while m_old = -inf
-          mref[tid] = m_new;
+      const bool mine = load_logits<kFp8, kHpt>(taddr_s, full, valid, kmul, mref + h0, x) > rescale_threshold<kFp8>();
+      // ---- does any logit of the group's heads exceed its reference maximum by 2^threshold?
+      if (barrier_group_or(g, mine)) {
+        (void)load_logits<kFp8, kHpt>(taddr_s, full, valid, kmul, nullptr, x);
+        warp_reduce_scatter<kHpt, true>(x, lane);  // x is reloaded below
+#pragma unroll
+        for (int i = 0; i < kHpt / 32; ++i) red[quad * 64 + h0 + (kHpt / 32) * lane + i] = x[i];
+        barrier_group(g);
+        if (row < kHpt) {
+          const int h = h0 + row;
+          const float m_old = mref[h];
+          const float m_new = fmaxf(m_old, fmaxf(fmaxf(red[h], red[64 + h]), fmaxf(red[128 + h], red[192 + h])));
+          alpha[h] = ex2_approx(m_old - m_new);  // 0 while m_old = -inf
+          mref[h] = m_new;
         }
-        named_barrier_softmax();
+        barrier_group(g);
         bool rescale_o = false;
         if (t > 0) {  // the first tile of a piece has nothing to rescale
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
-            lp[h] *= alpha[h];
-            rescale_o |= alpha[h] != 1.0f;
+          for (int h = 0; h < kHpt; ++h) {
+            lp[h] *= alpha[h0 + h];
+            rescale_o |= alpha[h0 + h] != 1.0f;
           }
         }
         if (rescale_o) {
-          // O^T holds the previous tiles: wait for their last P.V, then scale its columns
+          // O^T holds the previous tiles: wait for their last P.V, then scale the group's columns
           if (!wait_pv(p_cnt - 1)) return;
           tc_fence_after();
-          scale_o_columns<kFp8>(taddr_o, alpha);
+          scale_o_columns<kFp8, kHpt>(taddr_o, h0, alpha + h0);
         }
-        (void)load_logits<kFp8>(taddr_s, full, valid, kmul, qinv, mref, x);
+        (void)load_logits<kFp8, kHpt>(taddr_s, full, valid, kmul, mref + h0, x);
       }
       tc_fence_before();
       mbar_arrive(cx.bar(Bb::SEmpty + sbuf));  // S^T buffer free for the tile after next
@@ -1082,10 +1098,11 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       // chunk j = x1 and chunk 4 + j = x2 of heads [16j, 16j + 16).
       const uint32_t pbuf = p_cnt & 1;
       if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
-      const uint32_t prow = cx.base + L.p + pbuf * kPBytes + tid * 128;
+      const uint32_t prow = cx.base + L.p + pbuf * kPBytes + row * 128;
       constexpr int kHeadsPerChunk = kFp8 ? 16 : 8;
 #pragma unroll
-      for (int j = 0; j < 64 / kHeadsPerChunk; ++j) {
+      for (int j = 0; j < kHpt / kHeadsPerChunk; ++j) {
+        const int jj = h0 / kHeadsPerChunk + j;  // chunk index within the row
         uint32_t w1[4], w2[4];
 #pragma unroll
         for (int k = 0; k < kHeadsPerChunk / 2; ++k) {
@@ -1115,8 +1132,9 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
             w1[k] = pack2<kFp8>(p0, p1);
           }
         }
-        st_shared_v4(prow + ((j ^ (tid & 7)) << 4), make_uint4(w1[0], w1[1], w1[2], w1[3]));
-        if constexpr (kFp8) st_shared_v4(prow + (((4 + j) ^ (tid & 7)) << 4), make_uint4(w2[0], w2[1], w2[2], w2[3]));
+        st_shared_v4(prow + ((jj ^ (row & 7)) << 4), make_uint4(w1[0], w1[1], w1[2], w1[3]));
+        if constexpr (kFp8)
+          st_shared_v4(prow + (((4 + jj) ^ (row & 7)) << 4), make_uint4(w2[0], w2[1], w2[2], w2[3]));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -1126,18 +1144,19 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     }
     // ---- epilogue of this sequence piece: l = sum over the 128 lanes and the
     // LSE (final once the last P is out); O^T / l follows later (write_o)
-    warp_reduce_scatter_sum(lp, lane);
-    named_barrier_softmax();  // earlier readers of red/alpha are done
-    red[warp * 64 + 2 * lane] = lp[0];
-    red[warp * 64 + 2 * lane + 1] = lp[1];
-    named_barrier_softmax();
+    warp_reduce_scatter<kHpt, false>(lp, lane);
+    barrier_group(g);  // earlier readers of red/alpha are done
+#pragma unroll
+    for (int i = 0; i < kHpt / 32; ++i) red[quad * 64 + h0 + (kHpt / 32) * lane + i] = lp[i];
+    barrier_group(g);
     const size_t slot = (size_t)c + s.b;
-    if (tid < 64) {
-      const float l = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
-      inv_l[obuf * 64 + tid] = 1.0f / (l * pscale);
-      p.part_lse[slot * kHeads + tid] = (mref[tid] + log2f(l)) * kLn2;
+    if (row < kHpt) {
+      const int h = h0 + row;
+      const float l = red[h] + red[64 + h] + red[128 + h] + red[192 + h];
+      inv_l[obuf * 64 + h] = 1.0f / (l * pscale);
+      p.part_lse[slot * kHeads + h] = (mref[h] + log2f(l)) * kLn2;
     }
-    named_barrier_softmax();
+    barrier_group(g);
     pend = true;
     pend_pv = p_cnt - 1;
     pend_obuf = obuf;
@@ -1173,14 +1192,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars + 8 * (Bb::QFull + i), 1);
       mbar_init(bars + 8 * (Bb::QEmpty + i), 1);
-      mbar_init(bars + 8 * (Bb::QReady + i), kSoftmaxThreads);
+      mbar_init(bars + 8 * (Bb::QReady + i), C::kSoftmaxThreads);
       mbar_init(bars + 8 * (Bb::SFull + i), 1);
-      mbar_init(bars + 8 * (Bb::SEmpty + i), kSoftmaxThreads);
-      mbar_init(bars + 8 * (Bb::PFull + i), kSoftmaxThreads);
+      mbar_init(bars + 8 * (Bb::SEmpty + i), C::kSoftmaxThreads);
+      mbar_init(bars + 8 * (Bb::PFull + i), C::kSoftmaxThreads);
       mbar_init(bars + 8 * (Bb::PEmpty + i), 1);
     }
-    mbar_init(bars + 8 * (Bb::OFree + 0), kSoftmaxThreads);
-    mbar_init(bars + 8 * (Bb::OFree + 1), kSoftmaxThreads);
+    mbar_init(bars + 8 * (Bb::OFree + 0), C::kSoftmaxThreads);
+    mbar_init(bars + 8 * (Bb::OFree + 1), C::kSoftmaxThreads);
     mbar_init(bars + 8 * Bb::Drain, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bars + 8 * (Bb::StFull + i), 1);
@@ -1188,21 +1207,21 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars + 8 * (Bb::VRefFull + i), 1);
-      mbar_init(bars + 8 * (Bb::VRefEmpty + i), kSoftmaxThreads);
+      mbar_init(bars + 8 * (Bb::VRefEmpty + i), C::kSoftmaxThreads);
     }
     for (int i = 0; i < C::kScaleSlots; ++i) {
       mbar_init(bars + 8 * (Bb::ScFull + i), 1);
-      mbar_init(bars + 8 * (Bb::ScEmpty + i), kSoftmaxThreads);
+      mbar_init(bars + 8 * (Bb::ScEmpty + i), C::kSoftmaxThreads);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kProducerWarp && (threadIdx.x & 31) == 0) {
+  if (warp == C::kProducerWarp && (threadIdx.x & 31) == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
     prefetch_tensormap(&qmap);
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + L.misc),
                  "n"(kTmemCols)
                  : "memory");
@@ -1220,22 +1239,22 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const long long lo = cta_cost_lo(c, units, p.grid), hi = cta_cost_lo(c + 1, units, p.grid);
   Ctx cx{base, bars, abort_flag, p.err, p.wait_budget_ns};
 
-  if (warp < 4) {
+  if (warp < 4 * C::kGroups) {
     softmax_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
-  } else if (warp == kProducerWarp) {
+  } else if (warp == C::kProducerWarp) {
     producer_role<kFp8>(p, &kmap, &vmap, &qmap, cx, s_cost, s_len, lo, hi);
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
-    if (warp == kVProducerWarp)
+    if (warp == C::kVProducerWarp)
       producer_v_role(p, &vmap, cx, s_cost, s_len, lo, hi);
-    else if (warp == kVRefWarp)
+    else if (warp == C::kVRefWarp)
       vref_role(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 9 * 64);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp)
+  if (warp == C::kMmaWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
 }
 
