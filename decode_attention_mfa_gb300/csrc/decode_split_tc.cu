@@ -54,7 +54,7 @@ template <bool kFp8>
 struct Cfg;
 template <>
 struct Cfg<false> {
-  static constexpr int kThreads = 192;   // softmax warpgroup, producer, MMA
+  static constexpr int kThreads = 320;   // two softmax warpgroups, producer, MMA
   static constexpr int kSlots = 7;       // 16 KB operand chunks
   static constexpr int kKStages = 0;     // raw code pages: K ring
   static constexpr int kVStages = 0;     // raw code pages: V ring
@@ -65,7 +65,7 @@ struct Cfg<false> {
   static constexpr int kAbFormat = 1;    // bf16 operands
   static constexpr int kSCols = 64;      // TMEM columns of one S^T buffer: 64 heads
   static constexpr int kOBufs = 2;       // O^T buffers (pieces alternate)
-  static constexpr int kGroups = 1;      // softmax warpgroups (each owns 64 / kGroups heads)
+  static constexpr int kGroups = 2;      // softmax warpgroups (each owns 64 / kGroups heads)
   static constexpr int kSoftmaxThreads = 128 * kGroups;
   static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
 };
