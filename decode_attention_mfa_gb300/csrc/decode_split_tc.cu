@@ -1228,6 +1228,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     tc_fence_before();
   }
+  if (threadIdx.x == 0) {
+    // the page table and Q are not written by the KV append: warm this CTA's
+    // share of both in L2 while the append finishes (the first page-id and Q
+    // reads are otherwise two dependent HBM round trips at start)
+    prefetch_l2_share(p.page_table, (size_t)p.B * p.max_pages * sizeof(int32_t), blockIdx.x, gridDim.x);
+    prefetch_l2_share(p.q, (size_t)p.B * kHeads * kHeadDim * sizeof(uint16_t), blockIdx.x, gridDim.x);
+  }
   pdl_wait_prior_grid();    // the KV append (or previous step) must be complete before reading its results
   pdl_launch_dependents();  // the combine kernel may be scheduled now (its prologue reads seq_lens); it
                             // waits for this grid before it reads the partials

@@ -165,6 +165,21 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// Block `blk` of `nblk` prefetches its share of a buffer of `bytes` bytes
+// into L2, in pieces of at most 64 KB (nothing if the buffer is not 16-byte
+// aligned: the bulk prefetch requires it).
+__device__ __forceinline__ void prefetch_l2_share(const void* base, size_t bytes, int blk, int nblk) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return;
+  const size_t per = ((bytes + (size_t)nblk - 1) / nblk + 15) & ~(size_t)15;
+  size_t lo = per * (size_t)blk;
+  const size_t hi = min(bytes & ~(size_t)15, lo + per);
+  for (; lo < hi; lo += 65536)
+    prefetch_l2(static_cast<const uint8_t*>(base) + lo, (uint32_t)min((size_t)65536, hi - lo));
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
