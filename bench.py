@@ -2,8 +2,10 @@
 """Benchmark of the MFA decode hot path on GB300.
 
 One step = one decode step of a whole batch through the C ABI:
-    mfa_kv_append (one new token per sequence)
-    -> mfa_decode_attention (split-KV kernel + LSE combine) over the cache.
+    mfa_decode_attention (split-KV kernel + LSE combine) over the cache,
+preceded by mfa_kv_append (one new token per sequence) for the workload
+that appends before attending (ragged); the others attend over a cache of
+fixed length.
 Inputs are seeded synthetic data with the workload's shapes (64 query heads
 sharing one K/V head, d = 256, 64-token pages in a random page permutation).
 
@@ -14,9 +16,9 @@ Prints one JSON line (rank 0).  `value` is achieved HBM throughput in TB/s:
 algorithmic bytes (KV rows attended, queries, outputs, page-table entries and
 the append traffic, each counted once) divided by device time, with every
 input resident in HBM.  The timed region replays CUDA graphs of the steps.
-To defeat the 135 MB L2, steps rotate over many device-resident copies of the
-cache, so a step never finds its cache in L2; each copy grows by one token per
-visit, and the mean attended length is reported.
+To defeat the 135 MB L2, steps rotate over device-resident copies of the
+cache, so a step never finds its cache in L2; with an append each copy grows
+by one token per visit, and the mean attended length is reported.
 """
 from __future__ import annotations
 
@@ -130,18 +132,25 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ workload
+def appends(w: wl.Workload) -> bool:
+    """Whether a step of the workload appends one token per sequence first."""
+    return w.append_tokens > 0
+
+
 def bench_lengths(w: wl.Workload) -> np.ndarray:
-    """Cache lengths before the first timed append: the workload's own lengths
-    for a workload that appends before attending, else one token fewer, so the
-    first step attends over exactly the configured length."""
-    lens = wl.draw_lengths(w)
-    return lens if w.append_tokens else lens - 1
+    """Cache lengths when the benchmark starts (the workload's own lengths)."""
+    return wl.draw_lengths(w)
+
+
+def first_attended(w: wl.Workload) -> np.ndarray:
+    """Lengths the first step attends over."""
+    return bench_lengths(w) + (1 if appends(w) else 0)
 
 
 def choose_copies(w: wl.Workload, lens: np.ndarray, total_steps: int) -> int:
     kv_copy = float(lens.sum()) * acc.kv_bytes_per_token(w.kv_dtype)
     need_l2 = math.ceil(3 * L2_BYTES / kv_copy) + 1
-    need_drift = math.ceil(total_steps / max(1.0, 0.01 * float(lens.mean())))
+    need_drift = math.ceil(total_steps / max(1.0, 0.01 * float(lens.mean()))) if appends(w) else 0
     cap = max(2, int(COPY_MEM_BUDGET // (2.2 * kv_copy)))
     return int(max(2, min(cap, max(need_l2, need_drift))))
 
@@ -233,27 +242,32 @@ def run_ours(args, rank, world, local):
     host_len = np.tile(lens0.astype(np.int64), (R, 1))  # host mirror of every copy's length
     step_bytes, split_bytes = [], []
 
+    app = appends(w)
+
     def step(r, qsrc=None, kvsrc=None):
         kn = newkv[0] if kvsrc is None else kvsrc[0]
         vn = newkv[1] if kvsrc is None else kvsrc[1]
         qq = q[r] if qsrc is None else qsrc
         sl = seq_lens[r]
         if fp8:
-            capi.mfa_kv_append_fp8(kn, vn, 1, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl,
-                                   B, max_pages, num_pages, workspace, stream)
+            if app:
+                capi.mfa_kv_append_fp8(kn, vn, 1, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table,
+                                       sl, B, max_pages, num_pages, workspace, stream)
             capi.mfa_decode_attention_fp8(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl,
                                           out, lse, wl.SCALE, B, max_pages, num_pages, ws_hint, workspace,
                                           ws_bytes, stream)
         else:
-            capi.mfa_kv_append(kn, vn, 1, k_caches[r], v_caches[r], page_table, sl, B, max_pages, num_pages,
-                               workspace, stream)
+            if app:
+                capi.mfa_kv_append(kn, vn, 1, k_caches[r], v_caches[r], page_table, sl, B, max_pages, num_pages,
+                                   workspace, stream)
             capi.mfa_decode_attention(qq, k_caches[r], v_caches[r], page_table, sl, out, lse, wl.SCALE, B,
                                       max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
 
     def account(r):
-        host_len[r] += 1
-        L = host_len[r]
-        step_bytes.append(acc.decode_step_bytes(L, w.kv_dtype, appended_tokens=1))
+        if app:
+            host_len[r] += 1
+        L = host_len[r].copy()
+        step_bytes.append(acc.decode_step_bytes(L, w.kv_dtype, appended_tokens=1 if app else 0))
         split_bytes.append(int(L.sum()) * acc.kv_bytes_per_token(w.kv_dtype) + B * wl.HEADS * wl.HEAD_DIM * 2
                            + int(((L + 63) // 64).sum()) * 4 + B * 4)
         return L
@@ -285,7 +299,8 @@ def run_ours(args, rank, world, local):
                 else:
                     hq, hkv, hout, hlse, dq, dkv = e2e_bufs
                     dq.copy_(hq, non_blocking=True)
-                    dkv.copy_(hkv, non_blocking=True)
+                    if app:
+                        dkv.copy_(hkv, non_blocking=True)
                     step(r, qsrc=dq, kvsrc=dkv)
                     hout.copy_(out, non_blocking=True)
                     hlse.copy_(lse, non_blocking=True)
@@ -368,7 +383,7 @@ def run_ours(args, rank, world, local):
         e_bytes, e_s = mdist.aggregate(float(sum(step_bytes[n_before:])), e_ms / 1e3)
         capi.mfa_check_device_errors(workspace, clear=True, stream=stream)
         e2e = {"value": e_bytes / e_s / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": int(hq.numel() * 2 + hkv.numel() * 2),
+               "h2d_bytes_per_step": int(hq.numel() * 2 + (hkv.numel() * 2 if app else 0)),
                "d2h_bytes_per_step": int(hout.numel() * 2 + hlse.numel() * 4),
                "ms_per_step": e_ms / args.steps, "how": "CUDA graph of the C-ABI calls with pinned-host copies"}
 
@@ -380,14 +395,15 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "description": w.description, "batch": B, "heads": wl.HEADS,
                    "head_dim": wl.HEAD_DIM, "page_size": wl.PAGE_SIZE, "kv_dtype": w.kv_dtype,
                    "mean_attended_len": mean_len,
-                   "step": "mfa_kv_append(1 token/seq) + mfa_decode_attention (split + LSE combine)",
+                   "step": ("mfa_kv_append(1 token/seq) + " if app else "") +
+                           "mfa_decode_attention (split + LSE combine)",
                    "l2": f"inputs rotate over {R} device-resident cache copies "
                          f"({R * float(lens0.sum()) * acc.kv_bytes_per_token(w.kv_dtype) / 1e9:.1f} GB >> 135 MB L2)",
                    "parallelism": f"dp{world} (independent batch per GPU)"},
         "steps_per_s": args.steps * world / max_s,
         "pct_of_measured_peak": 100.0 * value * 1e3 / peak_gbs,
         "pct_of_8TBps": 100.0 * value * 1e3 / NOMINAL_HBM_GBS,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (3 if app else 2) * args.steps,
         "clocks": clk,
         "roofline": {"bound": "hbm", "kernel": "decode split (mfa_decode_attention)",
                      "achieved": achieved, "peak": peak_gbs, "peak_source": peak_kind, "unit": "GB/s",
@@ -435,7 +451,7 @@ class OracleSampler:
         self.sl = case.lengths0.astype(np.int32)
         self.total_rows = case.batch * wl.HEADS
         self.order = np.random.default_rng(0).permutation(self.total_rows)
-        self.step_bytes = acc.decode_step_bytes(self.sl, w.kv_dtype, appended_tokens=1)
+        self.step_bytes = acc.decode_step_bytes(self.sl, w.kv_dtype, appended_tokens=w.append_tokens)
 
     def run(self, nrows: int) -> float:
         rows = self.order[:nrows]
@@ -468,7 +484,7 @@ def run_reference(args):
     if rank != 0:
         return None
     w = wl.WORKLOADS[args.workload]
-    lens = bench_lengths(w) + 1   # lengths attended in the first step of our arm
+    lens = first_attended(w)   # lengths attended in the first step of our arm
     threads = len(os.sched_getaffinity(0))
     sampler = OracleSampler(w, lens, threads)
     rows = sampler.rows_for(max(0.05, 150.0 / max(1, args.steps + args.warmup)))
@@ -499,7 +515,7 @@ def main():
     res, lens0 = run_ours(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(wl.WORKLOADS[args.workload], lens0 + 1)
+            res["cpu_baseline"] = cpu_baseline(wl.WORKLOADS[args.workload], first_attended(wl.WORKLOADS[args.workload]))
         print(json.dumps(res), flush=True)
     mdist.finalize()
 
