@@ -246,8 +246,9 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   st = check_decode_args(q, k_cache, v_cache, page_table, seq_lens, out, lse, batch, max_pages, num_pages,
                          max_len_hint, workspace, workspace_bytes, info.num_sms, &plan);
   if (st != MFA_OK) return st;
-  const DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out,
-                                            lse, scale, batch, max_pages, num_pages, workspace, plan);
+  DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse,
+                                      scale, batch, max_pages, num_pages, workspace, plan);
+  if (fp8) p.piece_cost = kPieceCostPagesFp8;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (g_prof_start && (e = cudaEventRecordWithFlags(g_prof_start, s, cudaEventRecordExternal)) != cudaSuccess)

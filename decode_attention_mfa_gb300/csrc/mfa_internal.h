@@ -26,6 +26,10 @@ constexpr size_t kPartialLseBytes = (size_t)kHeads * sizeof(float);
 // is charged this many page-equivalents (a CTA pays for loading Q and page
 // ids and for writing the partial result of each piece it holds).
 constexpr int kPieceCostPages = 1;
+// E4M3: a piece also splits Q into E4M3 terms and finds the largest V scale,
+// and a tile (two pages) streams in about half the time of a bf16 tile, so a
+// piece is worth more pages.
+constexpr int kPieceCostPagesFp8 = 2;
 
 struct AppendParams {
   const uint16_t* k_new;  // [B][n_new][256] bf16 bits
