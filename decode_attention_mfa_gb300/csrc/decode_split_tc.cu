@@ -650,35 +650,41 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       // one 128-dim box per half), B = both P terms side by side (tokens x
       // 128 [term][head], 128-byte swizzle): N = 128, so O^T half hf holds
       // V^T.x1 in columns 0-63 and V^T.x2 in 64-127; K = 32 tokens per MMA
+      // both pages of the tile are waited for (and a partial last page zeroed
+      // past its rows) first, then all the tile's P.V MMAs go out as one batch
+      uint32_t vs[2];
       for (int i = 0; i < np; ++i) {
         const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page
-        const uint32_t vslot = C::kKStages + vc % C::kVStages;
-        if (!wait_all(Bb::StFull + vslot, (vc / C::kVStages) & 1)) return false;
-        const uint32_t vs = cx.base + L.stage + C::kKStages * kKTileBytes + (vc % C::kVStages) * kStageBytes;
+        const uint32_t vslot = C::kKStages + (vc + i) % C::kVStages;
+        if (!wait_all(Bb::StFull + vslot, ((vc + i) / C::kVStages) & 1)) return false;
+        vs[i] = cx.base + L.stage + C::kKStages * kKTileBytes + ((vc + i) % C::kVStages) * kStageBytes;
         if (nv < kPageSize) {
           // rows [nv, 64) of both boxes (whole 128 B rows): code 0x7F is NaN and 0 * NaN would poison P.V
           const int nbytes = (kPageSize - nv) * 128;
           for (int off = lane * 16; off < nbytes; off += 32 * 16) {
-            st_shared_v4(vs + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
-            st_shared_v4(vs + 8192 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
+            st_shared_v4(vs[i] + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
+            st_shared_v4(vs[i] + 8192 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
           }
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (lane == 0) {
-          tc_fence_after();
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        for (int i = 0; i < np; ++i) {
           const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;  // token rows 64i..
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks)
-              tc_mma_f8(tmem + tmem_o<kFp8>() + hf * 128, smem_desc(vs + hf * 8192 + ks * 4096, 16, 1024, 2),
+              tc_mma_f8(tmem + tmem_o<kFp8>() + hf * 128, smem_desc(vs[i] + hf * 8192 + ks * 4096, 16, 1024, 2),
                         smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3(), !(first_of_seg && i == 0 && ks == 0));
-          tc_commit(cx.bar(Bb::StEmpty + vslot));  // the V page's stage is free once these MMAs are done
+          // the V page's stage is free once these MMAs are done
+          tc_commit(cx.bar(Bb::StEmpty + C::kKStages + (vc + i) % C::kVStages));
         }
-        __syncwarp();
-        ++vc;
       }
+      __syncwarp();
+      vc += np;
     } else {
     for (int i = 0; i < np; ++i) {
       const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page
