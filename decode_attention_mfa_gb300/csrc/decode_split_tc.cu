@@ -579,6 +579,13 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   int pend_t = -1;
   uint32_t pend_piece = 0;
 
+  // The thread that issues the MMAs and the commits that track them: lane 0
+  // (E4M3), or the lane elect.sync picks, lane 0 of the converged warp
+  // (bf16); measured, each form is the faster one for its kernel.
+  auto issuer = [&]() -> bool {
+    if constexpr (kFp8) return lane == 0;
+    else return elect_one();
+  };
   auto wait_all = [&](int bar, uint32_t parity) -> bool {
     const bool r = cx.wait(bar, parity);  // every lane polls the same barrier
     __syncwarp();
@@ -594,7 +601,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       // holds K.t1^T in columns 0-63 and K.t2^T in 64-127; K = 32 dims per MMA
       const uint32_t kslot = cc % C::kKStages;
       if (!wait_all(Bb::StFull + kslot, (cc / C::kKStages) & 1)) return false;
-      if (lane == 0) {
+      if (issuer()) {
         tc_fence_after();
         const uint32_t ka = cx.base + L.stage + kslot * kKTileBytes;
         const uint32_t qa = cx.base + L.q + qb * kQBytes;
@@ -615,7 +622,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       for (int d = 0; d < 4; ++d) {
         const uint32_t slot = cc % C::kSlots, ph = (cc / C::kSlots) & 1;
         if (!wait_all(Bb::Full + slot, ph)) return false;
-        if (lane == 0) {
+        if (issuer()) {
           tc_fence_after();
           const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
           const uint32_t b0 = cx.base + L.q + qb * kQBytes + d * 8192;
@@ -628,7 +635,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         __syncwarp();
         ++cc;
       }
-      if (lane == 0) tc_commit(cx.bar(Bb::SFull + buf));
+      if (issuer()) tc_commit(cx.bar(Bb::SFull + buf));
       __syncwarp();
       ++s_cnt;
       return true;
@@ -669,7 +676,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
           __syncwarp();
         }
       }
-      if (lane == 0) {
+      if (issuer()) {
         tc_fence_after();
         for (int i = 0; i < np; ++i) {
           const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;  // token rows 64i..
@@ -703,7 +710,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (lane == 0) {
+        if (issuer()) {
           tc_fence_after();
           const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;
 #pragma unroll
@@ -718,7 +725,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       }
     }
     }
-    if (lane == 0) {
+    if (issuer()) {
       tc_commit(cx.bar(Bb::PEmpty + buf));
     }
     __syncwarp();
@@ -734,7 +741,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       // S(g), then P.V(g - 1), in the producer's order
       for (int t = 0; alive && t < T; ++t) {
         alive = do_s(qb);
-        if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
+        if (alive && t == T - 1 && issuer()) tc_commit(cx.bar(Bb::QEmpty + qb));
         __syncwarp();
         if (alive && pend_t >= 0) alive = do_pv(pend_s, pend_t, pend_piece);
         pend_s = s;
@@ -743,10 +750,10 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       }
     } else {
       alive = do_s(qb);
-      if (alive && T == 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
+      if (alive && T == 1 && issuer()) tc_commit(cx.bar(Bb::QEmpty + qb));
       for (int t = 1; alive && t < T; ++t) {
         alive = do_s(qb);
-        if (alive && t == T - 1 && lane == 0) tc_commit(cx.bar(Bb::QEmpty + qb));
+        if (alive && t == T - 1 && issuer()) tc_commit(cx.bar(Bb::QEmpty + qb));
         __syncwarp();
         if (alive) alive = do_pv(s, t - 1, seg_i);
       }
@@ -756,7 +763,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   }
   if (C::kCrossPiece && alive && pend_t >= 0) (void)do_pv(pend_s, pend_t, pend_piece);
   // drain: wait for every MMA this thread issued before TMEM is released
-  if (lane == 0) {
+  if (issuer()) {
     tc_commit(cx.bar(Bb::Drain));
     (void)mbar_wait(cx.bar(Bb::Drain), 0, cx.budget, nullptr, p.err);
   }
