@@ -568,7 +568,6 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
                          long long hi, uint32_t tmem) {
   using C = Cfg<kFp8>;
   using Bb = Bars<kFp8>;
-  const int lane = threadIdx.x & 31;
   const SmemLayout L = smem_layout<kFp8>(p.B);
   uint32_t cc = 0, seg_i = 0, s_cnt = 0, p_cnt = 0;
   uint32_t vc = 0;  // E4M3: V pages consumed from the V stage ring
@@ -579,18 +578,11 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   int pend_t = -1;
   uint32_t pend_piece = 0;
 
-  // The thread that issues the MMAs and the commits that track them: lane 0
-  // (E4M3), or the lane elect.sync picks, lane 0 of the converged warp
-  // (bf16); measured, each form is the faster one for its kernel.
-  auto issuer = [&]() -> bool {
-    if constexpr (kFp8) return lane == 0;
-    else return elect_one();
-  };
-  auto wait_all = [&](int bar, uint32_t parity) -> bool {
-    const bool r = cx.wait(bar, parity);  // every lane polls the same barrier
-    __syncwarp();
-    return r;
-  };
+  // One thread runs this role (the rest of its warp waits at the CTA's final
+  // barrier): it polls the barriers, zeroes the rows past a partial last V
+  // page, issues every MMA and the commits that track them. A warp whose
+  // lanes diverge around each issue block pays for the reconvergence.
+  auto wait_all = [&](int bar, uint32_t parity) -> bool { return cx.wait(bar, parity); };
   auto do_s = [&](uint32_t qb) -> bool {
     const uint32_t buf = s_cnt & 1, n = s_cnt >> 1;
     if (!wait_all(Bb::SEmpty + buf, (n & 1) ^ 1)) return false;
@@ -601,7 +593,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       // holds K.t1^T in columns 0-63 and K.t2^T in 64-127; K = 32 dims per MMA
       const uint32_t kslot = cc % C::kKStages;
       if (!wait_all(Bb::StFull + kslot, (cc / C::kKStages) & 1)) return false;
-      if (issuer()) {
+      {
         tc_fence_after();
         const uint32_t ka = cx.base + L.stage + kslot * kKTileBytes;
         const uint32_t qa = cx.base + L.q + qb * kQBytes;
@@ -614,7 +606,6 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         tc_commit(cx.bar(Bb::StEmpty + kslot));
         tc_commit(cx.bar(Bb::SFull + buf));
       }
-      __syncwarp();
       ++cc;
       ++s_cnt;
       return true;
@@ -622,7 +613,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       for (int d = 0; d < 4; ++d) {
         const uint32_t slot = cc % C::kSlots, ph = (cc / C::kSlots) & 1;
         if (!wait_all(Bb::Full + slot, ph)) return false;
-        if (issuer()) {
+        {
           tc_fence_after();
           const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
           const uint32_t b0 = cx.base + L.q + qb * kQBytes + d * 8192;
@@ -632,11 +623,9 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
                    idesc_s<kFp8>(), (d | kk) != 0);
           tc_commit(cx.bar(Bb::Empty + slot));
         }
-        __syncwarp();
         ++cc;
       }
-      if (issuer()) tc_commit(cx.bar(Bb::SFull + buf));
-      __syncwarp();
+      tc_commit(cx.bar(Bb::SFull + buf));
       ++s_cnt;
       return true;
     }
@@ -668,15 +657,14 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         if (nv < kPageSize) {
           // rows [nv, 64) of both boxes (whole 128 B rows): code 0x7F is NaN and 0 * NaN would poison P.V
           const int nbytes = (kPageSize - nv) * 128;
-          for (int off = lane * 16; off < nbytes; off += 32 * 16) {
+          for (int off = 0; off < nbytes; off += 16) {
             st_shared_v4(vs[i] + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
             st_shared_v4(vs[i] + 8192 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
           }
           fence_proxy_async_smem();
-          __syncwarp();
         }
       }
-      if (issuer()) {
+      {
         tc_fence_after();
         for (int i = 0; i < np; ++i) {
           const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;  // token rows 64i..
@@ -690,7 +678,6 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
           tc_commit(cx.bar(Bb::StEmpty + C::kKStages + (vc + i) % C::kVStages));
         }
       }
-      __syncwarp();
       vc += np;
     } else {
     for (int i = 0; i < np; ++i) {
@@ -701,16 +688,15 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
         if (!kFp8 && nv < kPageSize) {
           // rows [nv, 64) of both 64-dim blocks (whole 128 B rows, so the
-          // swizzle does not matter): 16 B per lane and step
+          // swizzle does not matter), 16 B per store
           const int nbytes = (kPageSize - nv) * 128;
-          for (int off = lane * 16; off < nbytes; off += 32 * 16) {
+          for (int off = 0; off < nbytes; off += 16) {
             st_shared_v4(a0 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
             st_shared_v4(a0 + 8192 + nv * 128 + off, make_uint4(0u, 0u, 0u, 0u));
           }
           fence_proxy_async_smem();
-          __syncwarp();
         }
-        if (issuer()) {
+        {
           tc_fence_after();
           const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;
 #pragma unroll
@@ -720,15 +706,13 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
                    !(first_of_seg && i == 0 && kk == 0));
           tc_commit(cx.bar(Bb::Empty + slot));
         }
-        __syncwarp();
         ++cc;
       }
     }
     }
-    if (issuer()) {
+    {
       tc_commit(cx.bar(Bb::PEmpty + buf));
     }
-    __syncwarp();
     ++p_cnt;
     return true;
   };
@@ -741,8 +725,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       // S(g), then P.V(g - 1), in the producer's order
       for (int t = 0; alive && t < T; ++t) {
         alive = do_s(qb);
-        if (alive && t == T - 1 && issuer()) tc_commit(cx.bar(Bb::QEmpty + qb));
-        __syncwarp();
+        if (alive && t == T - 1) tc_commit(cx.bar(Bb::QEmpty + qb));
         if (alive && pend_t >= 0) alive = do_pv(pend_s, pend_t, pend_piece);
         pend_s = s;
         pend_t = t;
@@ -750,11 +733,10 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       }
     } else {
       alive = do_s(qb);
-      if (alive && T == 1 && issuer()) tc_commit(cx.bar(Bb::QEmpty + qb));
+      if (alive && T == 1) tc_commit(cx.bar(Bb::QEmpty + qb));
       for (int t = 1; alive && t < T; ++t) {
         alive = do_s(qb);
-        if (alive && t == T - 1 && issuer()) tc_commit(cx.bar(Bb::QEmpty + qb));
-        __syncwarp();
+        if (alive && t == T - 1) tc_commit(cx.bar(Bb::QEmpty + qb));
         if (alive) alive = do_pv(s, t - 1, seg_i);
       }
       if (alive) alive = do_pv(s, T - 1, seg_i);
@@ -763,11 +745,10 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   }
   if (C::kCrossPiece && alive && pend_t >= 0) (void)do_pv(pend_s, pend_t, pend_piece);
   // drain: wait for every MMA this thread issued before TMEM is released
-  if (issuer()) {
+  {
     tc_commit(cx.bar(Bb::Drain));
     (void)mbar_wait(cx.bar(Bb::Drain), 0, cx.budget, nullptr, p.err);
   }
-  __syncwarp();
 }
 
 // ---------------------------------------------------------------- softmax
@@ -1264,7 +1245,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   } else if (warp == C::kProducerWarp) {
     producer_role<kFp8>(p, &kmap, &vmap, &qmap, cx, s_cost, s_len, lo, hi);
   } else if (warp == C::kMmaWarp) {
-    mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
+    if ((threadIdx.x & 31) == 0) mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
     if (warp == C::kVProducerWarp)
       producer_v_role(p, &vmap, cx, s_cost, s_len, lo, hi);

@@ -135,9 +135,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of `bar` with the given parity to complete, for at most
 // `budget_ns`. On expiry (or when another role already gave up, `*abort` != 0)
 // it records MFA_DEVERR_TIMEOUT, raises *abort and returns false; it never traps.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns,
-                                          volatile int* abort, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop is out of line: a wait whose phase has already completed
+// (the common case in a running pipeline) costs one try_wait.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t budget_ns,
+                                                   volatile int* abort, uint32_t* err) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -148,6 +149,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns,
+                                          volatile int* abort, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, budget_ns, abort, err);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -164,14 +170,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
-}
-// One thread of a converged warp (elect.sync): the same lane every time for
-// the same set of active lanes, so MMAs and the commits that track them come
-// from one thread.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile("{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}\n" : "=r"(pred));
-  return pred != 0;
 }
 // Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
