@@ -180,6 +180,31 @@ def mfa_decode(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_scale
     return out, lse
 
 
+def mfa_decode_mtp(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_scale=None,
+                   v_scale=None, threads=None):
+    """Multi-token (MTP) decode: T query tokens per sequence, in fp64.
+
+    "Step-3 is Large yet Affordable" (paper summary page), section 5.2: with
+    multi-token prediction a decode step carries extra predicted tokens, which
+    read the same KV cache. The tokens are the last T positions of sequence b
+    (the cache of seq_lens[b] tokens already holds them), so query token t sits
+    at position L_b - T + t and attends, causally, to positions
+    j < L_b - T + 1 + t. Each (b, t) is therefore the single-token decode of
+    ``mfa_decode`` over the first L_b - T + 1 + t tokens of sequence b (none if
+    that is <= 0: out = 0, lse = -inf).
+
+    q_bits [B, T, H, D] uint16 (bf16 bits); the other arguments as in mfa_decode.
+    Returns (out, lse): out [B, T, H, D] fp64, lse [B, T, H]."""
+    q = _c(q_bits, np.uint16)
+    B, T, H, D = q.shape
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32).astype(np.int64)
+    lens = np.maximum(sl[:, None] - T + 1 + np.arange(T)[None, :], 0).astype(np.int32).reshape(B * T)
+    out, lse = mfa_decode(q.reshape(B * T, H, D), k_cache, v_cache, np.repeat(pt, T, axis=0), lens, scale,
+                          k_scale=k_scale, v_scale=v_scale, threads=threads)
+    return out.reshape(B, T, H, D), lse.reshape(B, T, H)
+
+
 def kv_append(k_new_bits, v_new_bits, k_cache, v_cache, page_table, seq_lens, *, k_scale=None,
               v_scale=None):
     """Append n_new tokens per sequence to host copies of the cache, in place.
