@@ -47,6 +47,8 @@ _SIGNATURES = {
     "mfa_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P], _I),
+    "mfa_decode_mtp_workspace_bytes": ([_I, _I, _I], _Z),
+    "mfa_decode_attention_mtp": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_check_device_errors": ([_P, _I, _P], _I),
     "mfa_set_wait_budget_ns": ([_U64], None),
     "mfa_selftest_wait_timeout": ([_P, _U64, _P], _I),
@@ -142,6 +144,22 @@ def mfa_decode_attention(q, k_cache, v_cache, page_table, seq_lens, out, lse, sc
                                        _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch,
                                        max_pages, num_pages, max_len_hint, _ptr(workspace),
                                        workspace_bytes, _stream(stream)))
+
+
+def mfa_decode_mtp_workspace_bytes(batch: int, n_query: int, max_len_hint: int) -> int:
+    n = load().mfa_decode_mtp_workspace_bytes(batch, n_query, max_len_hint)
+    if n == 0:
+        raise MFAError(1, "bad arguments for mfa_decode_mtp_workspace_bytes")
+    return n
+
+
+def mfa_decode_attention_mtp(q, k_cache, v_cache, page_table, seq_lens, out, lse, scale, batch, n_query,
+                             max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream=None):
+    """Multi-token decode: q and out [batch, n_query, 64, 256] bf16, lse [batch, n_query, 64] fp32."""
+    _check(load().mfa_decode_attention_mtp(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                           _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch, n_query,
+                                           max_pages, num_pages, max_len_hint, _ptr(workspace),
+                                           workspace_bytes, _stream(stream)))
 
 
 def mfa_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse, scale,

@@ -137,6 +137,7 @@ extern "C" mfa_status_t mfa_decode_attention_noalloc(const void* q, const void* 
   p.num_pages = num_pages;
   p.grid = plan.grid_ctas;
   p.piece_cost = kPieceCostPages;
+  p.n_query = 1;
   p.wait_budget_ns = current_wait_budget_ns();
   CUtensorMap kmap, vmap, qmap;
   if ((st = encode_map(&kmap, k_cache, (uint64_t)num_pages * kPageSize)) != MFA_OK ||

@@ -50,10 +50,11 @@
 namespace mfa {
 namespace {
 
-template <bool kFp8>
+// kMtp: two query tokens per sequence share each pass over the cache (bf16).
+template <bool kFp8, bool kMtp = false>
 struct Cfg;
 template <>
-struct Cfg<false> {
+struct Cfg<false, false> {
   static constexpr int kThreads = 320;   // two softmax warpgroups, producer, MMA
   static constexpr int kSlots = 7;       // 16 KB operand chunks
   static constexpr int kKStages = 0;     // raw code pages: K ring
@@ -68,12 +69,39 @@ struct Cfg<false> {
   static constexpr int kGroups = 2;      // softmax warpgroups (each owns 64 / kGroups heads)
   static constexpr int kSoftmaxThreads = 128 * kGroups;
   static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
+  static constexpr int kQ = 1;           // query tokens per sequence
+  static constexpr int kCols = 64;       // softmax columns: [token][head]
+  static constexpr int kHpt = 32;        // columns per softmax thread
+  static constexpr int kOHalfCols = 64;  // O^T columns per 128-dim half
+};
+// Two query tokens per sequence (MTP): S^T and P are [token][head] = 128
+// columns, warpgroup g owns query token g; one O^T of 2 x 128 columns.
+template <>
+struct Cfg<false, true> {
+  static constexpr int kThreads = 320;
+  static constexpr int kSlots = 5;       // 16 KB operand chunks (Q and P are twice as large)
+  static constexpr int kKStages = 0;
+  static constexpr int kVStages = 0;
+  static constexpr int kStages = 0;
+  static constexpr int kQBufs = 1;
+  static constexpr bool kCrossPiece = true;
+  static constexpr int kScaleSlots = 0;
+  static constexpr int kAbFormat = 1;
+  static constexpr int kSCols = 128;
+  static constexpr int kOBufs = 1;
+  static constexpr int kGroups = 2;
+  static constexpr int kSoftmaxThreads = 128 * kGroups;
+  static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
+  static constexpr int kQ = 2;
+  static constexpr int kCols = 128;
+  static constexpr int kHpt = 64;
+  static constexpr int kOHalfCols = 128;
 };
 // E4M3: the producer stages the K tiles and scales, a second producer warp
 // the V pages, and one warp finds each piece's largest V scale; both products
 // run as 8-bit MMAs on the raw staged pages, so no code is converted on chip.
 template <>
-struct Cfg<true> {
+struct Cfg<true, false> {
   static constexpr int kThreads = 384;    // two softmax warpgroups, then 4 single-warp roles
   static constexpr int kSlots = 0;        // K and V are read raw by 8-bit MMAs: no operand ring
   static constexpr int kKStages = 2;      // raw K tiles (both pages of a tile, 32 KB): A of S^T
@@ -88,18 +116,22 @@ struct Cfg<true> {
   static constexpr int kSoftmaxThreads = 128 * kGroups;
   static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
   static constexpr int kVProducerWarp = kProducerWarp + 2, kVRefWarp = kProducerWarp + 3;
+  static constexpr int kQ = 1;
+  static constexpr int kCols = 64;        // per-head statistics (the two terms are summed)
+  static constexpr int kHpt = 32;
+  static constexpr int kOHalfCols = 128;  // [term][head]
 };
 
 constexpr int kSlotBytes = 16384;
 constexpr int kStageBytes = 16384;        // one E4M3 V page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
 constexpr int kKTileBytes = 32768;        // one E4M3 K tile: box h (dims [128h, 128h+128)) of 128 rows at 16 KB * h
 constexpr int kQTermBytes = 8192;         // one term of one 128-dim box: [64 heads x 128 B], 128-byte swizzle
-constexpr int kQBytes = 32768;            // Q: 4 dim blocks of [64 heads x 128 B]
-constexpr int kPBytes = 16384;            // P^T: [128 tokens x 64 heads], 16-bit
+constexpr int kQBytes = 32768;            // Q of one token: 4 dim blocks of [64 heads x 128 B]
+constexpr int kPBytes = 16384;            // P^T of one token: [128 tokens x 64 heads], 16-bit
 constexpr int kScaleBytes = 1024;         // per tile: 128 K scales, then 128 V scales
 constexpr int kTmemCols = 512;            // S^T x2 + O^T (bf16: 2 x 64 + 2 x 128; E4M3: 2 x 128 + 256)
-template <bool kFp8>
-__host__ __device__ constexpr int tmem_o() { return 2 * Cfg<kFp8>::kSCols; }  // first O^T column; bf16 buffer o at +128 * o
+template <bool kFp8, bool kMtp = false>
+__host__ __device__ constexpr int tmem_o() { return 2 * Cfg<kFp8, kMtp>::kSCols; }  // first O^T column; bf16 buffer o at +128 * o
 constexpr int kMaxBars = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -112,9 +144,9 @@ __host__ __device__ constexpr float rescale_threshold() { return kFp8 ? 3.0f : 8
 // stored side by side per token: [x1 of heads 0-63 | x2 of heads 0-63].
 constexpr float kPScale = 32.0f;
 
-template <bool kFp8>
+template <bool kFp8, bool kMtp = false>
 struct Bars {  // indices into the barrier array
-  using C = Cfg<kFp8>;
+  using C = Cfg<kFp8, kMtp>;
   static constexpr int Full = 0;                     // [kSlots] operand chunk ready
   static constexpr int Empty = Full + C::kSlots;     // [kSlots] operand chunk consumed
   static constexpr int QFull = Empty + C::kSlots;    // [2] Q landed
@@ -136,13 +168,13 @@ struct Bars {  // indices into the barrier array
   static_assert(Count <= kMaxBars, "barrier array too small");
 };
 
-template <bool kFp8>
-__host__ __device__ constexpr uint32_t idesc_s() {  // A = K tile (K-major), B = Q (K-major)
-  return idesc_f16(128, 64, Cfg<kFp8>::kAbFormat, 0, 0);
+template <bool kFp8, bool kMtp>
+__host__ __device__ constexpr uint32_t idesc_s() {  // A = K tile (K-major), B = Q (K-major), N = [token][head]
+  return idesc_f16(128, Cfg<kFp8, kMtp>::kSCols, Cfg<kFp8, kMtp>::kAbFormat, 0, 0);
 }
-template <bool kFp8>
-__host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = P^T (head-major)
-  return idesc_f16(128, 64, Cfg<kFp8>::kAbFormat, 1, 1);
+template <bool kFp8, bool kMtp>
+__host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = P^T (head-major), N = [token][head]
+  return idesc_f16(128, 64 * Cfg<kFp8, kMtp>::kQ, Cfg<kFp8, kMtp>::kAbFormat, 1, 1);
 }
 // kind::f8f6f4, A and B E4M3 (format 0), both K-major, fp32 accumulate, M=128 N=128
 __host__ __device__ constexpr uint32_t idesc_s_e4m3() { return (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24); }
@@ -157,20 +189,20 @@ struct SmemLayout {
   uint32_t total;
 };
 
-template <bool kFp8>
+template <bool kFp8, bool kMtp = false>
 __host__ __device__ constexpr SmemLayout smem_layout(int B) {
-  using C = Cfg<kFp8>;
+  using C = Cfg<kFp8, kMtp>;
   SmemLayout L{};
   L.ring = 0;
   L.stage = L.ring + C::kSlots * kSlotBytes;  // E4M3: K tiles, then V pages
   L.q = L.stage + C::kKStages * kKTileBytes + C::kVStages * kStageBytes;
-  L.p = L.q + C::kQBufs * kQBytes;  // E4M3: the Q terms overwrite the bf16 Q (same 32 KB)
-  L.scales = L.p + 2 * kPBytes;
+  L.p = L.q + C::kQBufs * C::kQ * kQBytes;  // E4M3: the Q terms overwrite the bf16 Q (same 32 KB)
+  L.scales = L.p + 2 * C::kQ * kPBytes;
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
-  // float red[4][64], mref[64], alpha[64], inv_l[2][64], qinv[64], vref[2]
+  // float red[4][kCols], mref[kCols], alpha[kCols], inv_l[2][kCols], scratch[kCols], vref[2]
   L.red = (L.prefix + 4 * (B + 1) + 15) & ~15u;
-  L.bars = (L.red + 9 * 64 * 4 + 8 + 7) & ~7u;    // mbarriers
+  L.bars = (L.red + 9 * C::kCols * 4 + 8 + 7) & ~7u;    // mbarriers
   L.misc = L.bars + 8 * kMaxBars;                 // tmem base, abort flag
   L.total = L.misc + 16;
   return L;
@@ -178,6 +210,7 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
 constexpr uint32_t kMaxDynamicSmem = 227u * 1024u;  // per-block opt-in limit of sm_103a
 static_assert(smem_layout<false>(kMaxBatch).total + 1024 <= kMaxDynamicSmem, "bf16 layout exceeds shared memory");
 static_assert(smem_layout<true>(kMaxBatch).total + 1024 <= kMaxDynamicSmem, "E4M3 layout exceeds shared memory");
+static_assert(smem_layout<false, true>(kMaxBatch).total + 1024 <= kMaxDynamicSmem, "MTP layout exceeds shared memory");
 
 struct Ctx {
   uint32_t base;      // shared address of the aligned dynamic smem base
@@ -285,16 +318,16 @@ struct PageIds {
 // tile t >= 1 those of K(t) and V(t-1), then V(T-1) -- the order in which the
 // MMA warp consumes them (bf16). E4M3: Q, then per tile the raw K tile and
 // its scale block (the V pages come from warp 6).
-template <bool kFp8>
+template <bool kFp8, bool kMtp>
 __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               const CUtensorMap* qmap, const Ctx& cx, const int* s_cost, const int* s_len,
                               long long lo, long long hi) {
-  using C = Cfg<kFp8>;
-  using Bb = Bars<kFp8>;
+  using C = Cfg<kFp8, kMtp>;
+  using Bb = Bars<kFp8, kMtp>;
   const int lane = threadIdx.x & 31;
   const uint64_t pol_stream = policy_evict_first();
   const uint64_t pol_keep = policy_evict_last();
-  const SmemLayout L = smem_layout<kFp8>(p.B);
+  const SmemLayout L = smem_layout<kFp8, kMtp>(p.B);
   uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged K tiles (E4M3); pieces; tiles
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
@@ -392,10 +425,14 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     __syncwarp();
     if (!qfree) break;
     if (lane == 0) {
-      const uint32_t q_dst = cx.base + L.q + qb * kQBytes;
-      mbar_arrive_expect_tx(cx.bar(Bb::QFull + qb), (uint32_t)kQBytes);
+      // dim block d of token t at (d * kQ + t) * 8 KB: per block, the tokens'
+      // 64-head rows stack into one 64 * kQ-row K-major operand
+      const uint32_t q_dst = cx.base + L.q + qb * C::kQ * kQBytes;
+      mbar_arrive_expect_tx(cx.bar(Bb::QFull + qb), (uint32_t)(C::kQ * kQBytes));
       for (int d = 0; d < 4; ++d)
-        tma_load_2d(q_dst + d * 8192, qmap, d * 64, s.b * kHeads, cx.bar(Bb::QFull + qb), pol_keep);
+        for (int t = 0; t < C::kQ; ++t)
+          tma_load_2d(q_dst + (d * C::kQ + t) * 8192, qmap, d * 64, (s.b * C::kQ + t) * kHeads,
+                      cx.bar(Bb::QFull + qb), pol_keep);
     }
     issued_q = true;
     last_q_parity = qn & 1;
@@ -563,12 +600,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 v) {
 }
 
 // ---------------------------------------------------------------- MMA issue
-template <bool kFp8>
+template <bool kFp8, bool kMtp>
 __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len, long long lo,
                          long long hi, uint32_t tmem) {
-  using C = Cfg<kFp8>;
-  using Bb = Bars<kFp8>;
-  const SmemLayout L = smem_layout<kFp8>(p.B);
+  using C = Cfg<kFp8, kMtp>;
+  using Bb = Bars<kFp8, kMtp>;
+  const SmemLayout L = smem_layout<kFp8, kMtp>(p.B);
   uint32_t cc = 0, seg_i = 0, s_cnt = 0, p_cnt = 0;
   uint32_t vc = 0;  // E4M3: V pages consumed from the V stage ring
   Seg s;
@@ -596,7 +633,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       {
         tc_fence_after();
         const uint32_t ka = cx.base + L.stage + kslot * kKTileBytes;
-        const uint32_t qa = cx.base + L.q + qb * kQBytes;
+        const uint32_t qa = cx.base + L.q + qb * C::kQ * kQBytes;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -616,11 +653,11 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         {
           tc_fence_after();
           const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
-          const uint32_t b0 = cx.base + L.q + qb * kQBytes + d * 8192;
+          const uint32_t b0 = cx.base + L.q + qb * C::kQ * kQBytes + d * C::kQ * 8192;  // 64 kQ rows
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc_mma(d_tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024),
-                   idesc_s<kFp8>(), (d | kk) != 0);
+                   idesc_s<kFp8, kMtp>(), (d | kk) != 0);
           tc_commit(cx.bar(Bb::Empty + slot));
         }
         ++cc;
@@ -667,12 +704,12 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
       {
         tc_fence_after();
         for (int i = 0; i < np; ++i) {
-          const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;  // token rows 64i..
+          const uint32_t bp = cx.base + L.p + buf * C::kQ * kPBytes + i * 8192;  // token rows 64i..
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks)
-              tc_mma_f8(tmem + tmem_o<kFp8>() + hf * 128, smem_desc(vs[i] + hf * 8192 + ks * 4096, 16, 1024, 2),
+              tc_mma_f8(tmem + tmem_o<kFp8, kMtp>() + hf * 128, smem_desc(vs[i] + hf * 8192 + ks * 4096, 16, 1024, 2),
                         smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3(), !(first_of_seg && i == 0 && ks == 0));
           // the V page's stage is free once these MMAs are done
           tc_commit(cx.bar(Bb::StEmpty + C::kKStages + (vc + i) % C::kVStages));
@@ -698,11 +735,13 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         }
         {
           tc_fence_after();
-          const uint32_t bp = cx.base + L.p + buf * kPBytes + i * 8192;
+          // token rows 64i.. of the P buffer; query token t's [tokens x 64 heads] block at t * kPBytes
+          const uint32_t bp = cx.base + L.p + buf * C::kQ * kPBytes + i * 8192;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma(tmem + tmem_o<kFp8>() + obuf * 128 + hf * 64, smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
-                   smem_desc_sw128(bp + kk * 2048, 8192, 1024), idesc_o<kFp8>(),
+            tc_mma(tmem + tmem_o<kFp8, kMtp>() + obuf * 128 + hf * C::kOHalfCols,
+                   smem_desc_sw128(a0 + kk * 2048, 8192, 1024), smem_desc_sw128(bp + kk * 2048, kPBytes, 1024),
+                   idesc_o<kFp8, kMtp>(),
                    !(first_of_seg && i == 0 && kk == 0));
           tc_commit(cx.bar(Bb::Empty + slot));
         }
@@ -900,9 +939,8 @@ __device__ __forceinline__ float split_q_e4m3(uint32_t q_addr, float* scratch, i
 
 // The group's O^T columns (this thread's TMEM lane, both 128-dim halves)
 // times col_scale[head - h0]; E4M3: both terms' columns of each head.
-template <bool kFp8, int kHpt>
+template <bool kFp8, int kHpt, int kHalfCols>
 __device__ __forceinline__ void scale_o_columns(uint32_t taddr_o, int h0, const float* col_scale) {
-  constexpr int kHalfCols = kFp8 ? 128 : 64;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -933,25 +971,26 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kMtp>
 __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len,
                              long long lo, long long hi, uint32_t tmem, int c, uint8_t* gbase) {
-  using C = Cfg<kFp8>;
-  using Bb = Bars<kFp8>;
-  constexpr int kHpt = 64 / C::kGroups;  // heads per thread
-  const int g = threadIdx.x >> 7;        // head group
+  using C = Cfg<kFp8, kMtp>;
+  using Bb = Bars<kFp8, kMtp>;
+  constexpr int kHpt = C::kHpt;          // columns per thread
+  constexpr int kCols = C::kCols;        // [query token][head] columns of the statistics
+  const int g = threadIdx.x >> 7;        // head group (with two query tokens: the query token)
   const int row = threadIdx.x & 127;     // TMEM lane = token of the tile = dim of each O^T half
   const int quad = row >> 5, lane = row & 31;
   const int h0 = g * kHpt;
-  const SmemLayout L = smem_layout<kFp8>(p.B);
-  float* red = reinterpret_cast<float*>(gbase + L.red);  // [4][64] per-warp partial reductions
-  float* mref = red + 4 * 64;                            // [64] reference maxima (log2 units), uniform
-  float* alpha = mref + 64;                              // [64] rescale factors, uniform
-  float* inv_l = alpha + 64;                             // [2][64] 1/l of the piece in O^T buffer i
-  float* qscratch = inv_l + 128;                         // [8] E4M3: per-warp max |Q|
-  float* s_vref = qscratch + 64;                         // [2] E4M3: largest V scale of a piece
+  const SmemLayout L = smem_layout<kFp8, kMtp>(p.B);
+  float* red = reinterpret_cast<float*>(gbase + L.red);  // [4][kCols] per-warp partial reductions
+  float* mref = red + 4 * kCols;                         // [kCols] reference maxima (log2 units), uniform
+  float* alpha = mref + kCols;                           // [kCols] rescale factors, uniform
+  float* inv_l = alpha + kCols;                          // [2][kCols] 1/l of the piece in O^T buffer i
+  float* qscratch = inv_l + 2 * kCols;                   // [8] E4M3: per-warp max |Q|
+  float* s_vref = qscratch + kCols;                      // [2] E4M3: largest V scale of a piece
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-  const uint32_t taddr_o0 = tmem + lane_base + tmem_o<kFp8>();
+  const uint32_t taddr_o0 = tmem + lane_base + tmem_o<kFp8, kMtp>();
   const float c2 = p.scale * kLog2e;
   uint32_t s_cnt = 0, p_cnt = 0;
   // P.V(g) completes phase g/2 of p_empty[g % 2]. Before P(g) is written the
@@ -972,9 +1011,9 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     if (!wait_pv(pend_pv)) return false;
     tc_fence_after();
     const uint32_t ta = taddr_o0 + pend_obuf * 128;
-    const float* il = inv_l + pend_obuf * 64 + h0;
-    float* dst = p.part_o + (pend_slot * kHeads + h0) * kHeadDim;
-    constexpr int kHalfCols = kFp8 ? 128 : 64;
+    const float* il = inv_l + pend_obuf * kCols + h0;
+    float* dst = p.part_o + (pend_slot * (C::kQ * kHeads) + h0) * kHeadDim;  // slot: [query token][head][dim]
+    constexpr int kHalfCols = C::kOHalfCols;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -1030,7 +1069,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     const int T = tiles_of(s);
     for (int t = 0; t < T; ++t) {
       const int tok0 = (s.pg0 + 2 * t) * kPageSize;
-      const int rows = min(pages_in_tile(s, t) * kPageSize, s.len - tok0);  // valid rows of the tile
+      // valid rows of the tile; query token g of kQ sees the first len - (kQ - 1 - g) positions
+      const int rows = max(0, min(pages_in_tile(s, t) * kPageSize, s.len - (kMtp ? C::kQ - 1 - g : 0) - tok0));
       const bool full = rows == 128, valid = row < rows;
       // E4M3: this token's K and V scales (the tile's scale block, slot = tile count)
       float kmul = c2, vmul = 1.0f;
@@ -1056,12 +1096,13 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
         (void)load_logits<kFp8, kHpt>(taddr_s, full, valid, kmul, nullptr, x);
         warp_reduce_scatter<kHpt, true>(x, lane);  // x is reloaded below
 #pragma unroll
-        for (int i = 0; i < kHpt / 32; ++i) red[quad * 64 + h0 + (kHpt / 32) * lane + i] = x[i];
+        for (int i = 0; i < kHpt / 32; ++i) red[quad * kCols + h0 + (kHpt / 32) * lane + i] = x[i];
         barrier_group(g);
         if (row < kHpt) {
           const int h = h0 + row;
           const float m_old = mref[h];
-          const float m_new = fmaxf(m_old, fmaxf(fmaxf(red[h], red[64 + h]), fmaxf(red[128 + h], red[192 + h])));
+          const float m_new =
+              fmaxf(m_old, fmaxf(fmaxf(red[h], red[kCols + h]), fmaxf(red[2 * kCols + h], red[3 * kCols + h])));
           alpha[h] = ex2_approx(m_old - m_new);  // 0 while m_old = -inf
           mref[h] = m_new;
         }
@@ -1078,7 +1119,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
           // O^T holds the previous tiles: wait for their last P.V, then scale the group's columns
           if (!wait_pv(p_cnt - 1)) return;
           tc_fence_after();
-          scale_o_columns<kFp8, kHpt>(taddr_o, h0, alpha + h0);
+          scale_o_columns<kFp8, kHpt, C::kOHalfCols>(taddr_o, h0, alpha + h0);
         }
         (void)load_logits<kFp8, kHpt>(taddr_s, full, valid, kmul, mref + h0, x);
       }
@@ -1092,11 +1133,12 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       // chunk j = x1 and chunk 4 + j = x2 of heads [16j, 16j + 16).
       const uint32_t pbuf = p_cnt & 1;
       if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
-      const uint32_t prow = cx.base + L.p + pbuf * kPBytes + row * 128;
+      // with two query tokens, token g's [tokens x 64 heads] block sits at g * kPBytes
+      const uint32_t prow = cx.base + L.p + pbuf * C::kQ * kPBytes + (kMtp ? g * kPBytes : 0) + row * 128;
       constexpr int kHeadsPerChunk = kFp8 ? 16 : 8;
 #pragma unroll
       for (int j = 0; j < kHpt / kHeadsPerChunk; ++j) {
-        const int jj = h0 / kHeadsPerChunk + j;  // chunk index within the row
+        const int jj = (kMtp ? 0 : h0 / kHeadsPerChunk) + j;  // chunk index within the row
         uint32_t w1[4], w2[4];
 #pragma unroll
         for (int k = 0; k < kHeadsPerChunk / 2; ++k) {
@@ -1141,14 +1183,14 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     warp_reduce_scatter<kHpt, false>(lp, lane);
     barrier_group(g);  // earlier readers of red/alpha are done
 #pragma unroll
-    for (int i = 0; i < kHpt / 32; ++i) red[quad * 64 + h0 + (kHpt / 32) * lane + i] = lp[i];
+    for (int i = 0; i < kHpt / 32; ++i) red[quad * kCols + h0 + (kHpt / 32) * lane + i] = lp[i];
     barrier_group(g);
     const size_t slot = (size_t)c + s.b;
     if (row < kHpt) {
       const int h = h0 + row;
-      const float l = red[h] + red[64 + h] + red[128 + h] + red[192 + h];
-      inv_l[obuf * 64 + h] = 1.0f / (l * pscale);
-      p.part_lse[slot * kHeads + h] = (mref[h] + log2f(l)) * kLn2;
+      const float l = red[h] + red[kCols + h] + red[2 * kCols + h] + red[3 * kCols + h];
+      inv_l[obuf * kCols + h] = 1.0f / (l * pscale);
+      p.part_lse[slot * (C::kQ * kHeads) + h] = (mref[h] + log2f(l)) * kLn2;
     }
     barrier_group(g);
     pend = true;
@@ -1160,17 +1202,17 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   if (pend) (void)write_o();
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
+template <bool kFp8, bool kMtp>
+__global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads, 1)
     decode_split_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap) {
-  using C = Cfg<kFp8>;
-  using Bb = Bars<kFp8>;
+  using C = Cfg<kFp8, kMtp>;
+  using Bb = Bars<kFp8, kMtp>;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   const uint32_t raw = smem_u32(dyn_smem);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = dyn_smem + (base - raw);
-  const SmemLayout L = smem_layout<kFp8>(p.B);
+  const SmemLayout L = smem_layout<kFp8, kMtp>(p.B);
   int* s_len = reinterpret_cast<int*>(gbase + L.len);
   int* s_cost = reinterpret_cast<int*>(gbase + L.prefix);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.misc);
@@ -1241,16 +1283,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   Ctx cx{base, bars, abort_flag, p.err, p.wait_budget_ns};
 
   if (warp < 4 * C::kGroups) {
-    softmax_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
+    softmax_role<kFp8, kMtp>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
   } else if (warp == C::kProducerWarp) {
-    producer_role<kFp8>(p, &kmap, &vmap, &qmap, cx, s_cost, s_len, lo, hi);
+    producer_role<kFp8, kMtp>(p, &kmap, &vmap, &qmap, cx, s_cost, s_len, lo, hi);
   } else if (warp == C::kMmaWarp) {
-    if ((threadIdx.x & 31) == 0) mma_role<kFp8>(p, cx, s_cost, s_len, lo, hi, tmem);
+    if ((threadIdx.x & 31) == 0) mma_role<kFp8, kMtp>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
     if (warp == C::kVProducerWarp)
       producer_v_role(p, &vmap, cx, s_cost, s_len, lo, hi);
     else if (warp == C::kVRefWarp)
-      vref_role(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 9 * 64);
+      vref_role(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 9 * C::kCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -1259,18 +1301,19 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kMtp>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, cudaStream_t stream) {
-  const size_t smem = (size_t)smem_layout<kFp8>(p.B).total + 1024;
+  const size_t smem = (size_t)smem_layout<kFp8, kMtp>(p.B).total + 1024;
   static int configured_bytes = 0;  // largest opt-in set so far (per process; one device family)
   if ((int)smem > configured_bytes) {
     const cudaError_t e =
-        cudaFuncSetAttribute(decode_split_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(decode_split_tc_kernel<kFp8, kMtp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
     configured_bytes = (int)smem;
   }
-  return launch_pdl(decode_split_tc_kernel<kFp8>, dim3(p.grid), dim3(Cfg<kFp8>::kThreads), smem, stream, p, kmap,
+  return launch_pdl(decode_split_tc_kernel<kFp8, kMtp>, dim3(p.grid), dim3(Cfg<kFp8, kMtp>::kThreads), smem, stream, p, kmap,
                     vmap, qmap);
 }
 
@@ -1278,15 +1321,21 @@ cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUte
 
 size_t decode_split_tc_smem_bytes(int B) { return (size_t)smem_layout<false>(B).total + 1024; }
 size_t decode_split_tc_fp8_smem_bytes(int B) { return (size_t)smem_layout<true>(B).total + 1024; }
+size_t decode_split_tc_mtp_smem_bytes(int B) { return (size_t)smem_layout<false, true>(B).total + 1024; }
 
 cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                    const CUtensorMap& qmap, cudaStream_t stream) {
-  return launch_tc<false>(p, kmap, vmap, qmap, stream);
+  return launch_tc<false, false>(p, kmap, vmap, qmap, stream);
 }
 
 cudaError_t launch_decode_split_tc_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                        const CUtensorMap& qmap, cudaStream_t stream) {
-  return launch_tc<true>(p, kmap, vmap, qmap, stream);
+  return launch_tc<true, false>(p, kmap, vmap, qmap, stream);
+}
+
+cudaError_t launch_decode_split_tc_mtp(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                       const CUtensorMap& qmap, cudaStream_t stream) {
+  return launch_tc<false, true>(p, kmap, vmap, qmap, stream);
 }
 
 }  // namespace mfa

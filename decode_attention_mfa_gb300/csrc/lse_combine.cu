@@ -7,7 +7,11 @@
 // which equals attention over the whole sequence (the splits partition the
 // softmax sum exactly).
 //
-// One CTA of 256 threads per (sequence, group of kH heads); kH is chosen from
+// With several query tokens per sequence (multi-token decode) every token t
+// is merged on its own: its partials are [slot][token][head][dim], and token
+// t of a sequence of length L sees the first L - (n_query - 1 - t) positions.
+//
+// One CTA of 256 threads per (sequence, token, group of kH heads); kH is chosen from
 // the batch so that small batches still spread over the SMs. Per head,
 // 256 / kH threads split the 256 output dimensions (4 or 8 each) and, when
 // there are more than 64 of them, also the partials (S interleaved subsets,
@@ -57,7 +61,8 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
   __shared__ float4 s_acc[Sh::kSubsets > 1 ? kCombineThreads * Sh::kVec : 1];
   // seq_lens is final before the split kernel starts; the partials are not
   build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, p.piece_cost, s_len, s_cost);
-  const int b = blockIdx.y;
+  const int nq = p.n_query;
+  const int b = blockIdx.y / nq, tq = blockIdx.y % nq;  // sequence, query token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hl = threadIdx.x / Sh::kThreadsPerHead;
   const int r = threadIdx.x % Sh::kThreadsPerHead;
@@ -66,12 +71,12 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
   const int G = p.grid;
   const long long C = s_cost[p.B];
   const int np = pages_of_len(s_len[b]);
-  uint16_t* out = p.out + ((size_t)b * kHeads + h) * kHeadDim;
-  if (np == 0) {  // empty sequence
+  uint16_t* out = p.out + ((size_t)blockIdx.y * kHeads + h) * kHeadDim;
+  if (np == 0 || s_len[b] - (nq - 1 - tq) <= 0) {  // empty sequence, or a token that sees no position
     if (sub == 0) {
 #pragma unroll
       for (int v = 0; v < Sh::kVec; ++v) reinterpret_cast<uint2*>(out)[dt * Sh::kVec + v] = make_uint2(0u, 0u);
-      if (dt == 0) p.lse[(size_t)b * kHeads + h] = -INFINITY;
+      if (dt == 0) p.lse[(size_t)blockIdx.y * kHeads + h] = -INFINITY;
     }
     return;
   }
@@ -80,8 +85,8 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
   const long long first = (long long)s_cost[b] + p.piece_cost;
   const int c_first = cta_of_cost(first, C, G);
   const int n = cta_of_cost(first + np - 1, C, G) - c_first + 1;
-  constexpr size_t kSlotStride = (size_t)kHeads * kHeadDim;  // floats from one slot to the next
-  const float* src = p.part_o + ((size_t)(c_first + b) * kHeads + h) * kHeadDim + 4 * Sh::kVec * dt;
+  const size_t kSlotStride = (size_t)nq * kHeads * kHeadDim;  // floats from one slot to the next
+  const float* src = p.part_o + (((size_t)(c_first + b) * nq + tq) * kHeads + h) * kHeadDim + 4 * Sh::kVec * dt;
 
   pdl_wait_prior_grid();
   // first round of O loads (partials sub, sub + S, ...), before the weights
@@ -100,7 +105,8 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
     float mx = -INFINITY;
     for (int i = lane; i < n; i += 32) {
       const int c = c_first + i;
-      const float v = cta_range_nonempty(c, C, G) ? __ldcg(p.part_lse + (size_t)(c + b) * kHeads + hh) : -INFINITY;
+      const float v =
+          cta_range_nonempty(c, C, G) ? __ldcg(p.part_lse + ((size_t)(c + b) * nq + tq) * kHeads + hh) : -INFINITY;
       w[i] = v;
       mx = fmaxf(mx, v);
     }
@@ -173,13 +179,13 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
     for (int v = 0; v < Sh::kVec; ++v)
       reinterpret_cast<uint2*>(out)[dt * Sh::kVec + v] =
           make_uint2(pack_bf16x2(acc[v].x, acc[v].y), pack_bf16x2(acc[v].z, acc[v].w));
-    if (dt == 0) p.lse[(size_t)b * kHeads + h] = s_lse[hl];
+    if (dt == 0) p.lse[(size_t)blockIdx.y * kHeads + h] = s_lse[hl];
   }
 }
 
 template <int kH>
 cudaError_t launch_kh(const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid(kHeads / kH, p.B);
+  dim3 grid(kHeads / kH, p.B * p.n_query);
   const size_t smem = sizeof(int) * (2 * (size_t)p.B + 1) + sizeof(float) * (size_t)kH * p.grid;
   return launch_pdl(lse_combine_kernel<kH>, grid, dim3(kCombineThreads), smem, stream, p);
 }

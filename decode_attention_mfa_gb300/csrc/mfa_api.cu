@@ -78,10 +78,12 @@ int plan_grid(int batch, int max_len_hint, int num_sms) {
   return (int)g;
 }
 
-void fill_plan(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan) {
+// A partial slot holds the results of every query token of its sequence piece.
+void fill_plan(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan, int n_query = 1) {
   plan->grid_ctas = plan_grid(batch, max_len_hint, num_sms);
   plan->partial_slots = plan->grid_ctas + batch - 1;
-  plan->workspace_bytes = kWsHeaderBytes + (size_t)plan->partial_slots * (kPartialOBytes + kPartialLseBytes);
+  plan->workspace_bytes =
+      kWsHeaderBytes + (size_t)plan->partial_slots * n_query * (kPartialOBytes + kPartialLseBytes);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -146,7 +148,7 @@ mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v
                                const int32_t* page_table, const int32_t* seq_lens, const void* out,
                                const float* lse, int batch, int max_pages, int num_pages,
                                int max_len_hint, const void* workspace, size_t workspace_bytes,
-                               int num_sms, mfa_plan_t* plan) {
+                               int num_sms, mfa_plan_t* plan, int n_query = 1) {
   if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out || !lse)
     return fail(MFA_ERR_INVALID_ARG, "null pointer argument");
   if (batch < 1 || batch > kMaxBatch) return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxBatch);
@@ -158,7 +160,7 @@ mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v
     return fail(MFA_ERR_INVALID_ARG, "misaligned pointer (q, caches, out need 16 bytes)");
   if (!workspace || !aligned(workspace, 256))
     return fail(MFA_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
-  fill_plan(batch, max_len_hint, num_sms, plan);
+  fill_plan(batch, max_len_hint, num_sms, plan, n_query);
   if (workspace_bytes < plan->workspace_bytes)
     return fail(MFA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, plan->workspace_bytes);
   return MFA_OK;
@@ -167,7 +169,7 @@ mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v
 DecodeParams make_decode_params(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                                 const float* v_scale, const int32_t* page_table, const int32_t* seq_lens,
                                 void* out, float* lse, float scale, int batch, int max_pages, int num_pages,
-                                void* workspace, const mfa_plan_t& plan) {
+                                void* workspace, const mfa_plan_t& plan, int n_query = 1) {
   DecodeParams p{};
   char* ws = static_cast<char*>(workspace);
   p.q = static_cast<const uint16_t*>(q);
@@ -181,13 +183,15 @@ DecodeParams make_decode_params(const void* q, const void* k_cache, const void* 
   p.lse = lse;
   p.err = reinterpret_cast<uint32_t*>(ws);
   p.part_o = reinterpret_cast<float*>(ws + kWsHeaderBytes);
-  p.part_lse = reinterpret_cast<float*>(ws + kWsHeaderBytes + (size_t)plan.partial_slots * kPartialOBytes);
+  p.part_lse =
+      reinterpret_cast<float*>(ws + kWsHeaderBytes + (size_t)plan.partial_slots * n_query * kPartialOBytes);
   p.scale = scale;
   p.B = batch;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.grid = plan.grid_ctas;
   p.piece_cost = kPieceCostPages;
+  p.n_query = n_query;
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   return p;
 }
@@ -235,7 +239,8 @@ mfa_status_t append_common(const void* k_new, const void* v_new, int n_new, void
 mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                            const float* v_scale, bool fp8, const int32_t* page_table, const int32_t* seq_lens,
                            void* out, float* lse, float scale, int batch, int max_pages, int num_pages,
-                           int max_len_hint, void* workspace, size_t workspace_bytes, void* stream) {
+                           int max_len_hint, void* workspace, size_t workspace_bytes, void* stream,
+                           int n_query = 1) {
   DeviceInfo info;
   mfa_status_t st = current_device(nullptr, &info);
   if (st != MFA_OK) return st;
@@ -244,10 +249,10 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
     return fail(MFA_ERR_INVALID_ARG, "misaligned scales (16 bytes needed)");
   mfa_plan_t plan;
   st = check_decode_args(q, k_cache, v_cache, page_table, seq_lens, out, lse, batch, max_pages, num_pages,
-                         max_len_hint, workspace, workspace_bytes, info.num_sms, &plan);
+                         max_len_hint, workspace, workspace_bytes, info.num_sms, &plan, n_query);
   if (st != MFA_OK) return st;
   DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse,
-                                      scale, batch, max_pages, num_pages, workspace, plan);
+                                      scale, batch, max_pages, num_pages, workspace, plan, n_query);
   if (fp8) p.piece_cost = kPieceCostPagesFp8;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -255,7 +260,7 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
     return cuda_fail(e, "profile event record");
   CUtensorMap kmap, vmap, qmap;
   const uint64_t rows = (uint64_t)num_pages * kPageSize;
-  if ((st = encode_rows_bf16(&qmap, q, (uint64_t)batch * kHeads)) != MFA_OK) return st;
+  if ((st = encode_rows_bf16(&qmap, q, (uint64_t)batch * n_query * kHeads)) != MFA_OK) return st;
   if (fp8) {
     if ((st = encode_rows_e4m3(&kmap, k_cache, rows)) != MFA_OK || (st = encode_rows_e4m3(&vmap, v_cache, rows)) != MFA_OK)
       return st;
@@ -263,7 +268,7 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   } else {
     if ((st = encode_rows_bf16(&kmap, k_cache, rows)) != MFA_OK || (st = encode_rows_bf16(&vmap, v_cache, rows)) != MFA_OK)
       return st;
-    e = launch_decode_split_tc(p, kmap, vmap, qmap, s);
+    e = n_query == 2 ? launch_decode_split_tc_mtp(p, kmap, vmap, qmap, s) : launch_decode_split_tc(p, kmap, vmap, qmap, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
   if (g_prof_stop && (e = cudaEventRecordWithFlags(g_prof_stop, s, cudaEventRecordExternal)) != cudaSuccess)
@@ -299,6 +304,13 @@ mfa_status_t mfa_plan_decode(int batch, int max_len_hint, int num_sms, mfa_plan_
 size_t mfa_decode_workspace_bytes(int batch, int max_len_hint) {
   mfa_plan_t plan;
   if (mfa_plan_decode(batch, max_len_hint, 0, &plan) != MFA_OK) return 0;
+  return plan.workspace_bytes;
+}
+
+size_t mfa_decode_mtp_workspace_bytes(int batch, int n_query, int max_len_hint) {
+  mfa_plan_t plan;
+  if (n_query < 1 || n_query > 2 || mfa_plan_decode(batch, max_len_hint, 0, &plan) != MFA_OK) return 0;
+  fill_plan(batch, max_len_hint, plan.grid_ctas, &plan, n_query);
   return plan.workspace_bytes;
 }
 
@@ -339,6 +351,15 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       size_t workspace_bytes, void* stream) {
   return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
                        max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream);
+}
+
+mfa_status_t mfa_decode_attention_mtp(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
+                                      float scale, int batch, int n_query, int max_pages, int num_pages,
+                                      int max_len_hint, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_query < 1 || n_query > 2) return fail(MFA_ERR_INVALID_ARG, "n_query %d is not 1 or 2", n_query);
+  return decode_common(q, k_cache, v_cache, nullptr, nullptr, false, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, n_query);
 }
 
 mfa_status_t mfa_check_device_errors(void* workspace, int clear, void* stream) {

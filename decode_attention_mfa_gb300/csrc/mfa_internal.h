@@ -53,14 +53,15 @@ struct DecodeParams {
   const float* v_scale;
   const int32_t* page_table;
   const int32_t* seq_lens;
-  uint16_t* out;           // [B][64][256] bf16 bits
-  float* lse;              // [B][64]
-  float* part_o;           // [slots][64][256]
-  float* part_lse;         // [slots][64]
+  uint16_t* out;           // [B][n_query][64][256] bf16 bits
+  float* lse;              // [B][n_query][64]
+  float* part_o;           // [slots][n_query][64][256]
+  float* part_lse;         // [slots][n_query][64]
   uint32_t* err;
   float scale;
   int B, max_pages, num_pages, grid;
   int piece_cost;          // cost units charged per sequence piece (work partition)
+  int n_query;             // query tokens per sequence (1, or 2 for multi-token decode); q is [B][n_query][64][256]
   uint64_t wait_budget_ns;
 };
 
@@ -90,6 +91,10 @@ cudaError_t launch_decode_split_tc_fp8(const DecodeParams& p, const CUtensorMap&
                                        const CUtensorMap& q_map, cudaStream_t stream);
 size_t decode_split_tc_smem_bytes(int B);
 size_t decode_split_tc_fp8_smem_bytes(int B);
+// Two query tokens per sequence (multi-token decode), bf16 cache.
+cudaError_t launch_decode_split_tc_mtp(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                       const CUtensorMap& q_map, cudaStream_t stream);
+size_t decode_split_tc_mtp_smem_bytes(int B);
 
 // Host-side services of mfa_api.cu for other entry points of the library.
 void set_last_error_message(const char* msg);

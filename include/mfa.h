@@ -158,15 +158,40 @@ mfa_status_t mfa_decode_attention(const void* q, const void* k_cache, const void
 
 /* MFA decode attention over an FP8-E4M3 paged cache with per-token fp32
  * scales (k_scale, v_scale [num_pages][64], [device], 16-byte aligned). The
- * cached value is decode(code) * scale. Queries stay bf16. The tensor cores
- * multiply in f16: q is rounded to f16 (exact for 2^-14 <= |q| < 65504) and
- * P is scaled by the V scale before rounding to f16, which needs
- * |v| < ~1e5. Everything else as mfa_decode_attention. */
+ * cached value is decode(code) * scale. Queries stay bf16. Both products run
+ * on the tensor cores with 8-bit operands straight from the cache: q enters
+ * as the sum of two E4M3 terms under a power-of-two scale (every element down
+ * to 2^-10.8 of the largest |q| of the sequence piece is held exactly, the
+ * rest within 2^-18.8 of it), and P times the V scale (relative to the
+ * piece's largest V scale) as the sum of two E4M3 terms (about 2^-8
+ * relative). Everything else as mfa_decode_attention. */
 mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
                                       const float* k_scale, const float* v_scale,
                                       const int32_t* page_table, const int32_t* seq_lens,
                                       void* out, float* lse, float scale,
                                       int batch, int max_pages, int num_pages, int max_len_hint,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Multi-token (MTP) decode over a bf16 paged cache ("Step-3 is Large yet
+ * Affordable", section 5.2: with multi-token prediction a decode step carries
+ * extra predicted tokens that read the same KV cache). Each sequence has
+ * n_query (1 or 2) query tokens, its last n_query positions: the cache of
+ * seq_lens[b] tokens already holds them (mfa_kv_append with n_new = n_query).
+ * Query token t attends, causally, to positions j < seq_lens[b] - n_query + 1
+ * + t; a token that sees no position gets out = 0 and lse = -inf.
+ *   q:   [device] bf16 [batch][n_query][64][256], 16-byte aligned
+ *   out: [device] bf16 [batch][n_query][64][256]; lse: fp32 [batch][n_query][64]
+ * With n_query = 2 both tokens share every pass over the cache: their 64 heads
+ * each form one 128-column product with a tile of keys (and of values), so
+ * the cache is read once for the two tokens. workspace: at least
+ * mfa_decode_mtp_workspace_bytes(batch, n_query, max_len_hint) bytes (0 for a
+ * bad argument). Host errors: MFA_ERR_INVALID_ARG also for n_query outside
+ * {1, 2}. Everything else as mfa_decode_attention. */
+size_t mfa_decode_mtp_workspace_bytes(int batch, int n_query, int max_len_hint);
+mfa_status_t mfa_decode_attention_mtp(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* page_table, const int32_t* seq_lens,
+                                      void* out, float* lse, float scale,
+                                      int batch, int n_query, int max_pages, int num_pages, int max_len_hint,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* Allocation-free variant of mfa_decode_attention (bf16 cache). The paper

@@ -25,6 +25,15 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(capi._SIGNATURES), "binding and header disagree"
 
 
+def test_mtp_query_count_is_checked_before_any_device_work(lib):
+    """n_query outside {1, 2}: MFA_ERR_INVALID_ARG from the host checks; the
+    workspace size query answers 0."""
+    for nq in (0, 3, -1):
+        assert lib.mfa_decode_attention_mtp(None, None, None, None, None, None, None, 0.0625, 1, nq, 1, 1, 0,
+                                            None, 0, None) == 1
+        assert lib.mfa_decode_mtp_workspace_bytes(4, nq, 1024) == 0
+
+
 def test_status_strings(lib):
     for code, name in capi.STATUS_NAMES.items():
         assert capi.mfa_status_string(code) == name
