@@ -197,7 +197,9 @@ def run_ours(args, rank, world, local):
     R = args.copies if args.copies > 0 else choose_copies(w, lens0, total_steps)
     headroom = math.ceil(total_steps / R) + 2
     # inputs: seeded on the host, one copy moved to HBM, cloned R times there
-    wr = wl.Workload(w.name, w.batch, w.lengths, w.kv_dtype, w.permute_pages, 0, w.seed + 1000 * rank)
+    wr = wl.Workload(w.name, w.batch, w.lengths, w.kv_dtype, w.permute_pages, 0, w.seed + 1000 * rank,
+                     queries=w.queries)
+    nq = w.queries
     case = wl.make_case(wr, lengths=lens0, headroom_tokens=headroom)
     max_pages = case.page_table.shape[1]
     num_pages = case.num_pages
@@ -205,7 +207,8 @@ def run_ours(args, rank, world, local):
     fp8 = w.kv_dtype == "fp8"
     stream = torch.cuda.Stream(device=dev)
     ws_hint = int(lens0.max()) + headroom
-    ws_bytes = capi.mfa_decode_workspace_bytes(B, ws_hint)
+    ws_bytes = (capi.mfa_decode_mtp_workspace_bytes(B, nq, ws_hint) if nq > 1
+                else capi.mfa_decode_workspace_bytes(B, ws_hint))
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     capi.mfa_workspace_init(workspace, ws_bytes)
     with torch.cuda.stream(stream):
@@ -233,10 +236,15 @@ def run_ours(args, rank, world, local):
         k_scales = [ks0] + [ks0.clone() for _ in range(R - 1)] if fp8 else [None] * R
         v_scales = [vs0] + [vs0.clone() for _ in range(R - 1)] if fp8 else [None] * R
         seq_lens = torch.from_numpy(np.tile(lens0.astype(np.int32), (R, 1))).to(dev)
-        q = case.q.to(dev).unsqueeze(0).repeat(R, 1, 1, 1).contiguous()
+        if nq > 1:  # [B, nq, 64, 256]: the step's query tokens
+            q1 = wl.draw_rows(B * nq * wl.HEADS, wl.HEAD_DIM, [wr.seed, 90], 0).view(B, nq, wl.HEADS, wl.HEAD_DIM)
+        else:
+            q1 = case.q
+        q = q1.to(dev).unsqueeze(0).repeat(R, *([1] * q1.dim())).contiguous()
         newkv = wl.draw_rows(2 * B, wl.HEAD_DIM, [w.seed, rank], 11).view(2, B, 1, wl.HEAD_DIM).to(dev)
-        out = torch.empty((B, wl.HEADS, wl.HEAD_DIM), dtype=torch.bfloat16, device=dev)
-        lse = torch.empty((B, wl.HEADS), dtype=torch.float32, device=dev)
+        qshape = (B, nq) if nq > 1 else (B,)
+        out = torch.empty(qshape + (wl.HEADS, wl.HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(qshape + (wl.HEADS,), dtype=torch.float32, device=dev)
     stream.synchronize()
     del case
     host_len = np.tile(lens0.astype(np.int64), (R, 1))  # host mirror of every copy's length
@@ -260,15 +268,19 @@ def run_ours(args, rank, world, local):
             if app:
                 capi.mfa_kv_append(kn, vn, 1, k_caches[r], v_caches[r], page_table, sl, B, max_pages, num_pages,
                                    workspace, stream)
-            capi.mfa_decode_attention(qq, k_caches[r], v_caches[r], page_table, sl, out, lse, wl.SCALE, B,
-                                      max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
+            if nq > 1:
+                capi.mfa_decode_attention_mtp(qq, k_caches[r], v_caches[r], page_table, sl, out, lse, wl.SCALE, B,
+                                              nq, max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
+            else:
+                capi.mfa_decode_attention(qq, k_caches[r], v_caches[r], page_table, sl, out, lse, wl.SCALE, B,
+                                          max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
 
     def account(r):
         if app:
             host_len[r] += 1
         L = host_len[r].copy()
-        step_bytes.append(acc.decode_step_bytes(L, w.kv_dtype, appended_tokens=1 if app else 0))
-        split_bytes.append(int(L.sum()) * acc.kv_bytes_per_token(w.kv_dtype) + B * wl.HEADS * wl.HEAD_DIM * 2
+        step_bytes.append(acc.decode_step_bytes(L, w.kv_dtype, appended_tokens=1 if app else 0, n_query=nq))
+        split_bytes.append(int(L.sum()) * acc.kv_bytes_per_token(w.kv_dtype) + nq * B * wl.HEADS * wl.HEAD_DIM * 2
                            + int(((L + 63) // 64).sum()) * 4 + B * 4)
         return L
 
@@ -370,12 +382,12 @@ def run_ours(args, rank, world, local):
 
     e2e = None
     if not args.no_e2e:
-        hq = torch.empty((B, wl.HEADS, wl.HEAD_DIM), dtype=torch.bfloat16).pin_memory()
+        hq = torch.empty(q[0].shape, dtype=torch.bfloat16).pin_memory()
         hq.copy_(q[0].cpu())
         hkv = torch.empty((2, B, 1, wl.HEAD_DIM), dtype=torch.bfloat16).pin_memory()
         hkv.copy_(newkv.cpu())
-        hout = torch.empty((B, wl.HEADS, wl.HEAD_DIM), dtype=torch.bfloat16).pin_memory()
-        hlse = torch.empty((B, wl.HEADS), dtype=torch.float32).pin_memory()
+        hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
         dq = torch.empty_like(q[0])
         dkv = torch.empty_like(newkv)
         n_before = len(step_bytes)
@@ -395,8 +407,10 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "description": w.description, "batch": B, "heads": wl.HEADS,
                    "head_dim": wl.HEAD_DIM, "page_size": wl.PAGE_SIZE, "kv_dtype": w.kv_dtype,
                    "mean_attended_len": mean_len,
+                   "queries_per_sequence": nq,
                    "step": ("mfa_kv_append(1 token/seq) + " if app else "") +
-                           "mfa_decode_attention (split + LSE combine)",
+                           ("mfa_decode_attention_mtp" if nq > 1 else "mfa_decode_attention") +
+                           " (split + LSE combine)",
                    "l2": f"inputs rotate over {R} device-resident cache copies "
                          f"({R * float(lens0.sum()) * acc.kv_bytes_per_token(w.kv_dtype) / 1e9:.1f} GB >> 135 MB L2)",
                    "parallelism": f"dp{world} (independent batch per GPU)"},
@@ -446,12 +460,21 @@ class OracleSampler:
             self.kc = wl.bits(wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
             self.vc = wl.bits(wl.scatter_rows(case.v_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
             self.ks = self.vs = None
-        self.q = wl.bits(case.q)
-        self.page_table = case.page_table
-        self.sl = case.lengths0.astype(np.int32)
-        self.total_rows = case.batch * wl.HEADS
+        nq = w.queries
+        self.step_bytes = acc.decode_step_bytes(case.lengths0, w.kv_dtype, appended_tokens=w.append_tokens,
+                                                n_query=nq)
+        if nq > 1:  # token t of sequence b: a single-token decode over its first L - nq + 1 + t positions
+            q = wl.draw_rows(case.batch * nq * wl.HEADS, wl.HEAD_DIM, [w.seed, 90], 0)
+            self.q = wl.bits(q.view(case.batch * nq, wl.HEADS, wl.HEAD_DIM))
+            self.page_table = np.repeat(case.page_table, nq, axis=0)
+            L = case.lengths0.astype(np.int64)
+            self.sl = np.maximum(L[:, None] - nq + 1 + np.arange(nq)[None, :], 0).astype(np.int32).reshape(-1)
+        else:
+            self.q = wl.bits(case.q)
+            self.page_table = case.page_table
+            self.sl = case.lengths0.astype(np.int32)
+        self.total_rows = self.sl.size * wl.HEADS
         self.order = np.random.default_rng(0).permutation(self.total_rows)
-        self.step_bytes = acc.decode_step_bytes(self.sl, w.kv_dtype, appended_tokens=w.append_tokens)
 
     def run(self, nrows: int) -> float:
         rows = self.order[:nrows]

@@ -37,19 +37,21 @@ def attention_flops_per_token(heads: int = HEADS, head_dim: int = HEAD_DIM) -> i
     return 4 * heads * head_dim
 
 
-def decode_step_bytes(lengths_attended, kv_dtype: str, appended_tokens: int = 0) -> int:
+def decode_step_bytes(lengths_attended, kv_dtype: str, appended_tokens: int = 0, n_query: int = 1) -> int:
     """Algorithmic HBM bytes of one decode step over a batch.
 
     Counts each byte the step must move once: the KV rows attended (after the
-    append), the queries (bf16), the outputs (bf16) and per-head LSE (fp32),
-    the page-table entries and sequence lengths read, and for an append the new
-    bf16 K/V rows read plus the cache rows (and scales) written.  Split-KV
+    append; with n_query query tokens per sequence, multi-token decode, the
+    rows of the longest, last token, which cover the others), the queries
+    (bf16), the outputs (bf16) and per-head LSE (fp32) of every query token,
+    the page-table entries and sequence lengths read, and for an append the
+    new bf16 K/V rows read plus the cache rows (and scales) written.  Split-KV
     partial results are an implementation choice and are not counted."""
     lens = np.asarray(lengths_attended, dtype=np.int64)
     B = int(lens.size)
     kv = int(lens.sum()) * kv_bytes_per_token(kv_dtype)
-    q = B * HEADS * HEAD_DIM * 2
-    out = B * HEADS * HEAD_DIM * 2 + B * HEADS * 4
+    q = n_query * B * HEADS * HEAD_DIM * 2
+    out = n_query * (B * HEADS * HEAD_DIM * 2 + B * HEADS * 4)
     table = int(((lens + PAGE_SIZE - 1) // PAGE_SIZE).sum()) * 4 + B * 4
     app = 0
     if appended_tokens:
@@ -57,6 +59,8 @@ def decode_step_bytes(lengths_attended, kv_dtype: str, appended_tokens: int = 0)
     return kv + q + out + table + app
 
 
-def decode_step_flops(lengths_attended) -> int:
+def decode_step_flops(lengths_attended, n_query: int = 1) -> int:
+    """FLOPs of one decode step; query token t of n_query sees L - n_query + 1 + t tokens."""
     lens = np.asarray(lengths_attended, dtype=np.int64)
-    return int(lens.sum()) * attention_flops_per_token()
+    seen = sum(int(np.maximum(lens - n_query + 1 + t, 0).sum()) for t in range(n_query))
+    return seen * attention_flops_per_token()

@@ -40,6 +40,7 @@ class Workload:
     append_tokens: int      # tokens appended through the KV-append call before attention
     seed: int
     description: str = ""
+    queries: int = 1        # query tokens per sequence (2: multi-token decode)
 
 
 WORKLOADS = {
@@ -51,6 +52,9 @@ WORKLOADS = {
                        "B=128, L uniform in [1024, 8192], one appended token per sequence"),
     "fp8": Workload("fp8", 64, ("fixed", 16384), "fp8", True, 0, 44,
                     "B=64, L=16384, E4M3 cache with per-token fp32 scales"),
+    "mtp4k": Workload("mtp4k", 32, ("fixed", 4096), "bf16", True, 0, 66,
+                      "B=32, L=4096, two query tokens per sequence (multi-token decode), pages randomly permuted",
+                      queries=2),
     "long": Workload("long", 8, ("uniform", 65536, 131072), "bf16", True, 0, 55,
                      "B=8, L uniform in [65536, 131072], pages randomly permuted"),
 }
