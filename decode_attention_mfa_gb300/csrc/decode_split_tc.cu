@@ -70,6 +70,7 @@ struct Cfg<false, false> {
   static constexpr int kSoftmaxThreads = 128 * kGroups;
   static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
   static constexpr int kQ = 1;           // query tokens per sequence
+  static constexpr int kPBufs = 2;       // P buffers
   static constexpr int kCols = 64;       // softmax columns: [token][head]
   static constexpr int kHpt = 32;        // columns per softmax thread
   static constexpr int kOHalfCols = 64;  // O^T columns per 128-dim half
@@ -79,7 +80,7 @@ struct Cfg<false, false> {
 template <>
 struct Cfg<false, true> {
   static constexpr int kThreads = 320;
-  static constexpr int kSlots = 5;       // 16 KB operand chunks (Q and P are twice as large)
+  static constexpr int kSlots = 7;       // 16 KB operand chunks
   static constexpr int kKStages = 0;
   static constexpr int kVStages = 0;
   static constexpr int kStages = 0;
@@ -93,6 +94,7 @@ struct Cfg<false, true> {
   static constexpr int kSoftmaxThreads = 128 * kGroups;
   static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
   static constexpr int kQ = 2;
+  static constexpr int kPBufs = 1;       // Q and P are twice as large: one P buffer keeps 7 ring slots
   static constexpr int kCols = 128;
   static constexpr int kHpt = 64;
   static constexpr int kOHalfCols = 128;
@@ -117,6 +119,7 @@ struct Cfg<true, false> {
   static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
   static constexpr int kVProducerWarp = kProducerWarp + 2, kVRefWarp = kProducerWarp + 3;
   static constexpr int kQ = 1;
+  static constexpr int kPBufs = 2;
   static constexpr int kCols = 64;        // per-head statistics (the two terms are summed)
   static constexpr int kHpt = 32;
   static constexpr int kOHalfCols = 128;  // [term][head]
@@ -154,8 +157,8 @@ struct Bars {  // indices into the barrier array
   static constexpr int QReady = QEmpty + 2;          // [2] Q split into E4M3 terms (E4M3 only)
   static constexpr int SFull = QReady + 2;           // [2]
   static constexpr int SEmpty = SFull + 2;           // [2]
-  static constexpr int PFull = SEmpty + 2;           // [2]
-  static constexpr int PEmpty = PFull + 2;           // [2]
+  static constexpr int PFull = SEmpty + 2;           // [kPBufs <= 2]
+  static constexpr int PEmpty = PFull + 2;           // [kPBufs <= 2]
   static constexpr int OFree = PEmpty + 2;           // [2] one completion per epilogue of a piece using O^T buffer i
   static constexpr int Drain = OFree + 2;
   static constexpr int StFull = Drain + 1;           // [kStages] raw K tile / V page landed
@@ -197,7 +200,7 @@ __host__ __device__ constexpr SmemLayout smem_layout(int B) {
   L.stage = L.ring + C::kSlots * kSlotBytes;  // E4M3: K tiles, then V pages
   L.q = L.stage + C::kKStages * kKTileBytes + C::kVStages * kStageBytes;
   L.p = L.q + C::kQBufs * C::kQ * kQBytes;  // E4M3: the Q terms overwrite the bf16 Q (same 32 KB)
-  L.scales = L.p + 2 * C::kQ * kPBytes;
+  L.scales = L.p + C::kPBufs * C::kQ * kPBytes;
   L.len = L.scales + C::kScaleSlots * kScaleBytes;
   L.prefix = L.len + 4 * B;
   // float red[4][kCols], mref[kCols], alpha[kCols], inv_l[2][kCols], scratch[kCols], vref[2]
@@ -669,7 +672,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   };
   // P.V of tile t of piece `piece` (sg)
   auto do_pv = [&](const Seg& sg, int t, uint32_t piece) -> bool {
-    const uint32_t buf = p_cnt & 1, n = p_cnt >> 1;
+    const uint32_t buf = p_cnt % C::kPBufs, n = p_cnt / C::kPBufs;
     const bool first_of_seg = t == 0;
     // pieces cycle through the O^T buffers; the first P.V of piece j
     // overwrites the buffer of piece j - kOBufs, whose epilogue must be done
@@ -993,12 +996,14 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   const uint32_t taddr_o0 = tmem + lane_base + tmem_o<kFp8, kMtp>();
   const float c2 = p.scale * kLog2e;
   uint32_t s_cnt = 0, p_cnt = 0;
-  // P.V(g) completes phase g/2 of p_empty[g % 2]. Before P(g) is written the
-  // softmax has seen P.V(g-2) complete, and P.V(g+2) cannot start before P(g+2)
-  // exists, so when it waits for P.V(g) that barrier is at phase g/2 or just
-  // past it: the parity wait is exact. Completion of P.V(g) implies that of
+  // With n = kPBufs P buffers, P.V(g) completes phase g/n of p_empty[g % n].
+  // Before P(g) is written the softmax has seen P.V(g-n) complete, and
+  // P.V(g+n) cannot start before P(g+n) exists, so when it waits for P.V(g)
+  // that barrier is at phase g/n or just past it: the parity wait is exact. Completion of P.V(g) implies that of
   // every earlier MMA (one issuing thread, commits track all prior MMAs).
-  auto wait_pv = [&](uint32_t gi) -> bool { return cx.wait(Bb::PEmpty + (gi & 1), (gi >> 1) & 1); };
+  auto wait_pv = [&](uint32_t gi) -> bool {
+    return cx.wait(Bb::PEmpty + gi % C::kPBufs, (gi / C::kPBufs) & 1);
+  };
   // Pieces cycle through the O^T buffers. A piece's O^T / l is written out
   // once the next piece's first P has been handed over (its last P.V was
   // issued before that piece's first S), so the softmax warps go on to the
@@ -1131,8 +1136,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       // (128-byte swizzle) as soon as it is formed. bf16: chunk j = heads
       // [8j, 8j + 8); E4M3: the row is [x1 of heads 0-63 | x2 of heads 0-63],
       // chunk j = x1 and chunk 4 + j = x2 of heads [16j, 16j + 16).
-      const uint32_t pbuf = p_cnt & 1;
-      if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt >> 1) & 1) ^ 1)) return;
+      const uint32_t pbuf = p_cnt % C::kPBufs;
+      if (!cx.wait(Bb::PEmpty + pbuf, ((p_cnt / C::kPBufs) & 1) ^ 1)) return;
       // with two query tokens, token g's [tokens x 64 heads] block sits at g * kPBytes
       const uint32_t prow = cx.base + L.p + pbuf * C::kQ * kPBytes + (kMtp ? g * kPBytes : 0) + row * 128;
       constexpr int kHeadsPerChunk = kFp8 ? 16 : 8;
