@@ -1,42 +1,46 @@
 // decode_split_tc.cu -- split-KV MFA decode on the 5th-generation tensor cores
-// (tcgen05, TMEM accumulators) with TMA streaming, for a bf16 cache and for an
-// FP8-E4M3 cache with per-token fp32 scales.
+// (tcgen05, TMEM accumulators) with TMA streaming: a bf16 cache, an FP8-E4M3
+// cache with per-token fp32 scales, and a bf16 cache read once for two query
+// tokens per sequence (multi-token decode).
 //
 // MFA ("Step-3 is Large yet Affordable", paper summary page, section 2 /
 // Table 1) gives all 64 query heads one shared K head and one shared V head
 // (d = 256), so for one sequence the logits of every head against a tile of
 // keys form one dense contraction. The kernel computes, per 128-token tile
 // (two 64-token pages), the transposed products
-//     S^T[tok, head] = K_tile[tok, :] . Q[head, :]^T       (M=128, N=64, K=256)
-//     O^T[dim, head] += V_tile[:, dim]^T . P^T[tok, head]  (2 x M=128, N=64, K=128)
+//     S^T[tok, col] = K_tile[tok, :] . Q[col, :]^T        (M=128, N=64 or 128)
+//     O^T[dim, col] += V_tile[:, dim]^T . P^T[tok, col]   (two 128-dim halves)
 // so every MMA uses the full 128-lane data path (an M=64 MMA costs as much as
 // an M=128 one on sm_103a), and softmax statistics are reduced across the 128
-// TMEM lanes.
+// TMEM lanes. The columns are the 64 heads (bf16), [token][head] (two query
+// tokens), or [E4M3 term][head] (E4M3, where the softmax adds the terms).
 //
 // Work split: a stream-K partition of cost units (each non-empty sequence
 // costs its pages plus a fixed charge per piece, see build_cost_prefix); CTA
 // c owns units [c*C/G, (c+1)*C/G) and writes one normalised partial result
-// plus its natural-log LSE per sequence piece into slot c + b; the LSE
-// combine kernel merges the pieces.
+// plus its natural-log LSE per sequence piece (and query token) into slot
+// c + b; the LSE combine kernel merges the pieces.
 //
-// Warp roles (one CTA per SM; G = 1 softmax warpgroup for bf16, 2 for E4M3):
-//   warps 0..4G-1  softmax: warpgroup g owns heads [64g/G, 64(g+1)/G); TMEM
-//                  lane = token of the tile; online softmax in fp32 with a
-//                  lazily updated reference maximum (only when a logit exceeds
-//                  it by 2^threshold are the row sums and O^T rescaled); then
-//                  the epilogue (row-sum reduction, O^T / l, partial LSE).
-//   warp 4G        producer: page-table walk and TMA loads.
-//   warp 4G+1      MMA issue (lane 0) and TMEM allocation.
-//   warp 4G+2      (E4M3 cache only) V page producer.
-//   warp 4G+3      (E4M3 cache only) largest V scale of each piece.
+// Warp roles (one CTA per SM):
+//   warps 0-7  softmax, two warpgroups: warpgroup g owns heads [32g, 32g+32)
+//              (with two query tokens: query token g); TMEM lane = token of
+//              the tile; online softmax in fp32 with a lazily updated
+//              reference maximum (only when a logit exceeds it by
+//              2^threshold are the row sums and O^T rescaled); then the
+//              epilogue (row-sum reduction, O^T / l, partial LSE).
+//   warp 8     producer: page-table walk and TMA loads.
+//   warp 9     MMA issue and TMEM allocation (one thread issues; the rest of
+//              the warp waits at the final barrier).
+//   warp 10    (E4M3 cache only) V page producer.
+//   warp 11    (E4M3 cache only) largest V scale of each piece.
 // bf16 cache: the producer loads 16 KB operand chunks (a 64-dim slice of a
 // 2-page K tile, or a 128-dim slice of one V page) straight into a ring of
-// shared-memory slots in the layouts the MMAs read; the MMA warp zeroes the
+// shared-memory slots in the layouts the MMAs read; the MMA thread zeroes the
 // unused rows of a partial last V page (0 * NaN would poison P.V).
 // E4M3 cache ("Step-3 is Large yet Affordable", section 7: 8-bit KV): both
 // products are 8-bit MMAs (kind::f8f6f4) on the raw code pages as TMA stages
-// them. Q enters S^T as two E4M3 terms (a per-head power-of-two scale, then
-// q = t1 + t2 holds every bf16 value down to 2^-10 of the scaled range); P
+// them. Q enters S^T as two E4M3 terms (one power-of-two scale per piece, so
+// q = t1 + t2 holds every bf16 value down to 2^-10.8 of the largest |q|); P
 // enters P.V as two E4M3 terms of P * v_scale, relative to the piece's
 // largest V scale. The K scale, the Q scale and the softmax scale multiply
 // the logits in fp32 in the softmax warps (the row sums use the unscaled P).
@@ -320,7 +324,7 @@ struct PageIds {
 // issues the copies. Per piece: Q, then the chunks of K(0), then for each
 // tile t >= 1 those of K(t) and V(t-1), then V(T-1) -- the order in which the
 // MMA warp consumes them (bf16). E4M3: Q, then per tile the raw K tile and
-// its scale block (the V pages come from warp 6).
+// its scale block (the V pages come from the V producer warp).
 template <bool kFp8, bool kMtp>
 __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               const CUtensorMap* qmap, const Ctx& cx, const int* s_cost, const int* s_len,
@@ -334,7 +338,7 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged K tiles (E4M3); pieces; tiles
   Seg s;
   bool ok = seg_first(s_cost, p.B, lo, hi, s);
-  constexpr int kRing = kFp8 ? C::kKStages : C::kSlots;  // E4M3: the K stage ring (V pages: warp 6)
+  constexpr int kRing = kFp8 ? C::kKStages : C::kSlots;  // E4M3: the K stage ring (V pages: the V producer warp)
   constexpr int kRingFull = kFp8 ? Bb::StFull : Bb::Full;
   constexpr int kRingEmpty = kFp8 ? Bb::StEmpty : Bb::Empty;
   auto wait_slot = [&](uint32_t& dst, uint32_t& bar) -> bool {
