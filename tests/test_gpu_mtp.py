@@ -110,3 +110,20 @@ def test_mtp_4k_context_full_size(oracle_mod):
     out, lse = run_mtp(dev, q)
     out_ref, lse_ref = oracle_mtp(oracle_mod, dev, q)
     compare(out, lse, out_ref, lse_ref, "mtp/4k")
+
+
+def test_mtp_maximum_batch(oracle_mod):
+    """MFA_MAX_BATCH sequences with two query tokens each: the largest shared-
+    memory layout of the two-token kernel and a 2048-row combine grid; short
+    ragged lengths, two of them 0 and two of them 1 (token 0 sees nothing)."""
+    rng = np.random.default_rng(321)
+    lengths = [int(x) for x in rng.integers(0, 200, size=capi.MAX_BATCH)]
+    lengths[3] = lengths[500] = 0
+    lengths[7] = lengths[900] = 1
+    case, q = mtp_case(lengths, seed=47)
+    dev = DeviceCache(case)
+    out, lse = run_mtp(dev, q)
+    out_ref, lse_ref = oracle_mtp(oracle_mod, dev, q)
+    compare(out, lse, out_ref, lse_ref, "mtp/max-batch", bf16_storage_slack=True)
+    assert torch.all(out[3] == 0) and torch.all(torch.isneginf(lse[3]))
+    assert torch.all(out[7, 0] == 0) and torch.all(torch.isneginf(lse[7, 0])) and torch.all(torch.isfinite(lse[7, 1]))
