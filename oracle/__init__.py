@@ -205,6 +205,28 @@ def mfa_decode_mtp(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_s
     return out.reshape(B, T, H, D), lse.reshape(B, T, H)
 
 
+def query_lowrank(x_bits, w_down_bits, gamma_bits, w_up_bits, eps):
+    """MFA's low-rank query path in fp64.
+
+    "Step-3 is Large yet Affordable" (paper summary page), section 2 / Table 1:
+    the query is projected down from the model width (7168) to a low rank
+    (2048), normalised, then projected up to 64 heads x 256. The normalisation
+    is read as RMSNorm with a learned gain: h = y / sqrt(mean(y^2) + eps) *
+    gamma, with y = x W_down. matmul is the library primitive for the two
+    products.
+
+    x_bits [B, Dm], w_down_bits [Dm, R], gamma_bits [R], w_up_bits [R, N]
+    (uint16, bf16 bits). Returns (q [B, N], h [B, R]) in fp64; q reshapes to
+    [B, 64, 256] when N = 16384."""
+    x = bf16_to_f64(_c(x_bits, np.uint16))
+    wd = bf16_to_f64(_c(w_down_bits, np.uint16))
+    g = bf16_to_f64(_c(gamma_bits, np.uint16))
+    wu = bf16_to_f64(_c(w_up_bits, np.uint16))
+    y = x @ wd
+    h = y / np.sqrt(np.mean(y * y, axis=1, keepdims=True) + float(eps)) * g[None, :]
+    return h @ wu, h
+
+
 def kv_append(k_new_bits, v_new_bits, k_cache, v_cache, page_table, seq_lens, *, k_scale=None,
               v_scale=None):
     """Append n_new tokens per sequence to host copies of the cache, in place.
