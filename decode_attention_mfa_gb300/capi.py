@@ -48,6 +48,8 @@ _SIGNATURES = {
     "mfa_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P], _I),
     "mfa_decode_mtp_workspace_bytes": ([_I, _I, _I], _Z),
+    "mfa_query_lowrank_workspace_bytes": ([_I, _I], _Z),
+    "mfa_query_lowrank": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _Z, _P], _I),
     "mfa_decode_attention_mtp": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_check_device_errors": ([_P, _I, _P], _I),
     "mfa_set_wait_budget_ns": ([_U64], None),
@@ -144,6 +146,23 @@ def mfa_decode_attention(q, k_cache, v_cache, page_table, seq_lens, out, lse, sc
                                        _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch,
                                        max_pages, num_pages, max_len_hint, _ptr(workspace),
                                        workspace_bytes, _stream(stream)))
+
+
+MAX_QUERY_BATCH = 256
+
+
+def mfa_query_lowrank_workspace_bytes(batch: int, rank: int) -> int:
+    n = load().mfa_query_lowrank_workspace_bytes(batch, rank)
+    if n == 0:
+        raise MFAError(1, "bad arguments for mfa_query_lowrank_workspace_bytes")
+    return n
+
+
+def mfa_query_lowrank(x, w_down, gamma, w_up, q, batch, d_model, rank, n_out, eps, workspace, workspace_bytes,
+                      stream=None):
+    """Low-rank query path: q = bf16(RMSNorm(x W_down) * gamma) W_up, bf16 in and out."""
+    _check(load().mfa_query_lowrank(_ptr(x), _ptr(w_down), _ptr(gamma), _ptr(w_up), _ptr(q), batch, d_model, rank,
+                                    n_out, float(eps), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def mfa_decode_mtp_workspace_bytes(batch: int, n_query: int, max_len_hint: int) -> int:

@@ -1,6 +1,7 @@
 // mfa_api.cu -- host side of the libmfa C ABI: argument checks, split
 // planning and kernel launches. No call here allocates device memory or
 // synchronises, except mfa_check_device_errors.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -118,6 +119,23 @@ mfa_status_t encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows)
   const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
   const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MFA_OK;
+}
+
+// 2-D bf16 tensor [rows][cols] read in [box_rows x 64 columns] boxes with the
+// 128-byte swizzle; rows past the end read as zeros.
+mfa_status_t encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  mfa_status_t st = get_encoder(&enc);
+  if (st != MFA_OK) return st;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -351,6 +369,56 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       size_t workspace_bytes, void* stream) {
   return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
                        max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream);
+}
+
+size_t mfa_query_lowrank_workspace_bytes(int batch, int rank) {
+  if (batch < 1 || batch > kMaxQueryBatch || rank < 128) return 0;
+  return kWsHeaderBytes + (size_t)batch * rank * (sizeof(float) + sizeof(uint16_t));
+}
+
+mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* gamma, const void* w_up, void* q,
+                               int batch, int d_model, int rank, int n_out, float eps, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!x || !w_down || !gamma || !w_up || !q) return fail(MFA_ERR_INVALID_ARG, "null pointer argument");
+  if (batch < 1 || batch > kMaxQueryBatch)
+    return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxQueryBatch);
+  if (d_model < 64 || d_model % 64 || rank < 128 || rank % 128 || n_out < 128 || n_out % 128)
+    return fail(MFA_ERR_INVALID_ARG, "d_model must be a multiple of 64, rank and n_out multiples of 128");
+  if (!(eps >= 0.0f)) return fail(MFA_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!aligned(x, 16) || !aligned(w_down, 16) || !aligned(w_up, 16) || !aligned(q, 16) || !aligned(gamma, 2))
+    return fail(MFA_ERR_INVALID_ARG, "misaligned pointer (x, weights, q need 16 bytes)");
+  if (!workspace || !aligned(workspace, 256)) return fail(MFA_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
+  const size_t need = mfa_query_lowrank_workspace_bytes(batch, rank);
+  if (workspace_bytes < need) return fail(MFA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  DeviceInfo info;
+  mfa_status_t st = current_device(nullptr, &info);
+  if (st != MFA_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  QueryLowrankParams p{};
+  p.gamma = static_cast<const uint16_t*>(gamma);
+  p.y = reinterpret_cast<float*>(ws + kWsHeaderBytes);
+  p.h = reinterpret_cast<uint16_t*>(ws + kWsHeaderBytes + (size_t)batch * rank * sizeof(float));
+  p.q = static_cast<uint16_t*>(q);
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  p.budget = g_wait_budget_ns.load(std::memory_order_relaxed);
+  p.eps = eps;
+  p.B = batch;
+  p.d_model = d_model;
+  p.rank = rank;
+  p.n_out = n_out;
+  // K split of the down-projection: about one CTA per SM, at most one 64-wide K block per CTA
+  const int blocks = rank / 128, kchunks = d_model / 64;
+  p.splits_down = std::max(1, std::min(kchunks, info.num_sms / blocks));
+  const uint32_t Bp = (uint32_t)((batch + 15) & ~15);
+  CUtensorMap wd_map, x_map, wu_map, h_map;
+  if ((st = encode_bf16_2d(&wd_map, w_down, (uint64_t)rank, (uint64_t)d_model, 64)) != MFA_OK ||
+      (st = encode_bf16_2d(&x_map, x, (uint64_t)d_model, (uint64_t)batch, Bp)) != MFA_OK ||
+      (st = encode_bf16_2d(&wu_map, w_up, (uint64_t)n_out, (uint64_t)rank, 64)) != MFA_OK ||
+      (st = encode_bf16_2d(&h_map, p.h, (uint64_t)rank, (uint64_t)batch, Bp)) != MFA_OK)
+    return st;
+  const cudaError_t e = launch_query_lowrank(p, wd_map, x_map, wu_map, h_map, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "query path launch");
+  return MFA_OK;
 }
 
 mfa_status_t mfa_decode_attention_mtp(const void* q, const void* k_cache, const void* v_cache,

@@ -16,6 +16,7 @@ constexpr int kHeads = MFA_HEADS;        // query heads sharing one K and one V 
 constexpr int kHeadDim = MFA_HEAD_DIM;   // head dimension
 constexpr int kPageSize = MFA_PAGE_SIZE; // tokens per cache page
 constexpr int kMaxBatch = MFA_MAX_BATCH;
+constexpr int kMaxQueryBatch = MFA_MAX_QUERY_BATCH;  // the query path's N = batch (one MMA, <= 256)
 
 // Workspace layout: [header 256 B][partial O: slots x 64 x 256 fp32][partial lse: slots x 64 fp32]
 constexpr size_t kWsHeaderBytes = 256;
@@ -100,6 +101,24 @@ size_t decode_split_tc_mtp_smem_bytes(int B);
 void set_last_error_message(const char* msg);
 uint64_t current_wait_budget_ns();
 cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream);
+
+// Low-rank query path: y = x W_down (fp32, K split over `splits_down` CTAs per
+// feature block), h = bf16(RMSNorm(y) * gamma), q = bf16(h W_up).
+struct QueryLowrankParams {
+  const uint16_t* gamma;   // [rank] bf16 bits
+  float* y;                // [B][rank] fp32 scratch
+  uint16_t* h;             // [B][rank] bf16 scratch
+  uint16_t* q;             // [B][n_out] bf16 bits
+  uint32_t* err;
+  uint64_t budget;
+  float eps;
+  int B, d_model, rank, n_out, splits_down;
+};
+// wd_map: W_down [d_model][rank]; x_map: x [B][d_model]; wu_map: W_up [rank][n_out]; h_map: h [B][rank]
+// (bf16, 64 x 64 boxes for the weights, 64 x Bp boxes for the activations, 128-byte swizzle).
+cudaError_t launch_query_lowrank(const QueryLowrankParams& p, const CUtensorMap& wd_map, const CUtensorMap& x_map,
+                                 const CUtensorMap& wu_map, const CUtensorMap& h_map, cudaStream_t stream);
+size_t query_lowrank_gemm_smem_bytes(int Bp);
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t budget_ns, cudaStream_t stream);
 
 }  // namespace mfa

@@ -61,6 +61,7 @@ extern "C" {
 #define MFA_HEAD_DIM 256
 #define MFA_PAGE_SIZE 64
 #define MFA_MAX_BATCH 1024
+#define MFA_MAX_QUERY_BATCH 256  /* batch limit of mfa_query_lowrank */
 
 typedef enum {
   MFA_OK = 0,
@@ -171,6 +172,30 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       void* out, float* lse, float scale,
                                       int batch, int max_pages, int num_pages, int max_len_hint,
                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* MFA's low-rank query path ("Step-3 is Large yet Affordable", section 2 /
+ * Table 1: the query is projected down from the model width to a low rank,
+ * normalised, and projected up to 64 heads x 256; Step-3: 7168 -> 2048 ->
+ * 64 x 256). Computes, for every row b,
+ *     y = x[b] W_down                         (fp32 accumulation)
+ *     h = bf16( y / sqrt(mean(y^2) + eps) * gamma )    (RMSNorm with gain)
+ *     q[b] = bf16( h W_up )
+ *   x:      [device] bf16 [batch][d_model], 16-byte aligned
+ *   w_down: [device] bf16 [d_model][rank]; w_up: [device] bf16 [rank][n_out]
+ *   gamma:  [device] bf16 [rank]
+ *   q:      [device] bf16 [batch][n_out] (n_out = 64 * 256 = 16384 gives the
+ *           [batch][64][256] query of mfa_decode_attention)
+ * Both products run on the tensor cores and stream each weight once, so the
+ * call is bound by memory bandwidth (96 MB of weights at the Step-3 shape).
+ * workspace: [device] at least mfa_query_lowrank_workspace_bytes(batch, rank)
+ * bytes, 256-byte aligned, initialised by mfa_workspace_init (error word and
+ * the y / h scratch). Host errors: MFA_ERR_INVALID_ARG for null or misaligned
+ * pointers, batch outside [1, MFA_MAX_QUERY_BATCH], d_model not a multiple of
+ * 64, rank or n_out not a multiple of 128, eps < 0; MFA_ERR_WORKSPACE. */
+size_t mfa_query_lowrank_workspace_bytes(int batch, int rank);
+mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* gamma, const void* w_up, void* q,
+                               int batch, int d_model, int rank, int n_out, float eps,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Multi-token (MTP) decode over a bf16 paged cache ("Step-3 is Large yet
  * Affordable", section 5.2: with multi-token prediction a decode step carries
