@@ -56,7 +56,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(wl.WORKLOADS), default="ctx4k")
+    ap.add_argument("--workload", choices=sorted(wl.WORKLOADS) + ["qproj"], default="ctx4k",
+                    help="a decode workload, or qproj: the low-rank query path at the Step-3 shape")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (debug runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--copies", type=int, default=0,
@@ -506,6 +507,21 @@ def run_reference(args):
     rank, world, _ = mdist.env_rank()
     if rank != 0:
         return None
+    if args.workload == "qproj":  # the fp64 oracle of the query path on a bounded sample of rows
+        import torch
+        g = torch.Generator().manual_seed(1234)
+        B, Dm, R_, N = QPROJ["batch"], QPROJ["d_model"], QPROJ["rank"], QPROJ["n_out"]
+        x = torch.randn(B, Dm, generator=g).to(torch.bfloat16)
+        w_down = (torch.randn(Dm, R_, generator=g) / Dm ** 0.5).to(torch.bfloat16)
+        gamma = (1.0 + 0.1 * torch.randn(R_, generator=g)).to(torch.bfloat16)
+        w_up = (torch.randn(R_, N, generator=g) / R_ ** 0.5).to(torch.bfloat16)
+        cb = qproj_cpu_baseline(x, w_down, gamma, w_up, budget_s=max(0.05, 150.0 / max(1, args.steps + args.warmup)))
+        return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+                "config": {"workload": "qproj", "batch": B, "d_model": Dm, "rank": R_, "n_out": N},
+                "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0}}
     w = wl.WORKLOADS[args.workload]
     lens = first_attended(w)   # lengths attended in the first step of our arm
     threads = len(os.sched_getaffinity(0))
@@ -527,8 +543,163 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------ query path
+QPROJ = {"batch": 32, "d_model": 7168, "rank": 2048, "n_out": 64 * 256, "eps": 1e-6}
+
+
+def qproj_bytes(B, d_model, rank, n_out):
+    """Algorithmic bytes of one query-path call: both weights and the gain once,
+    x read, q written (the fp32/bf16 scratch rows are not counted)."""
+    return 2 * (d_model * rank + rank * n_out + rank + B * d_model + B * n_out)
+
+
+def run_qproj(args, rank_id, world, local):
+    import torch
+    from decode_attention_mfa_gb300 import capi
+    from decode_attention_mfa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, Dm, R_, N = QPROJ["batch"], QPROJ["d_model"], QPROJ["rank"], QPROJ["n_out"]
+    g = torch.Generator(device=dev).manual_seed(1234 + rank_id)
+    copies = args.copies if args.copies > 0 else 3  # 3 x 96 MB of weights >> the 135 MB L2
+    w_down = [(torch.randn(Dm, R_, device=dev, generator=g) / Dm ** 0.5).to(torch.bfloat16) for _ in range(copies)]
+    w_up = [(torch.randn(R_, N, device=dev, generator=g) / R_ ** 0.5).to(torch.bfloat16) for _ in range(copies)]
+    gamma = (1.0 + 0.1 * torch.randn(R_, device=dev, generator=g)).to(torch.bfloat16)
+    x = torch.randn(B, Dm, device=dev, generator=g).to(torch.bfloat16)
+    q = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(B, R_)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    capi.mfa_workspace_init(ws, ws_bytes)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(i, xs=None):
+        capi.mfa_query_lowrank(x if xs is None else xs, w_down[i], gamma, w_up[i], q, B, Dm, R_, N, QPROJ["eps"], ws,
+                               ws_bytes, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i % copies)
+    stream.synchronize()
+    capi.mfa_check_device_errors(ws, clear=True, stream=stream)
+
+    def timed(n, e2e=None):
+        gr = torch.cuda.CUDAGraph()
+        stream.synchronize()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(copies):
+                if e2e is None:
+                    call(i)
+                else:
+                    hx, dx, hq = e2e
+                    dx.copy_(hx, non_blocking=True)
+                    call(i, dx)
+                    hq.copy_(q, non_blocking=True)
+        reps = max(1, n // copies)
+        torch.cuda.synchronize()
+        mdist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        mdist.barrier()
+        return e0.elapsed_time(e1), reps * copies, (t0, t1)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms, n, (t0, t1) = timed(args.steps)
+    time.sleep(0.15)
+    clocks.stop()
+    clk = clocks.summary(t0, t1)
+    # per-call device time: an event pair around each call, issued eagerly (the
+    # host enqueues far ahead of the GPU, so the stream never waits on it)
+    n_ev = min(args.steps, 64)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            call(i % copies)
+            b.record(stream)
+    torch.cuda.synchronize()
+    per_call = [a.elapsed_time(b) for a, b in evs]
+    capi.mfa_check_device_errors(ws, clear=True, stream=stream)
+    step_bytes = qproj_bytes(B, Dm, R_, N)
+    total_bytes, max_s = mdist.aggregate(float(step_bytes) * n, ms / 1e3)
+    value = total_bytes / max_s / 1e12
+    peak_gbs, peak_kind = measured_peaks()
+    avg_us = float(np.mean(per_call)) * 1e3
+    achieved = step_bytes / (avg_us * 1e-6) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
+        hx.copy_(x.cpu())
+        hq = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        dx = torch.empty_like(x)
+        e_ms, e_n, _ = timed(args.steps, (hx, dx, hq))
+        e_bytes, e_s = mdist.aggregate(float(step_bytes) * e_n, e_ms / 1e3)
+        e2e = {"value": e_bytes / e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(hx.numel() * 2),
+               "d2h_bytes_per_step": int(hq.numel() * 2), "ms_per_step": e_ms / e_n,
+               "how": "CUDA graph of the C-ABI call with pinned-host copies"}
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n, "warmup": args.warmup,
+        "ms_per_step": max_s * 1e3 / n, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights, bf16)",
+        "config": {"workload": "qproj", "description": "low-rank query path, Step-3 shape: x[32][7168] W_down[7168][2048] "
+                   "-> RMSNorm -> W_up[2048][16384]", "batch": B, "d_model": Dm, "rank": R_, "n_out": N,
+                   "step": "mfa_query_lowrank (two tensor-core GEMMs + RMSNorm)",
+                   "l2": f"weights rotate over {copies} device-resident copies "
+                         f"({copies * 2 * (Dm * R_ + R_ * N) / 1e9:.2f} GB >> 135 MB L2)",
+                   "parallelism": f"dp{world} (independent batch per GPU)"},
+        "steps_per_s": n * world / max_s,
+        "pct_of_measured_peak": 100.0 * value * 1e3 / peak_gbs,
+        "gpu_launches": 3 * n,
+        "clocks": clk,
+        "roofline": {"bound": "hbm", "kernel": "query path (GEMM, RMSNorm, GEMM)", "achieved": achieved,
+                     "peak": peak_gbs, "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak_gbs,
+                     "traffic": None, "algorithmic_bytes_per_launch": float(step_bytes), "avg_launch_us": avg_us,
+                     "launches_averaged": len(per_call),
+                     "how": "CUDA events around each call on its stream, eager calls after the headline region"},
+        "e2e": e2e,
+    }
+    if rank_id == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = qproj_cpu_baseline(x.cpu(), w_down[0].cpu(), gamma.cpu(), w_up[0].cpu())
+    return result
+
+
+def qproj_cpu_baseline(x, w_down, gamma, w_up, budget_s=10.0):
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    B = x.shape[0]
+    bx, bd, bg, bu = wl.bits(x), wl.bits(w_down), wl.bits(gamma), wl.bits(w_up)
+    t = time.perf_counter()
+    oracle.query_lowrank(bx[:1], bd, bg, bu, QPROJ["eps"])
+    one = time.perf_counter() - t
+    rows = int(max(1, min(B, budget_s / max(one, 1e-6))))
+    t = time.perf_counter()
+    oracle.query_lowrank(bx[:rows], bd, bg, bu, QPROJ["eps"])
+    dt = time.perf_counter() - t
+    step_bytes = qproj_bytes(B, *w_down.shape, w_up.shape[1])
+    return {"value": step_bytes * rows / B / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {B} rows of one query-path call (fp64 numpy oracle, {dt:.2f} s), bytes scaled "
+                      "by the rows"}
+
+
 def main():
     args = parse_args()
+    if args.workload == "qproj" and args.impl == "ours":
+        rank, world, local = mdist.init()
+        res = run_qproj(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        mdist.finalize()
+        return
     if args.impl == "reference":
         res = run_reference(args)
         if res is not None:

@@ -149,6 +149,7 @@ def mfa_decode_attention(q, k_cache, v_cache, page_table, seq_lens, out, lse, sc
 
 
 MAX_QUERY_BATCH = 256
+MAX_QUERY_RANK = 16384
 
 
 def mfa_query_lowrank_workspace_bytes(batch: int, rank: int) -> int:

@@ -335,7 +335,7 @@ size_t mfa_decode_mtp_workspace_bytes(int batch, int n_query, int max_len_hint) 
 mfa_status_t mfa_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256))
     return fail(MFA_ERR_WORKSPACE, "workspace missing, misaligned or smaller than its header");
-  const cudaError_t e = cudaMemsetAsync(workspace, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return MFA_OK;
 }
@@ -371,9 +371,11 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
                        max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream);
 }
 
+// Query-path workspace: header | y fp32 [rank/128][batch][128] | h bf16 [batch][rank] | ssq fp32 [rank/128][batch]
 size_t mfa_query_lowrank_workspace_bytes(int batch, int rank) {
-  if (batch < 1 || batch > kMaxQueryBatch || rank < 128) return 0;
-  return kWsHeaderBytes + (size_t)batch * rank * (sizeof(float) + sizeof(uint16_t));
+  if (batch < 1 || batch > kMaxQueryBatch || rank < 128 || rank > kMaxQueryRank) return 0;
+  const size_t ssq = ((size_t)(rank / 128) * batch * sizeof(float) + 255) & ~(size_t)255;
+  return kWsHeaderBytes + (size_t)batch * rank * (sizeof(float) + sizeof(uint16_t)) + ssq;
 }
 
 mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* gamma, const void* w_up, void* q,
@@ -384,6 +386,7 @@ mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* ga
     return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxQueryBatch);
   if (d_model < 64 || d_model % 64 || rank < 128 || rank % 128 || n_out < 128 || n_out % 128)
     return fail(MFA_ERR_INVALID_ARG, "d_model must be a multiple of 64, rank and n_out multiples of 128");
+  if (rank > kMaxQueryRank) return fail(MFA_ERR_INVALID_ARG, "rank %d above %d", rank, kMaxQueryRank);
   if (!(eps >= 0.0f)) return fail(MFA_ERR_INVALID_ARG, "eps must be >= 0");
   if (!aligned(x, 16) || !aligned(w_down, 16) || !aligned(w_up, 16) || !aligned(q, 16) || !aligned(gamma, 2))
     return fail(MFA_ERR_INVALID_ARG, "misaligned pointer (x, weights, q need 16 bytes)");
@@ -398,6 +401,8 @@ mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* ga
   p.gamma = static_cast<const uint16_t*>(gamma);
   p.y = reinterpret_cast<float*>(ws + kWsHeaderBytes);
   p.h = reinterpret_cast<uint16_t*>(ws + kWsHeaderBytes + (size_t)batch * rank * sizeof(float));
+  p.ssq = reinterpret_cast<float*>(ws + kWsHeaderBytes + (size_t)batch * rank * (sizeof(float) + sizeof(uint16_t)));
+  p.counters = reinterpret_cast<uint32_t*>(ws + kQueryCounterOffset);
   p.q = static_cast<uint16_t*>(q);
   p.err = reinterpret_cast<uint32_t*>(ws);
   p.budget = g_wait_budget_ns.load(std::memory_order_relaxed);
@@ -406,9 +411,9 @@ mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* ga
   p.d_model = d_model;
   p.rank = rank;
   p.n_out = n_out;
-  // K split of the down-projection: about one CTA per SM, at most one 64-wide K block per CTA
+  // K split of the down-projection: about one CTA per SM, at least one 64-wide K block per CTA
   const int blocks = rank / 128, kchunks = d_model / 64;
-  p.splits_down = std::max(1, std::min(kchunks, info.num_sms / blocks));
+  p.splits_down = std::max(1, std::min({kchunks, info.num_sms / blocks, kMaxQuerySplits}));
   const uint32_t Bp = (uint32_t)((batch + 15) & ~15);
   CUtensorMap wd_map, x_map, wu_map, h_map;
   if ((st = encode_bf16_2d(&wd_map, w_down, (uint64_t)rank, (uint64_t)d_model, 64)) != MFA_OK ||

@@ -104,10 +104,15 @@ cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream);
 
 // Low-rank query path: y = x W_down (fp32, K split over `splits_down` CTAs per
 // feature block), h = bf16(RMSNorm(y) * gamma), q = bf16(h W_up).
+constexpr size_t kQueryCounterOffset = 128;  // header bytes 128..255: one arrival byte per feature block
+constexpr int kMaxQueryRank = MFA_MAX_QUERY_RANK;  // 128 feature blocks: one arrival byte each
+constexpr int kMaxQuerySplits = 128;         // a byte holds every arrival
 struct QueryLowrankParams {
   const uint16_t* gamma;   // [rank] bf16 bits
-  float* y;                // [B][rank] fp32 scratch
-  uint16_t* h;             // [B][rank] bf16 scratch
+  float* y;                // [rank/128][B][128] fp32 scratch, zero between calls
+  uint16_t* h;             // [B][rank] bf16 scratch: bf16(y * gamma)
+  float* ssq;              // [rank/128][B] fp32 scratch: sums of y^2 per feature block
+  uint32_t* counters;      // arrival bytes in the workspace header
   uint16_t* q;             // [B][n_out] bf16 bits
   uint32_t* err;
   uint64_t budget;
@@ -116,6 +121,7 @@ struct QueryLowrankParams {
 };
 // wd_map: W_down [d_model][rank]; x_map: x [B][d_model]; wu_map: W_up [rank][n_out]; h_map: h [B][rank]
 // (bf16, 64 x 64 boxes for the weights, 64 x Bp boxes for the activations, 128-byte swizzle).
+// Two launches with programmatic stream serialisation.
 cudaError_t launch_query_lowrank(const QueryLowrankParams& p, const CUtensorMap& wd_map, const CUtensorMap& x_map,
                                  const CUtensorMap& wu_map, const CUtensorMap& h_map, cudaStream_t stream);
 size_t query_lowrank_gemm_smem_bytes(int Bp);

@@ -62,6 +62,7 @@ extern "C" {
 #define MFA_PAGE_SIZE 64
 #define MFA_MAX_BATCH 1024
 #define MFA_MAX_QUERY_BATCH 256  /* batch limit of mfa_query_lowrank */
+#define MFA_MAX_QUERY_RANK 16384 /* rank limit of mfa_query_lowrank */
 
 typedef enum {
   MFA_OK = 0,
@@ -105,8 +106,9 @@ mfa_status_t mfa_plan_decode(int batch, int max_len_hint, int num_sms, mfa_plan_
  * its header. */
 size_t mfa_decode_workspace_bytes(int batch, int max_len_hint);
 
-/* Zero the workspace header (error word). Call once after allocating the
- * workspace. [device] workspace. Enqueued on `stream`. */
+/* Zero the first `workspace_bytes` bytes of the workspace (the error word and
+ * every scratch area). Call once after allocating the workspace. [device]
+ * workspace. Enqueued on `stream`. */
 mfa_status_t mfa_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* KV append (bf16 cache). For every sequence b, writes n_new tokens
@@ -187,11 +189,16 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
  *           [batch][64][256] query of mfa_decode_attention)
  * Both products run on the tensor cores and stream each weight once, so the
  * call is bound by memory bandwidth (96 MB of weights at the Step-3 shape).
+ * The call is two kernel launches chained by programmatic dependent launch:
+ * the up-projection streams W_up while the down-projection runs.
  * workspace: [device] at least mfa_query_lowrank_workspace_bytes(batch, rank)
- * bytes, 256-byte aligned, initialised by mfa_workspace_init (error word and
- * the y / h scratch). Host errors: MFA_ERR_INVALID_ARG for null or misaligned
- * pointers, batch outside [1, MFA_MAX_QUERY_BATCH], d_model not a multiple of
- * 64, rank or n_out not a multiple of 128, eps < 0; MFA_ERR_WORKSPACE. */
+ * bytes, 256-byte aligned, zeroed once by mfa_workspace_init: the call needs
+ * its fp32 accumulator zero on entry and leaves it zero (also after a device
+ * error). Calls sharing a workspace run one after another on one stream.
+ * Host errors: MFA_ERR_INVALID_ARG for null or misaligned pointers, batch
+ * outside [1, MFA_MAX_QUERY_BATCH], d_model not a multiple of 64, rank or
+ * n_out not a multiple of 128, rank above MFA_MAX_QUERY_RANK, eps < 0;
+ * MFA_ERR_WORKSPACE. */
 size_t mfa_query_lowrank_workspace_bytes(int batch, int rank);
 mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* gamma, const void* w_up, void* q,
                                int batch, int d_model, int rank, int n_out, float eps,
