@@ -205,6 +205,28 @@ def make_case(w: Workload, *, lengths=None, headroom_tokens: int | None = None,
     return Case(w, lens, q, k_rows, v_rows, k_new, v_new, table, num_pages)
 
 
+def draw_blocks(lengths, n_select: int, seed, max_blocks: int | None = None):
+    """A seeded selection of historical 8-token blocks per sequence (an input:
+    the selection itself is the caller's). Sequence b of length L has
+    floor((L - 1) / 8) complete blocks before the one holding its last token;
+    min(n_select, that count) distinct ones are drawn uniformly, in random
+    order. Returns (block_idx int32 [B, max_blocks] padded with -1, n_blocks
+    int32 [B])."""
+    lens = np.asarray(lengths, dtype=np.int64)
+    B = lens.size
+    width = max(1, n_select if max_blocks is None else max_blocks)
+    rng = np.random.default_rng(np.random.SeedSequence([int(x) for x in np.atleast_1d(seed)] + [77]))
+    block_idx = np.full((B, width), -1, dtype=np.int32)
+    n_blocks = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        hist = max(0, (int(lens[b]) - 1) // 8)
+        k = min(n_select, hist, width)
+        if k:
+            block_idx[b, :k] = rng.choice(hist, size=k, replace=False)
+        n_blocks[b] = k
+    return block_idx, n_blocks
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (no copy when contiguous)."""
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -205,6 +205,84 @@ def mfa_decode_mtp(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_s
     return out.reshape(B, T, H, D), lse.reshape(B, T, H)
 
 
+BLOCK_SIZE = 8
+
+
+def selected_positions(seq_len, blocks):
+    """Positions attended by a decode query over selected 8-token blocks.
+
+    "Step-5-Preview" page (sparse attention, selection and main attention): the
+    query at position t = L - 1 attends to the union of the selected historical
+    blocks r (each covering positions 8r .. 8r + 7, with r < floor(t / 8)) and
+    the positions of its own block up to itself, 8 floor(t / 8) .. t; the
+    softmax runs over that set of original K/V rows. Returns the positions in
+    ascending order. Raises ValueError for a block outside [0, floor(t / 8))
+    or a block listed twice (the selection is a set)."""
+    L = int(seq_len)
+    blocks = [int(r) for r in blocks]
+    if L <= 0:
+        if blocks:
+            raise ValueError("an empty sequence has no blocks to select")
+        return np.zeros(0, dtype=np.int64)
+    cur = (L - 1) // BLOCK_SIZE
+    if len(set(blocks)) != len(blocks):
+        raise ValueError("a block is selected twice")
+    for r in blocks:
+        if not 0 <= r < cur:
+            raise ValueError(f"block {r} is not a historical block of a length-{L} sequence")
+    pos = [BLOCK_SIZE * r + i for r in sorted(blocks) for i in range(BLOCK_SIZE)]
+    pos += list(range(BLOCK_SIZE * cur, L))
+    return np.asarray(pos, dtype=np.int64)
+
+
+def mfa_decode_blocks(q_bits, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks, scale, *,
+                      threads=None):
+    """MFA decode attention over caller-selected 8-token blocks, in fp64.
+
+    The selection rule of ``selected_positions`` with the block list
+    block_idx[b, :n_blocks[b]] of sequence b, applied to MFA's shared K/V head
+    (the selection itself is an input). The selected rows are copied, in
+    ascending position order, into a fresh paged cache of their own (a plain
+    gather), and ``mfa_decode`` runs over it with the selected count as length.
+
+    q_bits [B, H, D] uint16; caches [num_pages, 64, D] uint16 (bf16 bits);
+    page_table [B, max_pages], seq_lens [B], block_idx [B, max_blocks],
+    n_blocks [B] int32. Returns (out [B, H, D], lse [B, H]) fp64."""
+    q = _c(q_bits, np.uint16)
+    B, H, D = q.shape
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    bi = np.asarray(block_idx, dtype=np.int32).reshape(B, -1)
+    nb = np.asarray(n_blocks, dtype=np.int32).reshape(B)
+    num_pages, page = kc.shape[0], kc.shape[1]
+    k_rows, v_rows = kc.reshape(-1, D), vc.reshape(-1, D)
+    sel = []
+    for b in range(B):
+        if not 0 <= nb[b] <= bi.shape[1]:
+            raise ValueError(f"n_blocks[{b}] = {nb[b]} outside [0, {bi.shape[1]}]")
+        pos = selected_positions(sl[b], bi[b, :nb[b]])
+        ids = pt[b, pos // page].astype(np.int64)
+        if np.any((ids < 0) | (ids >= num_pages)):
+            raise ValueError(f"sequence {b}: page id out of range")
+        sel.append(ids * page + pos % page)
+    lens = np.array([len(x) for x in sel], dtype=np.int32)
+    pages_of = [(n + page - 1) // page for n in lens]
+    max_p = max(1, max(pages_of))
+    tot = max(1, sum(pages_of))
+    gk = np.zeros((tot * page, D), dtype=np.uint16)
+    gv = np.zeros((tot * page, D), dtype=np.uint16)
+    gpt = np.zeros((B, max_p), dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        gk[nxt * page:nxt * page + lens[b]] = k_rows[sel[b]]
+        gv[nxt * page:nxt * page + lens[b]] = v_rows[sel[b]]
+        gpt[b, :pages_of[b]] = np.arange(nxt, nxt + pages_of[b])
+        nxt += pages_of[b]
+    return mfa_decode(q, gk.reshape(tot, page, D), gv.reshape(tot, page, D), gpt, lens, scale, threads=threads)
+
+
 def query_lowrank(x_bits, w_down_bits, gamma_bits, w_up_bits, eps):
     """MFA's low-rank query path in fp64.
 
