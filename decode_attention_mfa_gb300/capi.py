@@ -51,6 +51,7 @@ _SIGNATURES = {
     "mfa_query_lowrank_workspace_bytes": ([_I, _I], _Z),
     "mfa_query_lowrank": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _Z, _P], _I),
     "mfa_decode_attention_mtp": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_decode_attention_blocks": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_check_device_errors": ([_P, _I, _P], _I),
     "mfa_set_wait_budget_ns": ([_U64], None),
     "mfa_selftest_wait_timeout": ([_P, _U64, _P], _I),
@@ -180,6 +181,16 @@ def mfa_decode_attention_mtp(q, k_cache, v_cache, page_table, seq_lens, out, lse
                                            _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch, n_query,
                                            max_pages, num_pages, max_len_hint, _ptr(workspace),
                                            workspace_bytes, _stream(stream)))
+
+
+def mfa_decode_attention_blocks(q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks, max_blocks, out,
+                                lse, scale, batch, max_pages, num_pages, max_len_hint, workspace, workspace_bytes,
+                                stream=None):
+    """Decode over selected 8-token blocks: block_idx int32 [batch, max_blocks], n_blocks int32 [batch]."""
+    _check(load().mfa_decode_attention_blocks(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                              _ptr(seq_lens), _ptr(block_idx), _ptr(n_blocks), max_blocks, _ptr(out),
+                                              _ptr(lse), float(scale), batch, max_pages, num_pages, max_len_hint,
+                                              _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def mfa_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse, scale,

@@ -320,6 +320,43 @@ struct PageIds {
   }
 };
 
+// Block gather: cache rows of the virtual blocks of one sequence (the
+// selected blocks in the caller's order, then the block of the last token).
+struct BlockRows {
+  const int32_t* bidx;  // block_idx row of the sequence
+  const int32_t* prow;  // page_table row
+  int nb, cur, nvb;     // selected blocks, block of the last token, virtual blocks
+  __device__ void start(const Seg& s, const DecodeParams& p) {
+    const int len = clamp_len(__ldg(p.seq_lens + s.b), p.max_pages * kPageSize, nullptr);
+    nb = selected_blocks(len, p.n_blocks, s.b, p.max_blocks, nullptr);  // errors: recorded by the prefix
+    cur = (len - 1) >> 3;
+    nvb = len > 0 ? nb + 1 : 0;
+    bidx = p.block_idx + (size_t)s.b * p.max_blocks;
+    prow = p.page_table + (size_t)s.b * p.max_pages;
+  }
+  // Cache row (page id * 64 + row in the page) of virtual block i for lanes 0-15; -1 for the other
+  // lanes and past the last block. A block id outside [0, cur) or a bad page id is recorded as a page
+  // error and read as block 0 / page 0.
+  __device__ int row_of(int i, const DecodeParams& p, int lane) const {
+    if (lane >= 16 || i >= nvb) return -1;
+    int r = cur;
+    if (i < nb) {
+      r = __ldg(bidx + i);
+      if (r < 0 || r >= cur) {
+        raise_error(p.err, MFA_DEVERR_PAGE);
+        r = 0;
+      }
+    }
+    const int pos = 8 * r;
+    int id = __ldg(prow + (pos >> 6));
+    if (id < 0 || id >= p.num_pages) {
+      raise_error(p.err, MFA_DEVERR_PAGE);
+      id = 0;
+    }
+    return id * kPageSize + (pos & (kPageSize - 1));
+  }
+};
+
 // The whole producer warp runs this loop (uniform control flow); lane 0
 // issues the copies. Per piece: Q, then the chunks of K(0), then for each
 // tile t >= 1 those of K(t) and V(t-1), then V(T-1) -- the order in which the
@@ -415,6 +452,44 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   auto issue_v_tile = [&](int pa, int pb) -> bool {
     return issue_v(0, pa) && issue_v(1, pa) && (pb < 0 || (issue_v(0, pb) && issue_v(1, pb)));
   };
+  // Block gather (bf16, one query token): a tile is 16 blocks of 8 rows; lane j < 16 holds the cache
+  // row of block j of the tile (-1 past the end) and copies it itself (k/v maps with 8-row boxes; 8
+  // rows x 128 B is one swizzle atom, so the blocks land exactly where a whole page would).
+  // K dim block d of the tile:
+  auto issue_k_blocks = [&](int d, int row) -> bool {
+    uint32_t dst, bar;
+    if (!wait_slot(dst, bar)) return false;
+    const bool mine = lane < 16 && row >= 0;
+    const uint32_t n = __popc(__ballot_sync(0xffffffffu, mine));
+    if (lane == 0) mbar_arrive_expect_tx(bar, n * 1024u);
+    __syncwarp();
+    if (mine) tma_load_2d(dst + lane * 1024, kmap, d * 64, row, bar, pol_stream);
+    ++cc;
+    return true;
+  };
+  // V dims [hf*128, hf*128 + 128) of page i (blocks 8i .. 8i + 7) of the tile:
+  auto issue_v_blocks = [&](int hf, int i, int row) -> bool {
+    uint32_t dst, bar;
+    if (!wait_slot(dst, bar)) return false;
+    const bool mine = lane >= 8 * i && lane < 8 * i + 8 && row >= 0;
+    const uint32_t n = __popc(__ballot_sync(0xffffffffu, mine));
+    if (lane == 0) mbar_arrive_expect_tx(bar, n * 2048u);
+    __syncwarp();
+    if (mine) {
+      const uint32_t o = (uint32_t)(lane - 8 * i) * 1024u;
+      tma_load_2d(dst + o, vmap, hf * 128, row, bar, pol_stream);
+      tma_load_2d(dst + 8192 + o, vmap, hf * 128 + 64, row, bar, pol_stream);
+    }
+    ++cc;
+    return true;
+  };
+  auto issue_v_blocks_tile = [&](int row, bool two_pages) -> bool {
+    return issue_v_blocks(0, 0, row) && issue_v_blocks(1, 0, row) &&
+           (!two_pages || (issue_v_blocks(0, 1, row) && issue_v_blocks(1, 1, row)));
+  };
+  const bool gather = !kFp8 && !kMtp && p.block_idx != nullptr;
+  int pend_row = -1;  // gather: this lane's block row of the tile whose V is still to be issued
+  bool pend_two = false, pend_valid = false;
   int pend_a = -1, pend_b = -1;  // pages of the tile whose V is still to be issued (tile stream)
   uint32_t last_q_parity = 0, last_qb = 0;
   bool issued_q = false;
@@ -423,7 +498,9 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     PageIds ids;
     ids.row = p.page_table + (size_t)s.b * p.max_pages;
     ids.pg1 = s.pg1;
-    ids.start(s.pg0, p, lane);
+    if (!gather) ids.start(s.pg0, p, lane);
+    BlockRows blk;
+    if (gather) blk.start(s, p);
     // Q of this sequence; its buffer is free once every S MMA of the piece that
     // last used it is done (with two buffers the loads of this piece need not
     // wait for the previous piece to finish)
@@ -447,7 +524,19 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++seg_i;
     const int T = tiles_of(s);
     bool good = true;
-    if constexpr (C::kCrossPiece) {
+    if (C::kCrossPiece && gather) {
+      // the tile stream below, with blocks; the rows of tile t + 1 are looked up while tile t is issued
+      int row_next = blk.row_of(8 * s.pg0 + lane, p, lane);
+      for (int t = 0; good && t < T; ++t) {
+        const int row = row_next;
+        if (t + 1 < T) row_next = blk.row_of(8 * (s.pg0 + 2 * (t + 1)) + lane, p, lane);
+        for (int d = 0; good && d < 4; ++d) good = issue_k_blocks(d, row);
+        if (good && pend_valid) good = issue_v_blocks_tile(pend_row, pend_two);
+        pend_row = row;
+        pend_two = pages_in_tile(s, t) == 2;
+        pend_valid = true;
+      }
+    } else if constexpr (C::kCrossPiece) {
       // K(g), then V(g - 1) of the previous tile, which may belong to the
       // previous piece: the next piece's first K tile is not queued behind the
       // last V tile of the previous one
@@ -484,10 +573,12 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     }
     if (!good) {
       pend_a = -1;
+      pend_valid = false;
       break;
     }
   }
   if (C::kCrossPiece && pend_a >= 0) (void)issue_v_tile(pend_a, pend_b);
+  if (C::kCrossPiece && pend_valid) (void)issue_v_blocks_tile(pend_row, pend_two);
   // drain: every copy this warp issued must land before the CTA exits
   if (lane == 0) {
     for (uint32_t k = (cc > (uint32_t)kRing ? cc - kRing : 0); k < cc; ++k)
@@ -1283,7 +1374,8 @@ __global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads, 1)
   pdl_wait_prior_grid();    // the KV append (or previous step) must be complete before reading its results
   pdl_launch_dependents();  // the combine kernel may be scheduled now (its prologue reads seq_lens); it
                             // waits for this grid before it reads the partials
-  build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, p.err, p.piece_cost, s_len, s_cost);  // ends with a barrier
+  build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, p.err, p.piece_cost, s_len, s_cost, p.n_blocks,
+                    p.max_blocks);  // ends with a barrier
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long units = s_cost[p.B];  // total cost units

@@ -60,7 +60,8 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodePara
   __shared__ float s_lse[kH];
   __shared__ float4 s_acc[Sh::kSubsets > 1 ? kCombineThreads * Sh::kVec : 1];
   // seq_lens is final before the split kernel starts; the partials are not
-  build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, p.piece_cost, s_len, s_cost);
+  build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, p.piece_cost, s_len, s_cost, p.n_blocks,
+                    p.max_blocks);
   const int nq = p.n_query;
   const int b = blockIdx.y / nq, tq = blockIdx.y % nq;  // sequence, query token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

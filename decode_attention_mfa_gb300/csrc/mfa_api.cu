@@ -110,15 +110,15 @@ mfa_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return MFA_OK;
 }
 
-// 2-D bf16 tensor [rows][256] read in [64 rows x 64 columns] boxes with the
+// 2-D bf16 tensor [rows][256] read in [box_rows x 64 columns] boxes with the
 // 128-byte swizzle (128-byte box rows).
-mfa_status_t encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows) {
+mfa_status_t encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows = 64) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   mfa_status_t st = get_encoder(&enc);
   if (st != MFA_OK) return st;
   const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -258,7 +258,8 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
                            const float* v_scale, bool fp8, const int32_t* page_table, const int32_t* seq_lens,
                            void* out, float* lse, float scale, int batch, int max_pages, int num_pages,
                            int max_len_hint, void* workspace, size_t workspace_bytes, void* stream,
-                           int n_query = 1) {
+                           int n_query = 1, const int32_t* block_idx = nullptr, const int32_t* n_blocks = nullptr,
+                           int max_blocks = 0) {
   DeviceInfo info;
   mfa_status_t st = current_device(nullptr, &info);
   if (st != MFA_OK) return st;
@@ -272,6 +273,9 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse,
                                       scale, batch, max_pages, num_pages, workspace, plan, n_query);
   if (fp8) p.piece_cost = kPieceCostPagesFp8;
+  p.block_idx = block_idx;
+  p.n_blocks = n_blocks;
+  p.max_blocks = max_blocks;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (g_prof_start && (e = cudaEventRecordWithFlags(g_prof_start, s, cudaEventRecordExternal)) != cudaSuccess)
@@ -284,7 +288,9 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
       return st;
     e = launch_decode_split_tc_fp8(p, kmap, vmap, qmap, s);
   } else {
-    if ((st = encode_rows_bf16(&kmap, k_cache, rows)) != MFA_OK || (st = encode_rows_bf16(&vmap, v_cache, rows)) != MFA_OK)
+    const uint32_t box_rows = block_idx ? 8u : 64u;  // block gather: one 8-token block per box
+    if ((st = encode_rows_bf16(&kmap, k_cache, rows, box_rows)) != MFA_OK ||
+        (st = encode_rows_bf16(&vmap, v_cache, rows, box_rows)) != MFA_OK)
       return st;
     e = n_query == 2 ? launch_decode_split_tc_mtp(p, kmap, vmap, qmap, s) : launch_decode_split_tc(p, kmap, vmap, qmap, s);
   }
@@ -433,6 +439,20 @@ mfa_status_t mfa_decode_attention_mtp(const void* q, const void* k_cache, const 
   if (n_query < 1 || n_query > 2) return fail(MFA_ERR_INVALID_ARG, "n_query %d is not 1 or 2", n_query);
   return decode_common(q, k_cache, v_cache, nullptr, nullptr, false, page_table, seq_lens, out, lse, scale, batch,
                        max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, n_query);
+}
+
+mfa_status_t mfa_decode_attention_blocks(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* page_table, const int32_t* seq_lens, const int32_t* block_idx,
+                                         const int32_t* n_blocks, int max_blocks, void* out, float* lse, float scale,
+                                         int batch, int max_pages, int num_pages, int max_len_hint, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (!block_idx || !n_blocks) return fail(MFA_ERR_INVALID_ARG, "null block_idx or n_blocks");
+  if (!aligned(block_idx, 4) || !aligned(n_blocks, 4)) return fail(MFA_ERR_INVALID_ARG, "misaligned block lists");
+  if (max_blocks < 1 || (long long)max_blocks > (long long)max_pages * (kPageSize / 8))
+    return fail(MFA_ERR_INVALID_ARG, "max_blocks %d outside [1, 8 * max_pages]", max_blocks);
+  return decode_common(q, k_cache, v_cache, nullptr, nullptr, false, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, 1, block_idx,
+                       n_blocks, max_blocks);
 }
 
 mfa_status_t mfa_check_device_errors(void* workspace, int clear, void* stream) {

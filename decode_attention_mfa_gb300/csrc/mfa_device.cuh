@@ -47,13 +47,38 @@ __device__ __forceinline__ int clamp_len(int len, int cap_tokens, uint32_t* err)
 // The G CTAs split the C = s_cost[B] units into equal ranges and each works on
 // the pages whose positions fall in its range.
 //
-// Fill s_len[b] (clamped lengths) and s_cost[b] = sum_{c<b} cost(c) for
-// b <= B, using every thread of the block. s_cost has B + 1 entries.
+// Block gather: a sequence of length L > 0 holds c = floor((L - 1) / 8)
+// complete blocks before the one with its last token. With nb of them
+// selected (clamped to [0, min(c, max_blocks)], out of range recorded as a
+// capacity error) it is read as a virtual sequence of the selected blocks,
+// in the caller's order, followed by the L - 8c tokens of its last block.
+__device__ __forceinline__ int selected_blocks(int len, const int32_t* n_blocks, int b, int max_blocks,
+                                               uint32_t* err) {
+  if (len <= 0) return 0;
+  const int lim = min((len - 1) >> 3, max_blocks);
+  const int nb = __ldg(n_blocks + b);
+  if (nb < 0 || nb > lim) {
+    raise_error(err, MFA_DEVERR_CAPACITY);
+    return nb < 0 ? 0 : lim;
+  }
+  return nb;
+}
+__device__ __forceinline__ int virtual_len(int len, int nb) {
+  return len <= 0 ? 0 : 8 * nb + len - 8 * ((len - 1) >> 3);
+}
+
+// Fill s_len[b] (clamped lengths; virtual lengths under block gather, when
+// n_blocks is not null) and s_cost[b] = sum_{c<b} cost(c) for b <= B, using
+// every thread of the block. s_cost has B + 1 entries.
 // Must be called by all threads of the block; ends with __syncthreads().
 __device__ __forceinline__ void build_cost_prefix(const int32_t* __restrict__ seq_lens, int B,
                                                   int cap_tokens, uint32_t* err, int piece_cost, int* s_len,
-                                                  int* s_cost) {
-  for (int b = threadIdx.x; b < B; b += blockDim.x) s_len[b] = clamp_len(__ldg(seq_lens + b), cap_tokens, err);
+                                                  int* s_cost, const int32_t* n_blocks = nullptr,
+                                                  int max_blocks = 0) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int len = clamp_len(__ldg(seq_lens + b), cap_tokens, err);
+    s_len[b] = n_blocks ? virtual_len(len, selected_blocks(len, n_blocks, b, max_blocks, err)) : len;
+  }
   __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;

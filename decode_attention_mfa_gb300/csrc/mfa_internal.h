@@ -54,6 +54,12 @@ struct DecodeParams {
   const float* v_scale;
   const int32_t* page_table;
   const int32_t* seq_lens;
+  // Block gather (null block_idx: the whole sequence): sequence b attends to
+  // the 8-token blocks block_idx[b][0 .. n_blocks[b]) and to its own last block
+  // up to its last token; k/v tensor maps then use 8-row boxes.
+  const int32_t* block_idx;  // [B][max_blocks]
+  const int32_t* n_blocks;   // [B]
+  int max_blocks;
   uint16_t* out;           // [B][n_query][64][256] bf16 bits
   float* lse;              // [B][n_query][64]
   float* part_o;           // [slots][n_query][64][256]

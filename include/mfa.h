@@ -226,6 +226,36 @@ mfa_status_t mfa_decode_attention_mtp(const void* q, const void* k_cache, const 
                                       int batch, int n_query, int max_pages, int num_pages, int max_len_hint,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode attention over caller-selected 8-token blocks of a bf16 paged cache
+ * ("Step-5-Preview" page, sparse attention section: the query attends to the
+ * original K/V rows of the selected historical blocks and of its own block
+ * up to itself, with the softmax over that set; the selection -- the page's
+ * indexer and top-k -- is the caller's). For sequence b of length L > 0,
+ * block r covers positions 8r .. 8r + 7 and c = floor((L - 1) / 8) is the
+ * block of the last token; the query attends to
+ *     the blocks block_idx[b][0 .. n_blocks[b])   (each in [0, c), distinct)
+ *     and positions 8c .. L - 1,
+ * i.e. to J_b = {8r + i} U {8c, .., L - 1}, out = softmax(q K_J^T * scale) V_J
+ * and lse as in mfa_decode_attention (L = 0: out = 0, lse = -inf).
+ *   block_idx: [device] int32 [batch][max_blocks]; entries past n_blocks[b]
+ *              are not read. The order is free; a block listed twice is
+ *              attended twice (the caller passes a set).
+ *   n_blocks:  [device] int32 [batch], in [0, min(c, max_blocks)]
+ *   max_len_hint: expected maximum of 8 * n_blocks[b] + 8 (the attended
+ *              tokens); it sizes the grid and the workspace
+ *              (mfa_decode_workspace_bytes(batch, max_len_hint)).
+ * q, caches, page_table, seq_lens, out, lse as in mfa_decode_attention.
+ * Device errors: MFA_DEVERR_PAGE also for a block id outside [0, c) (read as
+ * block 0), MFA_DEVERR_CAPACITY for n_blocks[b] outside its range (clamped).
+ * Host errors: MFA_ERR_INVALID_ARG also for null or misaligned block lists,
+ * max_blocks < 1 or above 8 * max_pages. */
+mfa_status_t mfa_decode_attention_blocks(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* page_table, const int32_t* seq_lens,
+                                         const int32_t* block_idx, const int32_t* n_blocks, int max_blocks,
+                                         void* out, float* lse, float scale,
+                                         int batch, int max_pages, int num_pages, int max_len_hint,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* Allocation-free variant of mfa_decode_attention (bf16 cache). The paper
  * has no counterpart: it exists for callers that cannot give the library a
  * workspace -- a plugin or foreign-function host that passes only tensors it
