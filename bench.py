@@ -195,7 +195,12 @@ def run_ours(args, rank, world, local):
     B = int(lens0.size)
     total_steps = args.warmup + args.steps * (1 if args.no_e2e else 2) + 2
     total_steps += max(2, min(args.steps, 512))  # the region that times the split kernel alone
-    R = args.copies if args.copies > 0 else choose_copies(w, lens0, total_steps)
+    blocks = w.select_blocks > 0
+    if blocks:  # block gather: the caller's selection, the same every step
+        bidx_h, nblk_h = wl.draw_blocks(lens0, w.select_blocks, [w.seed + 1000 * rank])
+    # L2 sizing by the rows a step reads (block gather: the selected ones)
+    R = args.copies if args.copies > 0 else choose_copies(
+        w, acc.blocks_attended(lens0, nblk_h) if blocks else lens0, total_steps)
     headroom = math.ceil(total_steps / R) + 2
     # inputs: seeded on the host, one copy moved to HBM, cloned R times there
     wr = wl.Workload(w.name, w.batch, w.lengths, w.kv_dtype, w.permute_pages, 0, w.seed + 1000 * rank,
@@ -207,7 +212,7 @@ def run_ours(args, rank, world, local):
     page_table = torch.from_numpy(case.page_table).to(dev)
     fp8 = w.kv_dtype == "fp8"
     stream = torch.cuda.Stream(device=dev)
-    ws_hint = int(lens0.max()) + headroom
+    ws_hint = int(acc.blocks_attended(lens0, nblk_h).max()) if blocks else int(lens0.max()) + headroom
     ws_bytes = (capi.mfa_decode_mtp_workspace_bytes(B, nq, ws_hint) if nq > 1
                 else capi.mfa_decode_workspace_bytes(B, ws_hint))
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -243,6 +248,9 @@ def run_ours(args, rank, world, local):
             q1 = case.q
         q = q1.to(dev).unsqueeze(0).repeat(R, *([1] * q1.dim())).contiguous()
         newkv = wl.draw_rows(2 * B, wl.HEAD_DIM, [w.seed, rank], 11).view(2, B, 1, wl.HEAD_DIM).to(dev)
+        if blocks:
+            block_idx = torch.from_numpy(bidx_h).to(dev)
+            n_blocks = torch.from_numpy(nblk_h).to(dev)
         qshape = (B, nq) if nq > 1 else (B,)
         out = torch.empty(qshape + (wl.HEADS, wl.HEAD_DIM), dtype=torch.bfloat16, device=dev)
         lse = torch.empty(qshape + (wl.HEADS,), dtype=torch.float32, device=dev)
@@ -269,7 +277,11 @@ def run_ours(args, rank, world, local):
             if app:
                 capi.mfa_kv_append(kn, vn, 1, k_caches[r], v_caches[r], page_table, sl, B, max_pages, num_pages,
                                    workspace, stream)
-            if nq > 1:
+            if blocks:
+                capi.mfa_decode_attention_blocks(qq, k_caches[r], v_caches[r], page_table, sl, block_idx, n_blocks,
+                                                 block_idx.shape[1], out, lse, wl.SCALE, B, max_pages, num_pages,
+                                                 ws_hint, workspace, ws_bytes, stream)
+            elif nq > 1:
                 capi.mfa_decode_attention_mtp(qq, k_caches[r], v_caches[r], page_table, sl, out, lse, wl.SCALE, B,
                                               nq, max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
             else:
@@ -280,6 +292,11 @@ def run_ours(args, rank, world, local):
         if app:
             host_len[r] += 1
         L = host_len[r].copy()
+        if blocks:  # the split kernel reads everything but the outputs
+            sb = acc.decode_blocks_step_bytes(L, nblk_h, w.kv_dtype)
+            step_bytes.append(sb)
+            split_bytes.append(sb - B * wl.HEADS * (wl.HEAD_DIM * 2 + 4))
+            return acc.blocks_attended(L, nblk_h)
         step_bytes.append(acc.decode_step_bytes(L, w.kv_dtype, appended_tokens=1 if app else 0, n_query=nq))
         split_bytes.append(int(L.sum()) * acc.kv_bytes_per_token(w.kv_dtype) + nq * B * wl.HEADS * wl.HEAD_DIM * 2
                            + int(((L + 63) // 64).sum()) * 4 + B * 4)
@@ -410,7 +427,8 @@ def run_ours(args, rank, world, local):
                    "mean_attended_len": mean_len,
                    "queries_per_sequence": nq,
                    "step": ("mfa_kv_append(1 token/seq) + " if app else "") +
-                           ("mfa_decode_attention_mtp" if nq > 1 else "mfa_decode_attention") +
+                           ("mfa_decode_attention_blocks" if blocks else
+                            "mfa_decode_attention_mtp" if nq > 1 else "mfa_decode_attention") +
                            " (split + LSE combine)",
                    "l2": f"inputs rotate over {R} device-resident cache copies "
                          f"({R * float(lens0.sum()) * acc.kv_bytes_per_token(w.kv_dtype) / 1e9:.1f} GB >> 135 MB L2)",
@@ -493,13 +511,61 @@ class OracleSampler:
         return self.step_bytes * nrows / self.total_rows
 
 
+class BlockOracleSampler:
+    """The fp64 oracle of block-gather decode (gather of the selected rows, then
+    the fp64 decode) on the first n sequences of the workload, all heads; the
+    inputs of the largest sample are drawn once."""
+
+    def __init__(self, w: wl.Workload, lens, threads: int):
+        import oracle
+
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.threads = threads
+        self.lens = np.asarray(lens, dtype=np.int64)
+        self.bi, self.nb = wl.draw_blocks(self.lens, w.select_blocks, [w.seed])
+        self.total_rows = int(self.lens.size)  # sequences
+        self.inputs = None
+
+    def _prepare(self, n):
+        if self.inputs is None or self.inputs[0] < n:
+            case = wl.make_case(self.w, lengths=self.lens[:n], headroom_tokens=0)
+            kc = wl.bits(wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
+            vc = wl.bits(wl.scatter_rows(case.v_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
+            self.inputs = (n, wl.bits(case.q), kc, vc, case.page_table)
+        return self.inputs
+
+    def run(self, n: int) -> float:
+        _, q, kc, vc, pt = self._prepare(n)
+        t = time.perf_counter()
+        self.oracle.mfa_decode_blocks(q[:n], kc, vc, pt[:n], self.lens[:n].astype(np.int32), self.bi[:n],
+                                      self.nb[:n], wl.SCALE, threads=self.threads)
+        return time.perf_counter() - t
+
+    def rows_for(self, budget_s: float) -> int:
+        dt = self.run(1)
+        return int(min(self.total_rows, max(1, budget_s / max(dt, 1e-6))))
+
+    def bytes_of(self, n: int) -> float:
+        return float(acc.decode_blocks_step_bytes(self.lens[:n], self.nb[:n], self.w.kv_dtype))
+
+
+def make_sampler(w: wl.Workload, lens, threads):
+    return BlockOracleSampler(w, lens, threads) if w.select_blocks else OracleSampler(w, lens, threads)
+
+
+def sample_unit(w: wl.Workload) -> str:
+    return "sequences (all 64 heads)" if w.select_blocks else "(sequence, head) rows"
+
+
 def cpu_baseline(w: wl.Workload, lens_attended, budget_s=12.0):
     threads = len(os.sched_getaffinity(0))
-    sampler = OracleSampler(w, lens_attended, threads)
+    sampler = make_sampler(w, lens_attended, threads)
     rows = sampler.rows_for(budget_s)
     dt = sampler.run(rows)
     return {"value": sampler.bytes_of(rows) / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{rows} of {sampler.total_rows} (sequence, head) rows of one {w.name} step "
+            "sample": f"{rows} of {sampler.total_rows} {sample_unit(w)} of one {w.name} step "
                       f"(fp64 C oracle, {threads} OpenMP threads, {dt:.2f} s)"}
 
 
@@ -525,13 +591,13 @@ def run_reference(args):
     w = wl.WORKLOADS[args.workload]
     lens = first_attended(w)   # lengths attended in the first step of our arm
     threads = len(os.sched_getaffinity(0))
-    sampler = OracleSampler(w, lens, threads)
+    sampler = make_sampler(w, lens, threads)
     rows = sampler.rows_for(max(0.05, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         sampler.run(rows)
     secs = sum(sampler.run(rows) for _ in range(args.steps))
     value = sampler.bytes_of(rows) * args.steps / secs / 1e12
-    sample = (f"{rows} of {sampler.total_rows} (sequence, head) rows per step of {w.name} "
+    sample = (f"{rows} of {sampler.total_rows} {sample_unit(w)} per step of {w.name} "
               f"(fp64 C oracle, {threads} OpenMP threads)")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,

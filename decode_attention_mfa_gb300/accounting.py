@@ -59,6 +59,29 @@ def decode_step_bytes(lengths_attended, kv_dtype: str, appended_tokens: int = 0,
     return kv + q + out + table + app
 
 
+def blocks_attended(seq_lens, n_blocks) -> np.ndarray:
+    """Tokens a block-gather decode attends per sequence: 8 per selected block
+    plus the last block up to the last token (none for an empty sequence)."""
+    L = np.asarray(seq_lens, dtype=np.int64)
+    nb = np.asarray(n_blocks, dtype=np.int64)
+    return np.where(L > 0, 8 * nb + L - 8 * ((L - 1) // 8), 0)
+
+
+def decode_blocks_step_bytes(seq_lens, n_blocks, kv_dtype: str = "bf16") -> int:
+    """Algorithmic HBM bytes of one block-gather decode step: the K/V rows of
+    the attended tokens, queries, outputs and LSE, one page-table entry per
+    attended block, the selected block ids, and the per-sequence length and
+    block count."""
+    att = blocks_attended(seq_lens, n_blocks)
+    B = int(att.size)
+    nb = np.asarray(n_blocks, dtype=np.int64)
+    kv = int(att.sum()) * kv_bytes_per_token(kv_dtype)
+    q = B * HEADS * HEAD_DIM * 2
+    out = B * HEADS * HEAD_DIM * 2 + B * HEADS * 4
+    blocks = int(np.where(att > 0, nb + 1, 0).sum()) * 4 + int(nb.sum()) * 4
+    return kv + q + out + blocks + B * 8
+
+
 def decode_step_flops(lengths_attended, n_query: int = 1) -> int:
     """FLOPs of one decode step; query token t of n_query sees L - n_query + 1 + t tokens."""
     lens = np.asarray(lengths_attended, dtype=np.int64)

@@ -320,35 +320,49 @@ struct PageIds {
   }
 };
 
-// Block gather: cache rows of the virtual blocks of one sequence (the
+// Block gather: cache rows of the virtual blocks of one sequence piece (the
 // selected blocks in the caller's order, then the block of the last token).
+// Lane j < 16 looks up block j of each 16-block tile in three steps -- the
+// block id, then its page id, then the row -- each a tile apart, so that the
+// two dependent loads of a tile are in flight while earlier tiles are issued.
+// A block id outside [0, cur) or a bad page id is recorded as a page error and
+// read as block 0 / page 0.
 struct BlockRows {
   const int32_t* bidx;  // block_idx row of the sequence
   const int32_t* prow;  // page_table row
   int nb, cur, nvb;     // selected blocks, block of the last token, virtual blocks
+  int vb0;              // first virtual block of the piece
   __device__ void start(const Seg& s, const DecodeParams& p) {
     const int len = clamp_len(__ldg(p.seq_lens + s.b), p.max_pages * kPageSize, nullptr);
     nb = selected_blocks(len, p.n_blocks, s.b, p.max_blocks, nullptr);  // errors: recorded by the prefix
     cur = (len - 1) >> 3;
     nvb = len > 0 ? nb + 1 : 0;
+    vb0 = 8 * s.pg0;
     bidx = p.block_idx + (size_t)s.b * p.max_blocks;
     prow = p.page_table + (size_t)s.b * p.max_pages;
   }
-  // Cache row (page id * 64 + row in the page) of virtual block i for lanes 0-15; -1 for the other
-  // lanes and past the last block. A block id outside [0, cur) or a bad page id is recorded as a page
-  // error and read as block 0 / page 0.
-  __device__ int row_of(int i, const DecodeParams& p, int lane) const {
-    if (lane >= 16 || i >= nvb) return -1;
-    int r = cur;
-    if (i < nb) {
-      r = __ldg(bidx + i);
-      if (r < 0 || r >= cur) {
-        raise_error(p.err, MFA_DEVERR_PAGE);
-        r = 0;
-      }
+  __device__ bool has(int t, int lane) const { return lane < 16 && vb0 + 16 * t + lane < nvb; }
+  // step 1 for tile t: the block id (a load for a selected block)
+  __device__ int block_id(int t, int lane) const {
+    const int i = vb0 + 16 * t + lane;
+    return has(t, lane) ? (i < nb ? __ldg(bidx + i) : cur) : 0;
+  }
+  // step 2: the block's first position (returned in pos, -1 without a block) and a load of its page id
+  __device__ int page_id(int t, int lane, int r, int& pos, const DecodeParams& p) const {
+    if (!has(t, lane)) {
+      pos = -1;
+      return 0;
     }
-    const int pos = 8 * r;
-    int id = __ldg(prow + (pos >> 6));
+    if (vb0 + 16 * t + lane < nb && (r < 0 || r >= cur)) {
+      raise_error(p.err, MFA_DEVERR_PAGE);
+      r = 0;
+    }
+    pos = 8 * r;
+    return __ldg(prow + (pos >> 6));
+  }
+  // step 3: the cache row (page id * 64 + row in the page), -1 without a block
+  __device__ int row(int id, int pos, const DecodeParams& p) const {
+    if (pos < 0) return -1;
     if (id < 0 || id >= p.num_pages) {
       raise_error(p.err, MFA_DEVERR_PAGE);
       id = 0;
@@ -453,39 +467,41 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     return issue_v(0, pa) && issue_v(1, pa) && (pb < 0 || (issue_v(0, pb) && issue_v(1, pb)));
   };
   // Block gather (bf16, one query token): a tile is 16 blocks of 8 rows; lane j < 16 holds the cache
-  // row of block j of the tile (-1 past the end) and copies it itself (k/v maps with 8-row boxes; 8
-  // rows x 128 B is one swizzle atom, so the blocks land exactly where a whole page would).
-  // K dim block d of the tile:
-  auto issue_k_blocks = [&](int d, int row) -> bool {
-    uint32_t dst, bar;
-    if (!wait_slot(dst, bar)) return false;
-    const bool mine = lane < 16 && row >= 0;
-    const uint32_t n = __popc(__ballot_sync(0xffffffffu, mine));
-    if (lane == 0) mbar_arrive_expect_tx(bar, n * 1024u);
-    __syncwarp();
-    if (mine) tma_load_2d(dst + lane * 1024, kmap, d * 64, row, bar, pol_stream);
-    ++cc;
-    return true;
+  // row of block j of the tile (-1 past the end) and copies it itself. The TMA unit spends about the
+  // same time on a copy whatever its size, so every copy takes a whole block's row range, and the
+  // chunks are pairs of adjacent ring slots (32 KB; the last slot of the ring is skipped so that pairs
+  // never wrap): a K pair holds dim blocks 2h, 2h + 1 of the tile, block j at 2 KB * j as two swizzle
+  // atoms [8 rows x 128 B] (dim block 2h first); a V pair holds one page, block j at 4 KB * j as its
+  // four dim blocks. Only the pair's first slot's barriers are used.
+  auto wait_pair = [&](uint32_t& dst, uint32_t& bar) -> bool {
+    if (cc % kRing == kRing - 1) ++cc;  // pairs start at even slots
+    const bool r = wait_slot(dst, bar);
+    if (r) cc += 2;
+    return r;
   };
-  // V dims [hf*128, hf*128 + 128) of page i (blocks 8i .. 8i + 7) of the tile:
-  auto issue_v_blocks = [&](int hf, int i, int row) -> bool {
+  auto issue_k_pair = [&](int h, int row) -> bool {
     uint32_t dst, bar;
-    if (!wait_slot(dst, bar)) return false;
-    const bool mine = lane >= 8 * i && lane < 8 * i + 8 && row >= 0;
+    if (!wait_pair(dst, bar)) return false;
+    const bool mine = lane < 16 && row >= 0;
     const uint32_t n = __popc(__ballot_sync(0xffffffffu, mine));
     if (lane == 0) mbar_arrive_expect_tx(bar, n * 2048u);
     __syncwarp();
-    if (mine) {
-      const uint32_t o = (uint32_t)(lane - 8 * i) * 1024u;
-      tma_load_2d(dst + o, vmap, hf * 128, row, bar, pol_stream);
-      tma_load_2d(dst + 8192 + o, vmap, hf * 128 + 64, row, bar, pol_stream);
-    }
-    ++cc;
+    if (mine) tma_load_3d(dst + lane * 2048, kmap, 0, row, 2 * h, bar, pol_stream);
+    return true;
+  };
+  // page i (blocks 8i .. 8i + 7) of the tile; a block past the end is read from above the top of the
+  // cache, which fills it with zeros (0 * NaN of a stale row would poison P.V)
+  auto issue_v_pair = [&](int i, int row) -> bool {
+    uint32_t dst, bar;
+    if (!wait_pair(dst, bar)) return false;
+    if (lane == 0) mbar_arrive_expect_tx(bar, 8u * 4096u);
+    __syncwarp();
+    if (lane >= 8 * i && lane < 8 * i + 8)
+      tma_load_3d(dst + (uint32_t)(lane - 8 * i) * 4096u, vmap, 0, row >= 0 ? row : -8, 0, bar, pol_stream);
     return true;
   };
   auto issue_v_blocks_tile = [&](int row, bool two_pages) -> bool {
-    return issue_v_blocks(0, 0, row) && issue_v_blocks(1, 0, row) &&
-           (!two_pages || (issue_v_blocks(0, 1, row) && issue_v_blocks(1, 1, row)));
+    return issue_v_pair(0, row) && (!two_pages || issue_v_pair(1, row));
   };
   const bool gather = !kFp8 && !kMtp && p.block_idx != nullptr;
   int pend_row = -1;  // gather: this lane's block row of the tile whose V is still to be issued
@@ -525,16 +541,23 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     const int T = tiles_of(s);
     bool good = true;
     if (C::kCrossPiece && gather) {
-      // the tile stream below, with blocks; the rows of tile t + 1 are looked up while tile t is issued
-      int row_next = blk.row_of(8 * s.pg0 + lane, p, lane);
+      // the tile stream below, with blocks: while tile t is issued, the page id of tile t + 1 and the
+      // block id of tile t + 2 are in flight
+      int pos0, pos1;
+      const int r0 = blk.block_id(0, lane), r1 = blk.block_id(1, lane);
+      const int id0 = blk.page_id(0, lane, r0, pos0, p);
+      int id1 = blk.page_id(1, lane, r1, pos1, p);
+      int r2 = blk.block_id(2, lane);
+      int row = blk.row(id0, pos0, p);
       for (int t = 0; good && t < T; ++t) {
-        const int row = row_next;
-        if (t + 1 < T) row_next = blk.row_of(8 * (s.pg0 + 2 * (t + 1)) + lane, p, lane);
-        for (int d = 0; good && d < 4; ++d) good = issue_k_blocks(d, row);
+        for (int h = 0; good && h < 2; ++h) good = issue_k_pair(h, row);
         if (good && pend_valid) good = issue_v_blocks_tile(pend_row, pend_two);
         pend_row = row;
         pend_two = pages_in_tile(s, t) == 2;
         pend_valid = true;
+        row = blk.row(id1, pos1, p);
+        id1 = blk.page_id(t + 2, lane, r2, pos1, p);
+        r2 = blk.block_id(t + 3, lane);
       }
     } else if constexpr (C::kCrossPiece) {
       // K(g), then V(g - 1) of the previous tile, which may belong to the
@@ -581,8 +604,11 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   if (C::kCrossPiece && pend_valid) (void)issue_v_blocks_tile(pend_row, pend_two);
   // drain: every copy this warp issued must land before the CTA exits
   if (lane == 0) {
-    for (uint32_t k = (cc > (uint32_t)kRing ? cc - kRing : 0); k < cc; ++k)
+    for (uint32_t k = (cc > (uint32_t)kRing ? cc - kRing : 0); k < cc; ++k) {
+      // block gather: only the first slot of a pair carries its copies (the last slot is never used)
+      if (gather && (((k % kRing) & 1) || k % kRing == kRing - 1)) continue;
       (void)mbar_wait(cx.bar(kRingFull + k % kRing), (k / kRing) & 1, cx.budget, nullptr, p.err);
+    }
     if constexpr (kFp8) {
       for (uint32_t k = (sc_cnt > (uint32_t)C::kScaleSlots ? sc_cnt - C::kScaleSlots : 0); k < sc_cnt; ++k)
         (void)mbar_wait(cx.bar(Bb::ScFull + k % C::kScaleSlots), (k / C::kScaleSlots) & 1, cx.budget, nullptr,
@@ -718,6 +744,14 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   // page, issues every MMA and the commits that track them. A warp whose
   // lanes diverge around each issue block pays for the reconvergence.
   auto wait_all = [&](int bar, uint32_t parity) -> bool { return cx.wait(bar, parity); };
+  // block gather: operand chunks are pairs of adjacent ring slots, in the producer's sequence
+  const bool gather = !kFp8 && !kMtp && p.block_idx != nullptr;
+  auto next_pair = [&](uint32_t& slot, uint32_t& ph) {
+    if (cc % C::kSlots == C::kSlots - 1) ++cc;
+    slot = cc % C::kSlots;
+    ph = (cc / C::kSlots) & 1;
+    cc += 2;
+  };
   auto do_s = [&](uint32_t qb) -> bool {
     const uint32_t buf = s_cnt & 1, n = s_cnt >> 1;
     if (!wait_all(Bb::SEmpty + buf, (n & 1) ^ 1)) return false;
@@ -742,6 +776,27 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         tc_commit(cx.bar(Bb::SFull + buf));
       }
       ++cc;
+      ++s_cnt;
+      return true;
+    } else if (gather) {
+      // K pair h: dim blocks 2h + e at + 1 KB * e, 8-row groups 2 KB apart
+      for (int h = 0; h < 2; ++h) {
+        uint32_t slot, ph;
+        next_pair(slot, ph);
+        if (!wait_all(Bb::Full + slot, ph)) return false;
+        tc_fence_after();
+        const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
+        for (int e = 0; e < 2; ++e) {
+          const int d = 2 * h + e;
+          const uint32_t b0 = cx.base + L.q + qb * C::kQ * kQBytes + d * C::kQ * 8192;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma(d_tmem, smem_desc_sw128(a0 + e * 1024 + kk * 32, 16, 2048), smem_desc_sw128(b0 + kk * 32, 16, 1024),
+                   idesc_s<kFp8, kMtp>(), (d | kk) != 0);
+        }
+        tc_commit(cx.bar(Bb::Empty + slot));
+      }
+      tc_commit(cx.bar(Bb::SFull + buf));
       ++s_cnt;
       return true;
     } else {
@@ -814,6 +869,35 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         }
       }
       vc += np;
+    } else if (gather) {
+      // V pair of page i: block j at 4 KB * j, dim block c at + 1 KB * c (64-dim halves 1 KB apart,
+      // 8-token groups 4 KB apart); blocks past the end arrive as zeros, so only the rows past the last
+      // token of a partial block need zeroing
+      for (int i = 0; i < np; ++i) {
+        const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);
+        uint32_t slot, ph;
+        next_pair(slot, ph);
+        if (!wait_all(Bb::Full + slot, ph)) return false;
+        const uint32_t a0 = cx.base + L.ring + slot * kSlotBytes;
+        const int nz = min(kPageSize, (nv + 7) & ~7);
+        if (nv < nz) {
+          for (int r = nv; r < nz; ++r)
+            for (int c = 0; c < 4; ++c)
+              for (int off = 0; off < 128; off += 16)
+                st_shared_v4(a0 + (r >> 3) * 4096 + c * 1024 + (r & 7) * 128 + off, make_uint4(0u, 0u, 0u, 0u));
+          fence_proxy_async_smem();
+        }
+        tc_fence_after();
+        const uint32_t bp = cx.base + L.p + buf * C::kQ * kPBytes + i * 8192;
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma(tmem + tmem_o<kFp8, kMtp>() + obuf * 128 + hf * C::kOHalfCols,
+                   smem_desc_sw128(a0 + hf * 2048 + kk * 8192, 1024, 4096), smem_desc_sw128(bp + kk * 2048, kPBytes, 1024),
+                   idesc_o<kFp8, kMtp>(), !(first_of_seg && i == 0 && kk == 0));
+        }
+        tc_commit(cx.bar(Bb::Empty + slot));
+      }
     } else {
     for (int i = 0; i < np; ++i) {
       const int nv = min(kPageSize, sg.len - (pga + i) * kPageSize);  // valid rows of this page

@@ -112,13 +112,13 @@ mfa_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 
 // 2-D bf16 tensor [rows][256] read in [box_rows x 64 columns] boxes with the
 // 128-byte swizzle (128-byte box rows).
-mfa_status_t encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows = 64) {
+mfa_status_t encode_rows_bf16(CUtensorMap* map, const void* base, uint64_t rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   mfa_status_t st = get_encoder(&enc);
   if (st != MFA_OK) return st;
   const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t box[2] = {64, 64};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -141,6 +141,26 @@ mfa_status_t encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, u
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MFA_OK;
+}
+
+// Block gather: the bf16 cache [rows][256] viewed as 3-D -- x = 64 columns of
+// a 128-byte column block, y = row (512-byte stride), z = column block
+// (128-byte stride) -- read in boxes of 8 rows x `zbox` column blocks, which
+// land as zbox swizzle atoms of [8 rows x 128 B], one column block after the
+// other.
+mfa_status_t encode_blocks_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint32_t zbox) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  mfa_status_t st = get_encoder(&enc);
+  if (st != MFA_OK) return st;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kHeadDim / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, 128};
+  const cuuint32_t box[3] = {64, 8, zbox};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled (block view) failed (%d)", (int)r);
   return MFA_OK;
 }
 
@@ -288,10 +308,14 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
       return st;
     e = launch_decode_split_tc_fp8(p, kmap, vmap, qmap, s);
   } else {
-    const uint32_t box_rows = block_idx ? 8u : 64u;  // block gather: one 8-token block per box
-    if ((st = encode_rows_bf16(&kmap, k_cache, rows, box_rows)) != MFA_OK ||
-        (st = encode_rows_bf16(&vmap, v_cache, rows, box_rows)) != MFA_OK)
+    if (block_idx) {  // block gather: one 8-token block per box, K by column-block pairs, V whole
+      if ((st = encode_blocks_bf16(&kmap, k_cache, rows, 2)) != MFA_OK ||
+          (st = encode_blocks_bf16(&vmap, v_cache, rows, 4)) != MFA_OK)
+        return st;
+    } else if ((st = encode_rows_bf16(&kmap, k_cache, rows)) != MFA_OK ||
+               (st = encode_rows_bf16(&vmap, v_cache, rows)) != MFA_OK) {
       return st;
+    }
     e = n_query == 2 ? launch_decode_split_tc_mtp(p, kmap, vmap, qmap, s) : launch_decode_split_tc(p, kmap, vmap, qmap, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode split launch");

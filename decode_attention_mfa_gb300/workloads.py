@@ -41,6 +41,7 @@ class Workload:
     seed: int
     description: str = ""
     queries: int = 1        # query tokens per sequence (2: multi-token decode)
+    select_blocks: int = 0  # block gather: historical 8-token blocks selected per sequence (0: whole sequence)
 
 
 WORKLOADS = {
@@ -55,6 +56,10 @@ WORKLOADS = {
     "mtp4k": Workload("mtp4k", 32, ("fixed", 4096), "bf16", True, 0, 66,
                       "B=32, L=4096, two query tokens per sequence (multi-token decode), pages randomly permuted",
                       queries=2),
+    "blocks32k": Workload("blocks32k", 32, ("fixed", 32768), "bf16", True, 0, 77,
+                          "B=32, L=32768, 512 selected 8-token blocks plus the last block per sequence "
+                          "(4104 tokens attended, block-gather decode), pages randomly permuted",
+                          select_blocks=512),
     "long": Workload("long", 8, ("uniform", 65536, 131072), "bf16", True, 0, 55,
                      "B=8, L uniform in [65536, 131072], pages randomly permuted"),
 }
