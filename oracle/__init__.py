@@ -69,6 +69,12 @@ def _load():
         lib.oracle_e4m3_to_f64_array.restype = None
         lib.oracle_quantize_tokens_e4m3.argtypes = [P, i64, i32, P, P]
         lib.oracle_quantize_tokens_e4m3.restype = None
+        lib.oracle_e2m1_to_f64_array.argtypes = [P, i64, P]
+        lib.oracle_e2m1_to_f64_array.restype = None
+        lib.oracle_e2m1_from_f32_array.argtypes = [P, i64, P]
+        lib.oracle_e2m1_from_f32_array.restype = None
+        lib.oracle_quantize_tokens_e2m1.argtypes = [P, i64, i32, P, P]
+        lib.oracle_quantize_tokens_e2m1.restype = None
         lib.oracle_mfa_decode_rows.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
                                                i64, f64, P, P, i64, P, P, i32]
         lib.oracle_mfa_decode_rows.restype = i32
@@ -127,6 +133,60 @@ def quantize_tokens_e4m3(x_bf16_bits) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
+# ---------------------------------------------------------------- E2M1 codec (4-bit KV)
+def e2m1_decode(codes) -> np.ndarray:
+    """4-bit E2M1 codes (uint8 values 0..15) -> exact fp64 values (OCP MX FP4 definition)."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e2m1_to_f64_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """fp32 values -> nearest E2M1 code (0..15), ties to the even mantissa, saturating to +-6."""
+    xa = _c(x, np.float32)
+    out = np.empty(xa.shape, dtype=np.uint8)
+    _load().oracle_e2m1_from_f32_array(_ptr(xa), xa.size, _ptr(out))
+    return out
+
+
+def quantize_tokens_e2m1(x_bf16_bits) -> tuple[np.ndarray, np.ndarray]:
+    """Per-token 4-bit quantisation of bf16 rows [..., d] (uint16 bit patterns, d even).
+
+    "Step-3 is Large yet Affordable" (paper summary page), section 5.2: KV stored
+    in 4 bits, attention computed in 8 bits. Returns (packed uint8 [..., d/2],
+    scales float32 [...]): scale = absmax / 6 in fp32 (1 for an all-zero row),
+    code = E2M1(x / scale), element 2k in the low nibble of byte k."""
+    x = _c(x_bf16_bits, np.uint16)
+    d = x.shape[-1]
+    n = x.size // d
+    packed = np.empty(x.shape[:-1] + (d // 2,), dtype=np.uint8)
+    scales = np.empty(x.shape[:-1], dtype=np.float32)
+    _load().oracle_quantize_tokens_e2m1(_ptr(x), n, d, _ptr(packed), _ptr(scales))
+    return packed, scales
+
+
+def unpack_e2m1(packed) -> np.ndarray:
+    """Packed bytes [..., d/2] -> codes [..., d] (element 2k from the low nibble)."""
+    p = _c(packed, np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 15
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def _kv_format(cache, head_dim) -> int:
+    """0 bf16 (uint16 [..., D]), 1 E4M3 (uint8 [..., D]), 2 packed E2M1 (uint8 [..., D/2])."""
+    a = np.asarray(cache)
+    if a.dtype == np.uint16:
+        return 0
+    if a.dtype == np.uint8 and a.shape[-1] == head_dim:
+        return 1
+    if a.dtype == np.uint8 and 2 * a.shape[-1] == head_dim:
+        return 2
+    raise ValueError(f"cache of dtype {a.dtype} and row width {a.shape[-1]} matches no format for D = {head_dim}")
+
+
 def bf16_to_f64(bits) -> np.ndarray:
     """bf16 bit patterns -> exact fp64 values."""
     b = _c(bits, np.uint16).astype(np.uint32) << 16
@@ -139,16 +199,20 @@ def mfa_decode(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_scale
     """MFA decode attention over a paged KV cache, in fp64.
 
     q_bits     [B, H, D] uint16 (bf16 bits)
-    k_cache    [num_pages, page, D] uint16 (bf16 bits) or uint8 (E4M3 codes)
+    k_cache    [num_pages, page, D] uint16 (bf16 bits) or uint8 (E4M3 codes), or
+               [num_pages, page, D/2] uint8 (packed E2M1 codes, 4-bit KV)
     v_cache    same as k_cache
     page_table [B, max_pages] int32, seq_lens [B] int32
-    k_scale/v_scale [num_pages, page] float32 for an E4M3 cache
+    k_scale/v_scale [num_pages, page] float32 for an E4M3 or E2M1 cache
     rows       optional (b_idx, h_idx) int arrays: compute only those rows
     Returns (out, lse): out [B, H, D] (or [n_rows, D]) fp64, lse [B, H] (or [n_rows]).
     """
     q = _c(q_bits, np.uint16)
     B, H, D = q.shape
-    fp8 = np.asarray(k_cache).dtype == np.uint8
+    fmt = _kv_format(k_cache, D)
+    if _kv_format(v_cache, D) != fmt:
+        raise ValueError("k_cache and v_cache differ in format")
+    fp8 = fmt != 0
     kc = _c(k_cache, np.uint8 if fp8 else np.uint16)
     vc = _c(v_cache, np.uint8 if fp8 else np.uint16)
     num_pages, page_size = kc.shape[0], kc.shape[1]
@@ -163,7 +227,7 @@ def mfa_decode(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_scale
     if rows is None:
         out = np.empty((B, H, D), dtype=np.float64)
         lse = np.empty((B, H), dtype=np.float64)
-        st = lib.oracle_mfa_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), int(fp8),
+        st = lib.oracle_mfa_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), fmt,
                                    _ptr(pt), _ptr(sl), B, H, D, page_size, pt.shape[1], num_pages,
                                    float(scale), _ptr(out), _ptr(lse), int(threads))
     else:
@@ -171,7 +235,7 @@ def mfa_decode(q_bits, k_cache, v_cache, page_table, seq_lens, scale, *, k_scale
         rh = _c(rows[1], np.int32)
         out = np.empty((rb.size, D), dtype=np.float64)
         lse = np.empty((rb.size,), dtype=np.float64)
-        st = lib.oracle_mfa_decode_rows(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), int(fp8),
+        st = lib.oracle_mfa_decode_rows(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), fmt,
                                         _ptr(pt), _ptr(sl), B, H, D, page_size, pt.shape[1],
                                         num_pages, float(scale), _ptr(rb), _ptr(rh), rb.size,
                                         _ptr(out), _ptr(lse), int(threads))
@@ -309,20 +373,21 @@ def kv_append(k_new_bits, v_new_bits, k_cache, v_cache, page_table, seq_lens, *,
               v_scale=None):
     """Append n_new tokens per sequence to host copies of the cache, in place.
 
-    k_new_bits/v_new_bits: [B, n_new, D] uint16 (bf16 bits).  For an E4M3 cache
-    (uint8 k_cache/v_cache) the tokens are quantised per token; k_scale/v_scale
-    are updated in place.  seq_lens is incremented in place."""
+    k_new_bits/v_new_bits: [B, n_new, D] uint16 (bf16 bits).  For an E4M3 or a
+    packed E2M1 cache (uint8 k_cache/v_cache) the tokens are quantised per token;
+    k_scale/v_scale are updated in place.  seq_lens is incremented in place."""
     kn = _c(k_new_bits, np.uint16)
     vn = _c(v_new_bits, np.uint16)
     B, n_new, D = kn.shape
-    fp8 = k_cache.dtype == np.uint8
+    fmt = _kv_format(k_cache, D)
+    fp8 = fmt != 0
     for a in (k_cache, v_cache, page_table, seq_lens) + ((k_scale, v_scale) if fp8 else ()):
         if not a.flags.c_contiguous:
             raise ValueError("in-place arrays must be C-contiguous")
     num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
     st = _load().oracle_kv_append(_ptr(kn), _ptr(vn), n_new, _ptr(k_cache), _ptr(v_cache),
                                   _ptr(k_scale) if fp8 else None, _ptr(v_scale) if fp8 else None,
-                                  int(fp8), _ptr(page_table), _ptr(seq_lens), B, D, page_size,
+                                  fmt, _ptr(page_table), _ptr(seq_lens), B, D, page_size,
                                   page_table.shape[1], num_pages)
     if st != 0:
         raise ValueError(f"oracle append rejected the inputs (code {st})")

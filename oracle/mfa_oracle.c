@@ -28,12 +28,21 @@
  *   - E4M3 codes follow the OCP 8-bit floating point specification (OFP8),
  *     E4M3 format: 1 sign, 4 exponent (bias 7), 3 mantissa bits, no infinities,
  *     NaN = S.1111.111, largest finite magnitude 448.
+ *   - Same page, section 5.2: KV may be stored in 4 bits and the attention
+ *     computed in 8 bits. E2M1 codes follow the OCP Microscaling (MX)
+ *     specification's FP4 element format: 1 sign, 2 exponent (bias 1), 1
+ *     mantissa bit, no infinities or NaN, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - FP8 scale granularity: one fp32 scale per token, separately for K and V,
  *     s = absmax / 448 (fp32 division), code = RNE-to-E4M3(x / s) (fp32
  *     division) saturated to +-448; absmax == 0 gives s = 1 and all-zero codes.
  *   - The dequantised FP8 value is decode(code) * s, exact in fp64.
+ *   - 4-bit KV: one fp32 scale per token (K and V separately), s = absmax / 6,
+ *     code = nearest E2M1 value to x / s (ties to the even mantissa, saturating
+ *     to +-6, sign kept on zero), two codes per byte with element 2k in the low
+ *     nibble; the dequantised value is decode(code) * s. Every E2M1 value is an
+ *     E4M3 value, so "computing in 8 bits" loses nothing further.
  *   - A sequence with L_b == 0 yields out = 0 and lse = -inf.
  *   - Unused slots of a sequence's last page never contribute, whatever they hold.
  *
@@ -120,6 +129,65 @@ void oracle_e4m3_to_f64_array(const uint8_t* c, int64_t n, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_f64(c[i]);
 }
 
+/* OCP MX FP4 (E2M1) decode from the format definition: exponent field 0 is
+ * subnormal, m * 2^(1-1) * 2^-1; otherwise (1 + m/2) * 2^(e-1). */
+double oracle_e2m1_to_f64(uint8_t code) {
+  int sign = (code >> 3) & 1;
+  int e = (code >> 1) & 3;
+  int m = code & 1;
+  double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -mag : mag;
+}
+
+/* Nearest E2M1 code to x: the candidate magnitude closest to |x|, a tie going
+ * to the code whose mantissa bit is 0; beyond the largest value the code
+ * saturates at 6. The sign of x is kept (a negative x that rounds to zero
+ * gives code 8). */
+uint8_t oracle_e2m1_from_f32(float x) {
+  uint8_t sign = signbit(x) ? 8 : 0;
+  double a = fabs((double)x);
+  if (isnan(x)) return (uint8_t)(sign | 7);
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    double d = fabs(a - oracle_e2m1_to_f64((uint8_t)c));
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+void oracle_e2m1_to_f64_array(const uint8_t* c, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_to_f64(c[i]);
+}
+
+void oracle_e2m1_from_f32_array(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_from_f32(x[i]);
+}
+
+/* Per-token 4-bit quantisation of bf16 rows x[n_tokens][d] (d even): one fp32
+ * scale per row (absmax / 6), codes = E2M1(x / scale), packed two per byte,
+ * element 2k in the low nibble of byte k. */
+void oracle_quantize_tokens_e2m1(const uint16_t* x, int64_t n_tokens, int d, uint8_t* packed, float* scales) {
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const uint16_t* row = x + t * (int64_t)d;
+    float amax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+      float a = fabsf(bf16_to_f32(row[i]));
+      if (a > amax) amax = a;
+    }
+    float s = (amax > 0.0f) ? amax / 6.0f : 1.0f;
+    scales[t] = s;
+    for (int i = 0; i < d; i += 2) {
+      uint8_t lo = oracle_e2m1_from_f32(bf16_to_f32(row[i]) / s);
+      uint8_t hi = oracle_e2m1_from_f32(bf16_to_f32(row[i + 1]) / s);
+      packed[t * (int64_t)(d / 2) + i / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
 /* Per-token FP8 quantisation of bf16 rows x[n_tokens][d]: one fp32 scale per
  * row (absmax / 448), codes = E4M3(x / scale). */
 void oracle_quantize_tokens_e4m3(const uint16_t* x, int64_t n_tokens, int d,
@@ -140,10 +208,18 @@ void oracle_quantize_tokens_e4m3(const uint16_t* x, int64_t n_tokens, int d,
   }
 }
 
+/* Cache formats (the kv_fp8 argument): 0 bf16, 1 E4M3 + per-token scale,
+ * 2 packed E2M1 + per-token scale. */
+enum { KV_BF16 = 0, KV_E4M3 = 1, KV_E2M1 = 2 };
+
 /* Value of element i of the cache row at `slot` (slot = page * page_size + row),
- * as an exact fp64 number: the bf16 value, or decode(code) * scale for FP8. */
+ * as an exact fp64 number: the bf16 value, or decode(code) * scale. */
 static double cache_value(const void* cache, const float* scale_arr, int kv_fp8,
                           const double* e4m3_table, int64_t slot, int d, int i) {
+  if (kv_fp8 == KV_E2M1) {
+    const uint8_t byte = ((const uint8_t*)cache)[slot * (d / 2) + i / 2];
+    return oracle_e2m1_to_f64((i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15)) * (double)scale_arr[slot];
+  }
   if (kv_fp8) {
     const uint8_t* c = (const uint8_t*)cache;
     return e4m3_table[c[slot * d + i]] * (double)scale_arr[slot];
@@ -214,7 +290,8 @@ static int decode_row(const uint16_t* q, const void* k_cache, const void* v_cach
 /*
  * Decode attention for selected (b, h) rows over a paged cache.
  *   q          [B][H][D] bf16 bits
- *   k_cache    [num_pages][page_size][D]  bf16 bits, or E4M3 codes if kv_fp8
+ *   k_cache    [num_pages][page_size][D]  bf16 bits, or E4M3 codes if kv_fp8 == 1,
+ *              or [num_pages][page_size][D/2] packed E2M1 codes if kv_fp8 == 2
  *   v_cache    same layout as k_cache
  *   k_scale    [num_pages][page_size] fp32 (FP8 only, else may be NULL)
  *   v_scale    same (FP8 only)
@@ -283,7 +360,8 @@ int oracle_mfa_decode(const uint16_t* q, const void* k_cache, const void* v_cach
 /* The KV append of one decode step, on host copies: token t of sequence b goes
  * to position seq_lens[b] + t (page page_table[b][pos / page_size], row
  * pos % page_size); afterwards seq_lens[b] grows by n_new.  bf16 rows are
- * copied; with kv_fp8 they are quantised per token as above.
+ * copied; with kv_fp8 = 1 (E4M3) or 2 (packed E2M1) they are quantised per
+ * token as above.
  * k_new/v_new: [B][n_new][D] bf16 bits.  Returns 0 or a negative code. */
 int oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new, int n_new, void* k_cache,
                      void* v_cache, float* k_scale, float* v_scale, int kv_fp8,
@@ -312,7 +390,12 @@ int oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new, int n_new, vo
       int64_t slot = (int64_t)page * page_size + pos % page_size;
       const uint16_t* kr = k_new + ((int64_t)b * n_new + t) * D;
       const uint16_t* vr = v_new + ((int64_t)b * n_new + t) * D;
-      if (kv_fp8) {
+      if (kv_fp8 == KV_E2M1) {
+        oracle_quantize_tokens_e2m1(kr, 1, D, codes, &k_scale[slot]);
+        memcpy((uint8_t*)k_cache + slot * (D / 2), codes, (size_t)(D / 2));
+        oracle_quantize_tokens_e2m1(vr, 1, D, codes, &v_scale[slot]);
+        memcpy((uint8_t*)v_cache + slot * (D / 2), codes, (size_t)(D / 2));
+      } else if (kv_fp8) {
         oracle_quantize_tokens_e4m3(kr, 1, D, codes, &k_scale[slot]);
         memcpy((uint8_t*)k_cache + slot * D, codes, (size_t)D);
         oracle_quantize_tokens_e4m3(vr, 1, D, codes, &v_scale[slot]);

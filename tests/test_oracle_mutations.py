@@ -32,6 +32,11 @@ MUTANTS = {
                         "float s = (amax > 0.0f) ? amax / 240.0f : 1.0f;"),
     "append_no_increment": ("seq_lens[b] = (int32_t)(start + n_new);",
                             "seq_lens[b] = (int32_t)(start);"),
+    "e2m1_nibble_order": ("oracle_e2m1_to_f64((i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15))",
+                          "oracle_e2m1_to_f64((i & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4))"),
+    "e2m1_bias": ("ldexp(1.0 + 0.5 * m, e - 1);", "ldexp(1.0 + 0.5 * m, e - 2);"),
+    "e2m1_quant_wrong_max": ("? amax / 6.0f : 1.0f;", "? amax / 4.0f : 1.0f;"),
+    "e2m1_ties_to_odd": ("(d == best_d && (c & 1) == 0)", "(d == best_d && (c & 1) == 1)"),
 }
 
 
@@ -46,7 +51,7 @@ def _run_pins(tmp_path, source):
                MFA_ORACLE_EXPECT_DIR=str(pkg))
     return subprocess.run(
         [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-         os.path.join(ROOT, "tests", "test_oracle.py")],
+         os.path.join(ROOT, "tests", "test_oracle.py"), os.path.join(ROOT, "tests", "test_oracle_fp4.py")],
         env=env, cwd=str(tmp_path), capture_output=True, text=True, timeout=600)
 
 
