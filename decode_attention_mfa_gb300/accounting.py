@@ -29,6 +29,8 @@ def kv_bytes_per_token(kv_dtype: str, include_scales: bool = True, head_dim: int
         return 2 * head_dim * 2
     if kv_dtype == "fp8":
         return 2 * head_dim + (2 * 4 if include_scales else 0)
+    if kv_dtype == "fp4":  # two E2M1 codes per byte
+        return head_dim + (2 * 4 if include_scales else 0)
     raise ValueError(kv_dtype)
 
 

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "mfa_kv_append_fp8": ([_P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
     "mfa_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_kv_append_fp4": ([_P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "mfa_decode_attention_fp4": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P], _I),
     "mfa_decode_mtp_workspace_bytes": ([_I, _I, _I], _Z),
     "mfa_query_lowrank_workspace_bytes": ([_I, _I], _Z),
@@ -139,6 +141,25 @@ def mfa_kv_append_fp8(k_new, v_new, n_new, k_cache, v_cache, k_scale, v_scale, p
     _check(load().mfa_kv_append_fp8(_ptr(k_new), _ptr(v_new), n_new, _ptr(k_cache), _ptr(v_cache),
                                     _ptr(k_scale), _ptr(v_scale), _ptr(page_table), _ptr(seq_lens),
                                     batch, max_pages, num_pages, _ptr(workspace), _stream(stream)))
+
+
+def mfa_kv_append_fp4(k_new, v_new, n_new, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                      batch, max_pages, num_pages, workspace, stream=None):
+    """4-bit KV append: caches uint8 [num_pages, 64, 128] (packed E2M1), scales fp32 [num_pages, 64]."""
+    _check(load().mfa_kv_append_fp4(_ptr(k_new), _ptr(v_new), n_new, _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_scale), _ptr(v_scale), _ptr(page_table), _ptr(seq_lens),
+                                    batch, max_pages, num_pages, _ptr(workspace), _stream(stream)))
+
+
+def mfa_decode_attention_fp4(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse, scale,
+                             batch, max_pages, num_pages, max_len_hint, workspace, workspace_bytes,
+                             stream=None):
+    """Decode attention over a 4-bit (packed E2M1 + per-token scale) cache."""
+    _check(load().mfa_decode_attention_fp4(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                           _ptr(v_scale), _ptr(page_table), _ptr(seq_lens), _ptr(out),
+                                           _ptr(lse), float(scale), batch, max_pages, num_pages,
+                                           max_len_hint, _ptr(workspace), workspace_bytes,
+                                           _stream(stream)))
 
 
 def mfa_decode_attention(q, k_cache, v_cache, page_table, seq_lens, out, lse, scale, batch, max_pages,

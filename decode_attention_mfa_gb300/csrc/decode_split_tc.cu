@@ -185,6 +185,8 @@ __host__ __device__ constexpr uint32_t idesc_o() {  // A = V^T (dim-major), B = 
 }
 // kind::f8f6f4, A and B E4M3 (format 0), both K-major, fp32 accumulate, M=128 N=128
 __host__ __device__ constexpr uint32_t idesc_s_e4m3() { return (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24); }
+// 4-bit cache: the A operand (the K tile, or the V page) is E2M1 (format 5) against E4M3 B
+constexpr uint32_t kIdescAE2M1 = 5u << 7;
 // kind::f8f6f4, A and B E4M3 (format 0), both dim/head-major, fp32 accumulate, M=128 N=128
 __host__ __device__ constexpr uint32_t idesc_o_e4m3() {
   return (1u << 4) | (1u << 15) | (1u << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
@@ -430,7 +432,8 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     uint32_t dst, bar;
     if (!wait_slot(dst, bar)) return false;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar, pb >= 0 ? 32768u : 16384u);
+      // a 4-bit page counts its packed bytes, half those of E4M3 (the gaps TMA leaves are not transferred)
+      mbar_arrive_expect_tx(bar, (pb >= 0 ? 32768u : 16384u) >> p.kv_fp4);
       tma_load_2d(dst, kmap, 0, pa * kPageSize, bar, pol_stream);
       tma_load_2d(dst + 16384, kmap, 128, pa * kPageSize, bar, pol_stream);
       if (pb >= 0) {
@@ -647,7 +650,7 @@ __device__ void producer_v_role(const DecodeParams& p, const CUtensorMap* vmap, 
       if (good && lane == 0) {
         const uint32_t dst = cx.base + L.stage + C::kKStages * kKTileBytes + (vc % C::kVStages) * kStageBytes;
         const uint32_t bar = cx.bar(Bb::StFull + slot);
-        mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
+        mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes >> p.kv_fp4);
         tma_load_2d(dst, vmap, 0, id * kPageSize, bar, pol_stream);
         tma_load_2d(dst + 8192, vmap, 128, id * kPageSize, bar, pol_stream);
       }
@@ -744,6 +747,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   // page, issues every MMA and the commits that track them. A warp whose
   // lanes diverge around each issue block pays for the reconvergence.
   auto wait_all = [&](int bar, uint32_t parity) -> bool { return cx.wait(bar, parity); };
+  const uint32_t idesc_a_fmt = p.kv_fp4 ? kIdescAE2M1 : 0u;  // E4M3 kernel on a 4-bit cache
   // block gather: operand chunks are pairs of adjacent ring slots, in the producer's sequence
   const bool gather = !kFp8 && !kMtp && p.block_idx != nullptr;
   auto next_pair = [&](uint32_t& slot, uint32_t& ph) {
@@ -771,7 +775,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             tc_mma_f8(d_tmem, smem_desc(ka + h * 16384 + ks * 32, 16, 1024, 2),
-                      smem_desc(qa + h * 16384 + ks * 32, 16, 1024, 2), idesc_s_e4m3(), (h | ks) != 0);
+                      smem_desc(qa + h * 16384 + ks * 32, 16, 1024, 2), idesc_s_e4m3() | idesc_a_fmt, (h | ks) != 0);
         tc_commit(cx.bar(Bb::StEmpty + kslot));
         tc_commit(cx.bar(Bb::SFull + buf));
       }
@@ -844,7 +848,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         const uint32_t vslot = C::kKStages + (vc + i) % C::kVStages;
         if (!wait_all(Bb::StFull + vslot, ((vc + i) / C::kVStages) & 1)) return false;
         vs[i] = cx.base + L.stage + C::kKStages * kKTileBytes + ((vc + i) % C::kVStages) * kStageBytes;
-        if (nv < kPageSize) {
+        if (nv < kPageSize && !p.kv_fp4) {  // E2M1 has no NaN code: a 4-bit page needs no zeroing
           // rows [nv, 64) of both boxes (whole 128 B rows): code 0x7F is NaN and 0 * NaN would poison P.V
           const int nbytes = (kPageSize - nv) * 128;
           for (int off = 0; off < nbytes; off += 16) {
@@ -863,7 +867,8 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks)
               tc_mma_f8(tmem + tmem_o<kFp8, kMtp>() + hf * 128, smem_desc(vs[i] + hf * 8192 + ks * 4096, 16, 1024, 2),
-                        smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3(), !(first_of_seg && i == 0 && ks == 0));
+                        smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3() | idesc_a_fmt,
+                        !(first_of_seg && i == 0 && ks == 0));
           // the V page's stage is free once these MMAs are done
           tc_commit(cx.bar(Bb::StEmpty + C::kKStages + (vc + i) % C::kVStages));
         }

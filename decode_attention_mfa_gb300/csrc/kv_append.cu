@@ -1,5 +1,6 @@
 // kv_append.cu -- in-place KV append into the paged cache (bf16 copy or
-// per-token E4M3 quantisation), advancing the device-owned length counter.
+// per-token E4M3 or E2M1 quantisation), advancing the device-owned length
+// counter.
 //
 // Semantics: "DuckLLM decode fixed-cost reduction" page, sections 7.2 (static
 // KV cache written at a fixed slot, never re-materialised) and 7.6 (the append
@@ -7,7 +8,9 @@
 // attention after an append includes the new token). FP8 storage: "Step-3 is
 // Large yet Affordable" (paper summary page), section 7 (8-bit KV, 512 bytes
 // per token per layer); one fp32 scale per token (absmax / 448) because the
-// pages do not fix the granularity.
+// pages do not fix the granularity. 4-bit storage: same page, section 5.2 (KV
+// kept in 4 bits, attention computed in 8 bits), as OCP MX FP4 (E2M1) codes
+// with one fp32 scale per token (absmax / 6), two codes per byte.
 #include <cuda_fp8.h>
 
 #include "mfa_device.cuh"
@@ -49,6 +52,41 @@ __device__ __forceinline__ void quantise_row_e4m3(const uint4 raw, uint8_t* __re
     packed[i] = word;
   }
   reinterpret_cast<uint2*>(dst)[lane] = make_uint2(packed[0], packed[1]);
+  if (lane == 0) *scale_out = s;
+}
+
+// Nearest E2M1 code to y, a tie going to the code with mantissa bit 0, beyond 6
+// saturating; the sign is kept (sign bit 3, also on zero). The candidate
+// magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6: the comparisons are against the
+// midpoints, each tie resolved toward the even code.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  const uint32_t c = a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u
+                   : a <= 2.5f ? 4u : a < 3.5f ? 5u : a <= 5.0f ? 6u : 7u;
+  return c | (signbit(y) ? 8u : 0u);
+}
+
+// Quantise one bf16 row to E2M1 with scale = absmax / 6 (1 for a zero row):
+// lane i packs elements [8i, 8i + 8) into 4 bytes, element 2k in the low nibble.
+__device__ __forceinline__ void quantise_row_e2m1(const uint4 raw, uint8_t* __restrict__ dst,
+                                                  float* __restrict__ scale_out, int lane) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = (amax > 0.0f) ? __fdiv_rn(amax, 6.0f) : 1.0f;
+  uint32_t word = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) word |= e2m1_code(__fdiv_rn(x[i], s)) << (4 * i);
+  reinterpret_cast<uint32_t*>(dst)[lane] = word;
   if (lane == 0) *scale_out = s;
 }
 
@@ -107,7 +145,11 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(AppendParams 
     const size_t slot = (size_t)page * kPageSize + (pos % kPageSize);
     const uint16_t* src = (is_v ? p.v_new : p.k_new) + ((size_t)b * p.n_new + t) * kHeadDim;
     const uint4 row = (i == first) ? first_row : __ldg(reinterpret_cast<const uint4*>(src) + lane);
-    if (p.fp8) {
+    if (p.fmt == kKvE2M1) {
+      uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + slot * (kHeadDim / 2);
+      float* sc = (is_v ? p.v_scale : p.k_scale) + slot;
+      quantise_row_e2m1(row, dst, sc, lane);
+    } else if (p.fmt == kKvE4M3) {
       uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + slot * kHeadDim;
       float* sc = (is_v ? p.v_scale : p.k_scale) + slot;
       quantise_row_e4m3(row, dst, sc, lane);

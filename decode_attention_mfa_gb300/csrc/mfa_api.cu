@@ -181,6 +181,26 @@ mfa_status_t encode_rows_e4m3(CUtensorMap* map, const void* base, uint64_t rows)
   return MFA_OK;
 }
 
+// 4-bit cache: 2-D [rows][256] E2M1 codes packed two per byte (128-byte rows)
+// read in [64 rows x 128 codes] boxes; TMA expands each 16 codes (8 bytes) to
+// 16 bytes of shared memory (8-byte gap), which is the operand layout of the
+// 4-bit formats in kind::f8f6f4 MMAs, with the 128-byte swizzle. The box then
+// has the shared-memory geometry of a [64 x 128] E4M3 box.
+mfa_status_t encode_rows_e2m1(CUtensorMap* map, const void* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  mfa_status_t st = get_encoder(&enc);
+  if (st != MFA_OK) return st;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim / 2};
+  const cuuint32_t box[2] = {128, 64};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box,
+                         elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled (4-bit) failed (%d)", (int)r);
+  return MFA_OK;
+}
+
 // ------------------------------------------------------------ common checks
 mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* page_table, const int32_t* seq_lens, const void* out,
@@ -235,13 +255,13 @@ DecodeParams make_decode_params(const void* q, const void* k_cache, const void* 
 }
 
 mfa_status_t append_common(const void* k_new, const void* v_new, int n_new, void* k_cache, void* v_cache,
-                           float* k_scale, float* v_scale, int fp8, const int32_t* page_table,
+                           float* k_scale, float* v_scale, int fmt, const int32_t* page_table,
                            int32_t* seq_lens, int batch, int max_pages, int num_pages, void* workspace,
                            void* stream) {
   if (!k_new || !v_new || !k_cache || !v_cache || !page_table || !seq_lens)
     return fail(MFA_ERR_INVALID_ARG, "null pointer argument");
-  if (fp8 && (!k_scale || !v_scale)) return fail(MFA_ERR_INVALID_ARG, "null scale pointer");
-  if (fp8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return fail(MFA_ERR_INVALID_ARG, "misaligned scales");
+  if (fmt != kKvBf16 && (!k_scale || !v_scale)) return fail(MFA_ERR_INVALID_ARG, "null scale pointer");
+  if (fmt != kKvBf16 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return fail(MFA_ERR_INVALID_ARG, "misaligned scales");
   if (batch < 1 || batch > kMaxBatch) return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxBatch);
   if (n_new < 0) return fail(MFA_ERR_INVALID_ARG, "negative n_new");
   if (max_pages < 1 || num_pages < 1) return fail(MFA_ERR_INVALID_ARG, "max_pages and num_pages must be >= 1");
@@ -268,7 +288,7 @@ mfa_status_t append_common(const void* k_new, const void* v_new, int n_new, void
   p.B = batch;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
-  p.fp8 = fp8;
+  p.fmt = fmt;
   const cudaError_t e = launch_kv_append(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   return MFA_OK;
@@ -279,7 +299,7 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
                            void* out, float* lse, float scale, int batch, int max_pages, int num_pages,
                            int max_len_hint, void* workspace, size_t workspace_bytes, void* stream,
                            int n_query = 1, const int32_t* block_idx = nullptr, const int32_t* n_blocks = nullptr,
-                           int max_blocks = 0) {
+                           int max_blocks = 0, int kv_fp4 = 0) {
   DeviceInfo info;
   mfa_status_t st = current_device(nullptr, &info);
   if (st != MFA_OK) return st;
@@ -293,6 +313,7 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse,
                                       scale, batch, max_pages, num_pages, workspace, plan, n_query);
   if (fp8) p.piece_cost = kPieceCostPagesFp8;
+  p.kv_fp4 = kv_fp4;
   p.block_idx = block_idx;
   p.n_blocks = n_blocks;
   p.max_blocks = max_blocks;
@@ -304,8 +325,14 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   const uint64_t rows = (uint64_t)num_pages * kPageSize;
   if ((st = encode_rows_bf16(&qmap, q, (uint64_t)batch * n_query * kHeads)) != MFA_OK) return st;
   if (fp8) {
-    if ((st = encode_rows_e4m3(&kmap, k_cache, rows)) != MFA_OK || (st = encode_rows_e4m3(&vmap, v_cache, rows)) != MFA_OK)
+    if (kv_fp4) {
+      if ((st = encode_rows_e2m1(&kmap, k_cache, rows)) != MFA_OK ||
+          (st = encode_rows_e2m1(&vmap, v_cache, rows)) != MFA_OK)
+        return st;
+    } else if ((st = encode_rows_e4m3(&kmap, k_cache, rows)) != MFA_OK ||
+               (st = encode_rows_e4m3(&vmap, v_cache, rows)) != MFA_OK) {
       return st;
+    }
     e = launch_decode_split_tc_fp8(p, kmap, vmap, qmap, s);
   } else {
     if (block_idx) {  // block gather: one 8-token block per box, K by column-block pairs, V whole
@@ -380,7 +407,16 @@ mfa_status_t mfa_kv_append(const void* k_new, const void* v_new, int n_new, void
 mfa_status_t mfa_kv_append_fp8(const void* k_new, const void* v_new, int n_new, void* k_cache, void* v_cache,
                                float* k_scale, float* v_scale, const int32_t* page_table, int32_t* seq_lens,
                                int batch, int max_pages, int num_pages, void* workspace, void* stream) {
-  return append_common(k_new, v_new, n_new, k_cache, v_cache, k_scale, v_scale, 1, page_table, seq_lens, batch,
+  return append_common(k_new, v_new, n_new, k_cache, v_cache, k_scale, v_scale, kKvE4M3, page_table, seq_lens, batch,
+                       max_pages, num_pages, workspace, stream);
+}
+
+mfa_status_t mfa_kv_append_fp4(const void* k_new, const void* v_new, int n_new, void* k_cache, void* v_cache,
+                               float* k_scale, float* v_scale, const int32_t* page_table, int32_t* seq_lens,
+                               int batch, int max_pages, int num_pages, void* workspace, void* stream) {
+  if (!aligned(k_cache, 32) || !aligned(v_cache, 32))
+    return fail(MFA_ERR_INVALID_ARG, "misaligned 4-bit cache (32 bytes needed)");
+  return append_common(k_new, v_new, n_new, k_cache, v_cache, k_scale, v_scale, kKvE2M1, page_table, seq_lens, batch,
                        max_pages, num_pages, workspace, stream);
 }
 
@@ -399,6 +435,18 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       size_t workspace_bytes, void* stream) {
   return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
                        max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream);
+}
+
+mfa_status_t mfa_decode_attention_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale, const int32_t* page_table,
+                                      const int32_t* seq_lens, void* out, float* lse, float scale, int batch,
+                                      int max_pages, int num_pages, int max_len_hint, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (!aligned(k_cache, 32) || !aligned(v_cache, 32))
+    return fail(MFA_ERR_INVALID_ARG, "misaligned 4-bit cache (32 bytes needed)");
+  return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, 1, nullptr, nullptr,
+                       0, 1);
 }
 
 // Query-path workspace: header | y fp32 [rank/128][batch][128] | h bf16 [batch][rank] | ssq fp32 [rank/128][batch]

@@ -32,6 +32,9 @@ constexpr int kPieceCostPages = 1;
 // piece is worth more pages.
 constexpr int kPieceCostPagesFp8 = 2;
 
+// Cache formats: bf16 rows, E4M3 codes + per-token scale, packed E2M1 codes + per-token scale.
+constexpr int kKvBf16 = 0, kKvE4M3 = 1, kKvE2M1 = 2;
+
 struct AppendParams {
   const uint16_t* k_new;  // [B][n_new][256] bf16 bits
   const uint16_t* v_new;
@@ -43,7 +46,7 @@ struct AppendParams {
   int32_t* seq_lens;
   uint32_t* err;
   int n_new, B, max_pages, num_pages;
-  int fp8;
+  int fmt;                // kKvBf16, kKvE4M3 or kKvE2M1
 };
 
 struct DecodeParams {
@@ -60,6 +63,7 @@ struct DecodeParams {
   const int32_t* block_idx;  // [B][max_blocks]
   const int32_t* n_blocks;   // [B]
   int max_blocks;
+  int kv_fp4;              // E4M3 kernel: the cache holds packed E2M1 codes ([num_pages][64][128] bytes)
   uint16_t* out;           // [B][n_query][64][256] bf16 bits
   float* lse;              // [B][n_query][64]
   float* part_o;           // [slots][n_query][64][256]

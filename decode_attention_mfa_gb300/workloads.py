@@ -35,7 +35,7 @@ class Workload:
     name: str
     batch: int
     lengths: tuple          # ("fixed", L) | ("list", (L0, L1, ...)) | ("uniform", lo, hi)
-    kv_dtype: str           # "bf16" | "fp8"
+    kv_dtype: str           # "bf16" | "fp8" (E4M3) | "fp4" (packed E2M1)
     permute_pages: bool     # False: sequence b owns a contiguous run of pages
     append_tokens: int      # tokens appended through the KV-append call before attention
     seed: int
@@ -53,6 +53,8 @@ WORKLOADS = {
                        "B=128, L uniform in [1024, 8192], one appended token per sequence"),
     "fp8": Workload("fp8", 64, ("fixed", 16384), "fp8", True, 0, 44,
                     "B=64, L=16384, E4M3 cache with per-token fp32 scales"),
+    "fp4": Workload("fp4", 64, ("fixed", 16384), "fp4", True, 0, 88,
+                    "B=64, L=16384, 4-bit KV: packed E2M1 codes with per-token fp32 scales"),
     "mtp4k": Workload("mtp4k", 32, ("fixed", 4096), "bf16", True, 0, 66,
                       "B=32, L=4096, two query tokens per sequence (multi-token decode), pages randomly permuted",
                       queries=2),

@@ -175,6 +175,34 @@ mfa_status_t mfa_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       int batch, int max_pages, int num_pages, int max_len_hint,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* 4-bit KV ("Step-3 is Large yet Affordable", section 5.2: KV stored in 4
+ * bits, the attention computed in 8 bits), read as OCP MX FP4 (E2M1) codes
+ * with one fp32 scale per token, K and V separately:
+ *   k_cache, v_cache: [device] uint8 [num_pages][64][128], 32-byte aligned:
+ *     the 256 codes of a row packed two per byte, element 2k in the low nibble;
+ *   k_scale, v_scale: [device] fp32 [num_pages][64].
+ * mfa_kv_append_fp4 quantises each new row with s = absmax / 6 (fp32 division;
+ * 1 for an all-zero row) and code = the nearest E2M1 value to x / s (fp32
+ * division), ties to the even mantissa, saturating to +-6, sign kept on zero.
+ * mfa_decode_attention_fp4 is the attention of mfa_decode_attention over the
+ * dequantised cache (decode(code) * s). Every E2M1 value is exact in E4M3:
+ * both products run as 8-bit tensor-core MMAs with the 4-bit codes as one
+ * operand, Q and P as in mfa_decode_attention_fp8. Arguments, workspace,
+ * lengths and errors as the _fp8 calls; MFA_ERR_INVALID_ARG also for caches
+ * that are not 32-byte aligned. */
+mfa_status_t mfa_kv_append_fp4(const void* k_new, const void* v_new, int n_new,
+                               void* k_cache, void* v_cache,
+                               float* k_scale, float* v_scale,
+                               const int32_t* page_table, int32_t* seq_lens,
+                               int batch, int max_pages, int num_pages,
+                               void* workspace, void* stream);
+mfa_status_t mfa_decode_attention_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* page_table, const int32_t* seq_lens,
+                                      void* out, float* lse, float scale,
+                                      int batch, int max_pages, int num_pages, int max_len_hint,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* MFA's low-rank query path ("Step-3 is Large yet Affordable", section 2 /
  * Table 1: the query is projected down from the model width to a low rank,
  * normalised, and projected up to 64 heads x 256; Step-3: 7168 -> 2048 ->

@@ -14,6 +14,9 @@ REL_L2 = 5e-3
 LSE_ABS = 1e-3
 
 E4M3_NAN = 0x7F
+E2M1_POISON = 0x77  # E2M1 has no NaN: unused 4-bit slots hold +6, +6, and their scales are NaN
+POISON = {"fp8": E4M3_NAN, "fp4": E2M1_POISON}
+ROW_BYTES = {"fp8": 256, "fp4": 128}
 
 
 class DeviceCache:
@@ -33,10 +36,10 @@ class DeviceCache:
             self.k_scale = self.v_scale = None
             self.seq_lens = torch.from_numpy(case.lengths0.astype(np.int32)).to(device)
         else:
-            # E4M3 cache: poisoned (NaN codes, NaN scales), then filled by the device append
-            self.k_cache = torch.full((self.num_pages, wl.PAGE_SIZE, wl.HEAD_DIM), E4M3_NAN, dtype=torch.uint8,
-                                      device=device)
-            self.v_cache = torch.full_like(self.k_cache, E4M3_NAN)
+            # E4M3 or packed E2M1 cache: poisoned (NaN codes / +6 codes, NaN scales), then filled by the device append
+            self.k_cache = torch.full((self.num_pages, wl.PAGE_SIZE, ROW_BYTES[kv_dtype]), POISON[kv_dtype],
+                                      dtype=torch.uint8, device=device)
+            self.v_cache = torch.full_like(self.k_cache, POISON[kv_dtype])
             self.k_scale = torch.full((self.num_pages, wl.PAGE_SIZE), float("nan"), dtype=torch.float32,
                                       device=device)
             self.v_scale = torch.full_like(self.k_scale, float("nan"))
@@ -47,17 +50,20 @@ class DeviceCache:
         self.ws_bytes = capi.mfa_decode_workspace_bytes(self.B, self.max_len_hint)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         capi.mfa_workspace_init(self.workspace, self.ws_bytes)
-        if kv_dtype == "fp8":
-            self.fill_fp8(case.k_rows, case.v_rows, case.lengths0)
+        if kv_dtype != "bf16":
+            self.fill_quantised(case.k_rows, case.v_rows, case.lengths0)
 
-    def fill_fp8(self, k_rows, v_rows, lengths):
+    def _append_fn(self):
+        return capi.mfa_kv_append_fp4 if self.kv_dtype == "fp4" else capi.mfa_kv_append_fp8
+
+    def fill_quantised(self, k_rows, v_rows, lengths):
         """Quantise the initial tokens on the device: one append call per sequence."""
         off = 0
         kd, vd = k_rows.to(self.q.device), v_rows.to(self.q.device)
         for b, n in enumerate(np.asarray(lengths)):
             n = int(n)
             if n:
-                capi.mfa_kv_append_fp8(
+                self._append_fn()(
                     kd[off:off + n], vd[off:off + n], n, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                     self.page_table.data_ptr() + 4 * b * self.max_pages, self.seq_lens.data_ptr() + 4 * b,
                     1, self.max_pages, self.num_pages, self.workspace)
@@ -71,9 +77,9 @@ class DeviceCache:
             capi.mfa_kv_append(kd, vd, n_new, self.k_cache, self.v_cache, self.page_table, self.seq_lens,
                                self.B, self.max_pages, self.num_pages, self.workspace)
         else:
-            capi.mfa_kv_append_fp8(kd, vd, n_new, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
-                                   self.page_table, self.seq_lens, self.B, self.max_pages, self.num_pages,
-                                   self.workspace)
+            self._append_fn()(kd, vd, n_new, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                              self.page_table, self.seq_lens, self.B, self.max_pages, self.num_pages,
+                              self.workspace)
 
     def attend(self, stream=None, max_len_hint=None):
         hint = self.max_len_hint if max_len_hint is None else max_len_hint
@@ -88,9 +94,10 @@ class DeviceCache:
                                       self.out, self.lse, wl.SCALE, self.B, self.max_pages, self.num_pages,
                                       hint, self.workspace, ws_bytes, stream)
         else:
-            capi.mfa_decode_attention_fp8(self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
-                                          self.page_table, self.seq_lens, self.out, self.lse, wl.SCALE, self.B,
-                                          self.max_pages, self.num_pages, hint, self.workspace, ws_bytes, stream)
+            fn = capi.mfa_decode_attention_fp4 if self.kv_dtype == "fp4" else capi.mfa_decode_attention_fp8
+            fn(self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.page_table, self.seq_lens,
+               self.out, self.lse, wl.SCALE, self.B, self.max_pages, self.num_pages, hint, self.workspace, ws_bytes,
+               stream)
 
     def check_errors(self):
         capi.mfa_check_device_errors(self.workspace, clear=True)
@@ -106,17 +113,18 @@ class DeviceCache:
 
 
 def oracle_caches(oracle, case: wl.Case, kv_dtype: str):
-    """The oracle's own host copy of the cache (bf16 bits, or E4M3 via its quantiser)."""
+    """The oracle's own host copy of the cache (bf16 bits, or E4M3 / packed E2M1 via its quantisers)."""
     n = case.num_pages
     if kv_dtype == "bf16":
         kc = wl.bits(wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, n)).copy()
         vc = wl.bits(wl.scatter_rows(case.v_rows, case.lengths0, case.page_table, n)).copy()
         return kc, vc, None, None, case.lengths0.astype(np.int32).copy()
-    kcodes, kscale = oracle.quantize_tokens_e4m3(wl.bits(case.k_rows))
-    vcodes, vscale = oracle.quantize_tokens_e4m3(wl.bits(case.v_rows))
+    quant = oracle.quantize_tokens_e2m1 if kv_dtype == "fp4" else oracle.quantize_tokens_e4m3
+    kcodes, kscale = quant(wl.bits(case.k_rows))
+    vcodes, vscale = quant(wl.bits(case.v_rows))
     slots = wl.slots_of(case.lengths0, case.page_table)
-    kc = np.full((n * wl.PAGE_SIZE, wl.HEAD_DIM), E4M3_NAN, np.uint8)
-    vc = np.full_like(kc, E4M3_NAN)
+    kc = np.full((n * wl.PAGE_SIZE, ROW_BYTES[kv_dtype]), POISON[kv_dtype], np.uint8)
+    vc = np.full_like(kc, POISON[kv_dtype])
     ks = np.full(n * wl.PAGE_SIZE, np.nan, np.float32)
     vs = np.full_like(ks, np.nan)
     kc[slots], vc[slots], ks[slots], vs[slots] = kcodes, vcodes, kscale, vscale

@@ -6,7 +6,7 @@ import torch
 
 from decode_attention_mfa_gb300 import capi
 from decode_attention_mfa_gb300 import workloads as wl
-from gpu_util import DeviceCache, oracle_caches, used_slots_equal
+from gpu_util import POISON, DeviceCache, oracle_caches, used_slots_equal
 
 pytestmark = pytest.mark.gpu
 
@@ -19,7 +19,7 @@ def _case(lengths, seed, headroom, kv="bf16"):
     return wl.make_case(w, lengths=lengths, headroom_tokens=headroom, spare_pages=2)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "fp4"])
 @pytest.mark.parametrize("n_new", [1, 70])
 def test_append_bit_exact(oracle_mod, kv, n_new):
     lengths = [0, 1, 63, 64, 200]
@@ -36,7 +36,7 @@ def test_append_bit_exact(oracle_mod, kv, n_new):
     assert np.array_equal(gsl, np.asarray(lengths) + n_new)
     assert used_slots_equal(gk, kc, sl, case.page_table)
     assert used_slots_equal(gv, vc, sl, case.page_table)
-    if kv == "fp8":
+    if kv != "bf16":
         assert used_slots_equal(gks[..., None], ks[..., None], sl, case.page_table)
         assert used_slots_equal(gvs[..., None], vs[..., None], sl, case.page_table)
     # slots past the new lengths are untouched (still poisoned)
@@ -46,7 +46,7 @@ def test_append_bit_exact(oracle_mod, kv, n_new):
     if kv == "bf16":
         assert np.all((flat & 0x7FFF) > 0x7F80)  # NaN bit patterns
     else:
-        assert np.all(flat == 0x7F)
+        assert np.all(flat == POISON[kv])
 
 
 def test_fp8_quantiser_special_rows(oracle_mod):
@@ -118,3 +118,31 @@ def test_append_rejects_bad_arguments():
     with pytest.raises(capi.MFAError) as ei:
         capi.mfa_kv_append(t, t, 1, t, t, t, t, 1, 1, 1, None)
     assert ei.value.status == 4
+
+
+def test_fp4_quantiser_special_rows(oracle_mod):
+    """All-zero rows, rows whose scaled values sit exactly on the E2M1 midpoints
+    (ties go to the even mantissa), tiny entries (negative zero codes) and
+    huge magnitudes quantise exactly like the oracle, packed low nibble first."""
+    rows = wl.draw_rows(6, wl.HEAD_DIM, [6], 9).float()
+    rows[0] = 0.0
+    ties = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0])  # absmax 6: scale 1
+    rows[1] = ties.repeat(wl.HEAD_DIM // 8) * torch.where(torch.arange(wl.HEAD_DIM) % 16 < 8, 1.0, -1.0)
+    rows[2] = rows[2] * 1e-4
+    rows[2, 0] = 3.0                      # most entries round to +-0 at scale 0.5
+    rows[3] = rows[3] * 1e30
+    rows[5] = -rows[5].abs()
+    rows = rows.to(torch.bfloat16)
+    case = _case([0], seed=4, headroom=6, kv="fp4")
+    dev = DeviceCache(case, "fp4")
+    dev.append(rows.view(1, 6, -1), rows.view(1, 6, -1))
+    dev.check_errors()
+    packed, scales = oracle_mod.quantize_tokens_e2m1(wl.bits(rows))
+    gk, _, gks, _, gsl = dev.host_caches()
+    assert gsl[0] == 6
+    slots = wl.slots_of([6], case.page_table)
+    assert np.array_equal(gk.reshape(-1, wl.HEAD_DIM // 2)[slots], packed)
+    assert np.array_equal(gks.reshape(-1)[slots].view(np.uint32), scales.view(np.uint32))
+    codes = oracle_mod.unpack_e2m1(packed)
+    assert scales[1] == 1.0 and np.array_equal(oracle_mod.e2m1_decode(codes[1, :8]), [0, 1, 1, 2, 2, 4, 4, 6])
+    assert np.any(codes[2] == 8)  # the sign survives on zero codes

@@ -46,7 +46,7 @@ def _oracle(oracle_mod, case, kv):
 
 
 @pytest.mark.parametrize("grid", ["planned", "one_cta"])
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "fp4"])
 @pytest.mark.parametrize("name", list(SMALL))
 def test_small_parity(oracle_mod, kv, name, grid):
     """`planned` uses the grid the planner picks (few tiles per CTA); `one_cta`
@@ -102,7 +102,7 @@ def test_page_placement_is_bitwise_invariant():
     assert torch.equal(da.out, db.out) and torch.equal(da.lse, db.lse)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "fp4"])
 def test_split_count_invariance(oracle_mod, kv):
     """Different grid sizes (one CTA, a few, one per SM) all match the oracle."""
     case = _case([3000, 17, 900], seed=9, kv=kv)
@@ -114,7 +114,7 @@ def test_split_count_invariance(oracle_mod, kv):
         compare(dev.out, dev.lse, out_ref, lse_ref, f"{kv}/hint={hint}")
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "fp4"])
 def test_query_heads_of_very_different_norms(oracle_mod, kv):
     """Head h of Q scaled by 2^-(h % 13) (a 4096x spread), four heads by 8
     (peaked softmax): the E4M3 path splits Q into E4M3 terms under one
@@ -130,7 +130,7 @@ def test_query_heads_of_very_different_norms(oracle_mod, kv):
     compare(dev.out, dev.lse, out_ref, lse_ref, f"{kv}/head-norm spread")
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "fp4"])
 def test_maximum_batch(oracle_mod, kv):
     """The largest batch the ABI accepts (MFA_MAX_BATCH sequences): the largest
     shared-memory layout of the split kernel and the widest combine grid.
@@ -190,7 +190,7 @@ def test_decode_rejects_bad_arguments():
     assert ei.value.status == 1
 
 
-@pytest.mark.parametrize("name", ["tiny", "ctx4k", "ragged", "fp8", "long"])
+@pytest.mark.parametrize("name", ["tiny", "ctx4k", "ragged", "fp8", "fp4", "long"])
 def test_named_workload_full_size(oracle_mod, name):
     """Every output of each named workload, as the benchmark launches it."""
     w = wl.WORKLOADS[name]
