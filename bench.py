@@ -227,7 +227,11 @@ def run_ours(args, rank, world, local):
     max_pages = case.page_table.shape[1]
     num_pages = case.num_pages
     page_table = torch.from_numpy(case.page_table).to(dev)
-    fp8 = w.kv_dtype == "fp8"
+    fp8 = w.kv_dtype in ("fp8", "fp4")  # quantised cache with per-token scales (E4M3, or packed E2M1)
+    fp4 = w.kv_dtype == "fp4"
+    row_bytes = wl.HEAD_DIM // 2 if fp4 else wl.HEAD_DIM
+    append_q = capi.mfa_kv_append_fp4 if fp4 else capi.mfa_kv_append_fp8
+    decode_q = capi.mfa_decode_attention_fp4 if fp4 else capi.mfa_decode_attention_fp8
     stream = torch.cuda.Stream(device=dev)
     ws_hint = int(acc.blocks_attended(lens0, nblk_h).max()) if blocks else int(lens0.max()) + headroom
     ws_bytes = (capi.mfa_decode_mtp_workspace_bytes(B, nq, ws_hint) if nq > 1
@@ -236,7 +240,7 @@ def run_ours(args, rank, world, local):
     capi.mfa_workspace_init(workspace, ws_bytes)
     with torch.cuda.stream(stream):
         if fp8:
-            k0 = torch.zeros((num_pages, wl.PAGE_SIZE, wl.HEAD_DIM), dtype=torch.uint8, device=dev)
+            k0 = torch.zeros((num_pages, wl.PAGE_SIZE, row_bytes), dtype=torch.uint8, device=dev)
             v0 = torch.zeros_like(k0)
             ks0 = torch.ones((num_pages, wl.PAGE_SIZE), dtype=torch.float32, device=dev)
             vs0 = torch.ones_like(ks0)
@@ -245,7 +249,7 @@ def run_ours(args, rank, world, local):
             off = 0
             for b, n in enumerate(lens0):   # quantise on the device, one append per sequence
                 n = int(n)
-                capi.mfa_kv_append_fp8(kr[off:off + n], vr[off:off + n], n, k0, v0, ks0, vs0,
+                append_q(kr[off:off + n], vr[off:off + n], n, k0, v0, ks0, vs0,
                                        page_table.data_ptr() + 4 * b * max_pages, sl_tmp.data_ptr() + 4 * b,
                                        1, max_pages, num_pages, workspace, stream)
                 off += n
@@ -285,9 +289,9 @@ def run_ours(args, rank, world, local):
         sl = seq_lens[r]
         if fp8:
             if app:
-                capi.mfa_kv_append_fp8(kn, vn, 1, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table,
+                append_q(kn, vn, 1, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table,
                                        sl, B, max_pages, num_pages, workspace, stream)
-            capi.mfa_decode_attention_fp8(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl,
+            decode_q(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl,
                                           out, lse, wl.SCALE, B, max_pages, num_pages, ws_hint, workspace,
                                           ws_bytes, stream)
         else:
@@ -437,7 +441,7 @@ def run_ours(args, rank, world, local):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_s * 1e3 / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if not fp8 else "e4m3",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1" if fp4 else "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), bf16)",
         "config": {"workload": w.name, "description": w.description, "batch": B, "heads": wl.HEADS,
                    "head_dim": wl.HEAD_DIM, "page_size": wl.PAGE_SIZE, "kv_dtype": w.kv_dtype,
@@ -481,16 +485,18 @@ class OracleSampler:
         self.w = w
         self.threads = threads
         case = wl.make_case(w, lengths=lens_attended, headroom_tokens=0)
-        if w.kv_dtype == "fp8":
-            kc_, ks_ = oracle.quantize_tokens_e4m3(wl.bits(case.k_rows))
-            vc_, vs_ = oracle.quantize_tokens_e4m3(wl.bits(case.v_rows))
+        if w.kv_dtype in ("fp8", "fp4"):
+            quant = oracle.quantize_tokens_e2m1 if w.kv_dtype == "fp4" else oracle.quantize_tokens_e4m3
+            width = wl.HEAD_DIM // 2 if w.kv_dtype == "fp4" else wl.HEAD_DIM
+            kc_, ks_ = quant(wl.bits(case.k_rows))
+            vc_, vs_ = quant(wl.bits(case.v_rows))
             slots = wl.slots_of(case.lengths0, case.page_table)
             n = case.num_pages * wl.PAGE_SIZE
-            kc = np.zeros((n, wl.HEAD_DIM), np.uint8); kc[slots] = kc_
-            vc = np.zeros((n, wl.HEAD_DIM), np.uint8); vc[slots] = vc_
+            kc = np.zeros((n, width), np.uint8); kc[slots] = kc_
+            vc = np.zeros((n, width), np.uint8); vc[slots] = vc_
             ks = np.ones(n, np.float32); ks[slots] = ks_
             vs = np.ones(n, np.float32); vs[slots] = vs_
-            self.kc, self.vc = kc.reshape(-1, wl.PAGE_SIZE, wl.HEAD_DIM), vc.reshape(-1, wl.PAGE_SIZE, wl.HEAD_DIM)
+            self.kc, self.vc = kc.reshape(-1, wl.PAGE_SIZE, width), vc.reshape(-1, wl.PAGE_SIZE, width)
             self.ks, self.vs = ks.reshape(-1, wl.PAGE_SIZE), vs.reshape(-1, wl.PAGE_SIZE)
         else:
             self.kc = wl.bits(wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
