@@ -658,7 +658,7 @@ def run_qproj(args, rank_id, world, local):
     gamma = (1.0 + 0.1 * torch.randn(R_, device=dev, generator=g)).to(torch.bfloat16)
     x = torch.randn(B, Dm, device=dev, generator=g).to(torch.bfloat16)
     q = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
-    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(B, R_)
+    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(B, R_, N)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     capi.mfa_workspace_init(ws, ws_bytes)
     stream = torch.cuda.Stream(device=dev)
@@ -742,7 +742,7 @@ def run_qproj(args, rank_id, world, local):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights, bf16)",
         "config": {"workload": "qproj", "description": "low-rank query path, Step-3 shape: x[32][7168] W_down[7168][2048] "
                    "-> RMSNorm -> W_up[2048][16384]", "batch": B, "d_model": Dm, "rank": R_, "n_out": N,
-                   "step": "mfa_query_lowrank (two tensor-core GEMMs + RMSNorm)",
+                   "step": "mfa_query_lowrank (two tensor-core GEMM launches + RMSNorm in their epilogues)",
                    "l2": f"weights rotate over {copies} device-resident copies "
                          f"({copies * 2 * (Dm * R_ + R_ * N) / 1e9:.2f} GB >> 135 MB L2)",
                    "parallelism": f"dp{world} (independent batch per GPU)"},

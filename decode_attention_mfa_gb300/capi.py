@@ -50,7 +50,7 @@ _SIGNATURES = {
     "mfa_decode_attention_fp4": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P], _I),
     "mfa_decode_mtp_workspace_bytes": ([_I, _I, _I], _Z),
-    "mfa_query_lowrank_workspace_bytes": ([_I, _I], _Z),
+    "mfa_query_lowrank_workspace_bytes": ([_I, _I, _I], _Z),
     "mfa_query_lowrank": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _Z, _P], _I),
     "mfa_decode_attention_mtp": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_blocks": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
@@ -174,8 +174,9 @@ MAX_QUERY_BATCH = 256
 MAX_QUERY_RANK = 16384
 
 
-def mfa_query_lowrank_workspace_bytes(batch: int, rank: int) -> int:
-    n = load().mfa_query_lowrank_workspace_bytes(batch, rank)
+def mfa_query_lowrank_workspace_bytes(batch: int, rank: int, n_out: int) -> int:
+    """Workspace bytes for query-path calls of up to `batch` rows."""
+    n = load().mfa_query_lowrank_workspace_bytes(batch, rank, n_out)
     if n == 0:
         raise MFAError(1, "bad arguments for mfa_query_lowrank_workspace_bytes")
     return n

@@ -449,11 +449,30 @@ mfa_status_t mfa_decode_attention_fp4(const void* q, const void* k_cache, const 
                        0, 1);
 }
 
-// Query-path workspace: header | y fp32 [rank/128][batch][128] | h bf16 [batch][rank] | ssq fp32 [rank/128][batch]
-size_t mfa_query_lowrank_workspace_bytes(int batch, int rank) {
-  if (batch < 1 || batch > kMaxQueryBatch || rank < 128 || rank > kMaxQueryRank) return 0;
-  const size_t ssq = ((size_t)(rank / 128) * batch * sizeof(float) + 255) & ~(size_t)255;
-  return kWsHeaderBytes + (size_t)batch * rank * (sizeof(float) + sizeof(uint16_t)) + ssq;
+// Query-path workspace for up to `cap` rows: header (arrival counters at bytes 128-255) |
+// y fp32 [cap * rank] | h bf16 [cap * rank] | ssq fp32 [rank/128 * cap].
+// A call with batch B <= cap uses the first B * rank floats of y, which it leaves zero, so y is zero on
+// entry whatever batch the previous call had.
+namespace {
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+struct QueryWs {
+  size_t y, h, ssq, total;
+};
+QueryWs query_ws(int cap, int rank) {
+  QueryWs w;
+  w.y = kWsHeaderBytes;
+  w.h = w.y + (size_t)cap * rank * sizeof(float);
+  w.ssq = w.h + round256((size_t)cap * rank * sizeof(uint16_t));
+  w.total = w.ssq + round256((size_t)(rank / 128) * cap * sizeof(float));
+  return w;
+}
+}  // namespace
+
+size_t mfa_query_lowrank_workspace_bytes(int batch, int rank, int n_out) {
+  if (batch < 1 || batch > kMaxQueryBatch || rank < 128 || rank > kMaxQueryRank || rank % 128 || n_out < 128 ||
+      n_out % 128)
+    return 0;
+  return query_ws(batch, rank).total;
 }
 
 mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* gamma, const void* w_up, void* q,
@@ -469,7 +488,7 @@ mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* ga
   if (!aligned(x, 16) || !aligned(w_down, 16) || !aligned(w_up, 16) || !aligned(q, 16) || !aligned(gamma, 2))
     return fail(MFA_ERR_INVALID_ARG, "misaligned pointer (x, weights, q need 16 bytes)");
   if (!workspace || !aligned(workspace, 256)) return fail(MFA_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
-  const size_t need = mfa_query_lowrank_workspace_bytes(batch, rank);
+  const size_t need = mfa_query_lowrank_workspace_bytes(batch, rank, n_out);
   if (workspace_bytes < need) return fail(MFA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
   DeviceInfo info;
   mfa_status_t st = current_device(nullptr, &info);
@@ -477,9 +496,12 @@ mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* ga
   char* ws = static_cast<char*>(workspace);
   QueryLowrankParams p{};
   p.gamma = static_cast<const uint16_t*>(gamma);
-  p.y = reinterpret_cast<float*>(ws + kWsHeaderBytes);
-  p.h = reinterpret_cast<uint16_t*>(ws + kWsHeaderBytes + (size_t)batch * rank * sizeof(float));
-  p.ssq = reinterpret_cast<float*>(ws + kWsHeaderBytes + (size_t)batch * rank * (sizeof(float) + sizeof(uint16_t)));
+  int cap = kMaxQueryBatch;  // the most rows this workspace holds
+  while (cap > batch && query_ws(cap, rank).total > workspace_bytes) --cap;
+  const QueryWs lay = query_ws(cap, rank);
+  p.y = reinterpret_cast<float*>(ws + lay.y);
+  p.h = reinterpret_cast<uint16_t*>(ws + lay.h);
+  p.ssq = reinterpret_cast<float*>(ws + lay.ssq);
   p.counters = reinterpret_cast<uint32_t*>(ws + kQueryCounterOffset);
   p.q = static_cast<uint16_t*>(q);
   p.err = reinterpret_cast<uint32_t*>(ws);

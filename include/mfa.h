@@ -219,15 +219,17 @@ mfa_status_t mfa_decode_attention_fp4(const void* q, const void* k_cache, const 
  * call is bound by memory bandwidth (96 MB of weights at the Step-3 shape).
  * The call is two kernel launches chained by programmatic dependent launch:
  * the up-projection streams W_up while the down-projection runs.
- * workspace: [device] at least mfa_query_lowrank_workspace_bytes(batch, rank)
- * bytes, 256-byte aligned, zeroed once by mfa_workspace_init: the call needs
- * its fp32 accumulator zero on entry and leaves it zero (also after a device
- * error). Calls sharing a workspace run one after another on one stream.
+ * workspace: [device] at least mfa_query_lowrank_workspace_bytes(batch, rank,
+ * n_out) bytes (a workspace sized for `batch` rows serves every call with as
+ * many rows or fewer), 256-byte aligned, zeroed once by mfa_workspace_init:
+ * the call needs its fp32 accumulator and arrival counters zero on entry and
+ * leaves them zero (also after a device error). Calls sharing a workspace run
+ * one after another on one stream.
  * Host errors: MFA_ERR_INVALID_ARG for null or misaligned pointers, batch
  * outside [1, MFA_MAX_QUERY_BATCH], d_model not a multiple of 64, rank or
  * n_out not a multiple of 128, rank above MFA_MAX_QUERY_RANK, eps < 0;
  * MFA_ERR_WORKSPACE. */
-size_t mfa_query_lowrank_workspace_bytes(int batch, int rank);
+size_t mfa_query_lowrank_workspace_bytes(int batch, int rank, int n_out);
 mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* gamma, const void* w_up, void* q,
                                int batch, int d_model, int rank, int n_out, float eps,
                                void* workspace, size_t workspace_bytes, void* stream);

@@ -35,10 +35,11 @@ def run_query(x, w_down, gamma, w_up, eps, ws=None, calls=1):
     dev = torch.device("cuda")
     xd, wd, gd, wu = (t.to(dev).contiguous() for t in (x, w_down, gamma, w_up))
     q = torch.empty((B, n_out), dtype=torch.bfloat16, device=dev)
-    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(B, rank)
     if ws is None:
+        ws_bytes = capi.mfa_query_lowrank_workspace_bytes(B, rank, n_out)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         capi.mfa_workspace_init(ws, ws_bytes)
+    ws_bytes = ws.numel()  # the whole workspace: its layout follows from its size
     for _ in range(calls):
         capi.mfa_query_lowrank(xd, wd, gd, wu, q, B, d_model, rank, n_out, eps, ws, ws_bytes)
     capi.mfa_check_device_errors(ws, clear=True)
@@ -82,28 +83,30 @@ def test_query_feeds_decode_attention(oracle_mod):
 
 def test_query_leaves_its_scratch_zero(oracle_mod):
     """The fp32 accumulator and the arrival counters are zero after every call,
-    so calls on one workspace (different inputs, different batch sizes) agree
-    with the oracle one after another."""
+    so single calls on one workspace (different inputs, different batch sizes,
+    larger and smaller than before) each agree with the oracle."""
     w_down, gamma, w_up = weights(*STEP3, seed=7)
-    rank = STEP3[1]
-    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(capi.MAX_QUERY_BATCH, rank)
+    _, rank, n_out = STEP3
+    cap = capi.MAX_QUERY_BATCH
+    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(cap, rank, n_out)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     ws.fill_(0xA5)
     capi.mfa_workspace_init(ws, ws_bytes)
-    for i, B in enumerate((32, 7, 32, 256)):
+    # the regions that must be zero between calls: the header's counter bytes 128-255, then y [cap * rank] fp32
+    zero_end = 256 + cap * rank * 4
+    for i, B in enumerate((32, 7, 32, 256, 1)):
         x = wl.draw_rows(B, STEP3[0], [75, i], 0)
-        q = run_query(x, w_down, gamma, w_up, 1e-6, ws=ws, calls=2)
+        q = run_query(x, w_down, gamma, w_up, 1e-6, ws=ws)  # one call: its result needs zero scratch on entry
         q_ref, _ = oracle_mod.query_lowrank(wl.bits(x), wl.bits(w_down), wl.bits(gamma), wl.bits(w_up), 1e-6)
         check(q, q_ref, f"repeat/B={B}")
-        y_bytes = B * rank * 4
-        assert torch.count_nonzero(ws[128:256 + y_bytes]) == 0, f"B={B}: counters or accumulator not zero"
+        assert torch.count_nonzero(ws[128:zero_end]) == 0, f"B={B}: counters or accumulator not zero"
 
 
 def test_query_rejects_bad_shapes():
     w_down, gamma, w_up = weights(256, 128, 384, seed=6)
     x = wl.draw_rows(2, 256, [74], 0).cuda()
     q = torch.empty((2, 384), dtype=torch.bfloat16, device="cuda")
-    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(2, 128)
+    ws_bytes = capi.mfa_query_lowrank_workspace_bytes(2, 128, 384)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     for args in ((2, 250, 128, 384), (2, 256, 100, 384), (2, 256, 128, 300), (0, 256, 128, 384), (300, 256, 128, 384),
                  (2, 256, capi.MAX_QUERY_RANK + 128, 384)):
