@@ -34,6 +34,38 @@ def test_mtp_query_count_is_checked_before_any_device_work(lib):
         assert lib.mfa_decode_mtp_workspace_bytes(4, nq, 1024) == 0
 
 
+def test_block_lists_are_checked_before_any_device_work(lib):
+    """Block gather: null or misaligned block lists and max_blocks outside
+    [1, 8 * max_pages] are refused by the host checks."""
+    arr = (ctypes.c_int32 * 8)()
+    p = ctypes.addressof(arr)
+    cases = [(None, p, 4), (p, None, 4), (p + 2, p, 4), (p, p, 0), (p, p, 8 * 3 + 1)]
+    for bi, nb, mb in cases:
+        assert lib.mfa_decode_attention_blocks(None, None, None, None, None, bi, nb, mb, None, None, 0.0625, 1, 3, 3,
+                                               64, None, 0, None) == 1
+
+
+def test_four_bit_caches_must_be_32_byte_aligned(lib):
+    """4-bit KV: TMA reads the packed codes only from 32-byte aligned rows;
+    a misaligned cache is refused before any device work."""
+    buf = (ctypes.c_uint8 * 128)()
+    base = (ctypes.addressof(buf) + 31) & ~31
+    for kc, vc in ((base + 16, base), (base, base + 16)):
+        assert lib.mfa_decode_attention_fp4(None, kc, vc, None, None, None, None, None, None, 0.0625, 1, 1, 1, 64,
+                                            None, 0, None) == 1
+        assert lib.mfa_kv_append_fp4(None, None, 1, kc, vc, None, None, None, None, 1, 1, 1, None, None) == 1
+
+
+def test_query_workspace_size_rules(lib):
+    """The query path's workspace grows with the batch it holds and is refused
+    (0) outside the limits; a workspace sized for more rows serves fewer."""
+    R, N = 2048, 16384
+    sizes = [lib.mfa_query_lowrank_workspace_bytes(b, R, N) for b in (1, 16, 32, 256)]
+    assert all(x > 0 for x in sizes) and sizes == sorted(sizes)
+    for b, r, n in ((0, R, N), (257, R, N), (4, 100, N), (4, R, 100), (4, capi.MAX_QUERY_RANK + 128, N)):
+        assert lib.mfa_query_lowrank_workspace_bytes(b, r, n) == 0
+
+
 def test_status_strings(lib):
     for code, name in capi.STATUS_NAMES.items():
         assert capi.mfa_status_string(code) == name
