@@ -151,3 +151,16 @@ def test_blocks_host_argument_checks():
                                              *args, dev.out, dev.lse, wl.SCALE, 1, dev.max_pages, dev.num_pages, 64,
                                              dev.workspace, dev.ws_bytes)
         assert e.value.status == 1
+
+
+def test_blocks32k_workload_full_size(oracle_mod):
+    """The benchmark's block-gather workload as the benchmark launches it: B=32 sequences of 32768
+    tokens, 512 selected blocks each (4104 tokens attended), every output against the oracle."""
+    w = wl.WORKLOADS["blocks32k"]
+    case = wl.make_case(w, headroom_tokens=0)
+    dev = DeviceCache(case)
+    bi, nb = wl.draw_blocks(case.lengths0, w.select_blocks, [w.seed])
+    out, lse, ws = run_blocks(dev, bi, nb)   # length hint = the largest attended count, as in bench.py
+    capi.mfa_check_device_errors(ws, clear=True)
+    out_ref, lse_ref = oracle_blocks(oracle_mod, dev, bi, nb)
+    compare(out, lse, out_ref, lse_ref, "blocks32k")
