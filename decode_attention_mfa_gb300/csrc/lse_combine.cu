@@ -50,8 +50,10 @@ struct CombineShape {
   static_assert(kH <= 8, "weights are computed by warps 0 .. kH-1");
 };
 
+// At most 64 registers a thread, so four CTAs share an SM (608 on 152 SMs), which holds the whole
+// grid of batches up to 64 sequences in one wave (at 80 registers, three a SM, B = 64 took two).
 template <int kH>
-__global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeParams p) {
   using Sh = CombineShape<kH>;
   extern __shared__ int smem_i[];
   int* s_len = smem_i;
