@@ -1495,14 +1495,9 @@ template <bool kFp8, bool kMtp>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, cudaStream_t stream) {
   const size_t smem = (size_t)smem_layout<kFp8, kMtp>(p.B).total + 1024;
-  static int configured_bytes = 0;  // largest opt-in set so far (per process; one device family)
-  if ((int)smem > configured_bytes) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(decode_split_tc_kernel<kFp8, kMtp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    configured_bytes = (int)smem;
-  }
+  static int configured[kTrackedDevices] = {};  // largest opt-in set so far, per device
+  const cudaError_t e = ensure_dynamic_smem(decode_split_tc_kernel<kFp8, kMtp>, smem, configured);
+  if (e != cudaSuccess) return e;
   return launch_pdl(decode_split_tc_kernel<kFp8, kMtp>, dim3(p.grid), dim3(Cfg<kFp8, kMtp>::kThreads), smem, stream, p, kmap,
                     vmap, qmap);
 }

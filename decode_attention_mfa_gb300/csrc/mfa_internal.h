@@ -94,6 +94,26 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Raises a kernel's dynamic shared-memory opt-in (and, with full_carveout, its preferred carve-out to all
+// of the unified L1 / shared array) on the current device before a launch that needs `bytes`. The
+// attributes belong to each device's context, so `record` keeps the largest value set per device
+// ordinal; a device past its end is set on every call.
+constexpr int kTrackedDevices = 64;
+template <typename... KArgs>
+inline cudaError_t ensure_dynamic_smem(void (*kernel)(KArgs...), size_t bytes, int (&record)[kTrackedDevices],
+                                       bool full_carveout = false) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int* rec = (dev >= 0 && dev < kTrackedDevices) ? &record[dev] : nullptr;
+  if (rec && (int)bytes <= *rec) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && full_carveout)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess && rec) *rec = (int)bytes;
+  return e;
+}
+
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,

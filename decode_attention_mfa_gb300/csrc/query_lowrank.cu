@@ -316,17 +316,11 @@ template <bool kDown>
 cudaError_t launch_gemm(const GemmParams& g, const CUtensorMap& wmap, const CUtensorMap& xmap, int features,
                         cudaStream_t s) {
   const size_t smem = gemm_smem_bytes(g.Bp, g.stages);
-  static int configured = 0;
-  if ((int)smem > configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(lowrank_gemm_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    // all of the unified L1 / shared array as shared memory: a down CTA and an up CTA then fit on one SM
-    // together (the carve-out an SM runs with is set by the first kernel placed on it)
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(lowrank_gemm_kernel<kDown>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    configured = (int)smem;
-  }
+  // the full carve-out: a down CTA and an up CTA then fit on one SM together (the carve-out an SM runs
+  // with is set by the first kernel placed on it)
+  static int configured[kTrackedDevices] = {};
+  const cudaError_t e = ensure_dynamic_smem(lowrank_gemm_kernel<kDown>, smem, configured, true);
+  if (e != cudaSuccess) return e;
   return launch_pdl(lowrank_gemm_kernel<kDown>, dim3(features / 128, g.splits), dim3(kGemmThreads), smem, s, g, wmap,
                     xmap);
 }
