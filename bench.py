@@ -23,6 +23,7 @@ by one token per visit, and the mean attended length is reported.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -48,6 +49,10 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 135_528_448
 COPY_MEM_BUDGET = 100e9
+DRIFT = 0.03              # with an append, each cache copy grows by at most about this fraction of its length
+MAX_HEADLINE_STEPS = 20000
+MIN_GRAPH_STEPS = 32      # steps per captured graph (graph launches amortised over at least this many)
+EXTRA_WORKLOADS = ("long", "fp8", "ragged")
 
 
 def parse_args():
@@ -60,6 +65,10 @@ def parse_args():
                     help="a decode workload, or qproj: the low-rank query path at the Step-3 shape")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (debug runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--region-seconds", type=float, default=0.5,
+                    help="device time the headline's repeated K-step regions add up to (median region reported)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the extra workloads timed after the headline")
     ap.add_argument("--copies", type=int, default=0,
                     help="device-resident cache copies to rotate over (default: enough to defeat L2 "
                          "and keep the per-copy length growth near 1%%; small values suit ncu captures)")
@@ -76,7 +85,7 @@ def measured_peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples (every 100 ms) while running."""
+    """nvidia-smi clock and throttle-reason samples (every 20 ms) while running."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -92,7 +101,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=open(self.path + ".err", "w"))
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=open(self.path + ".err", "w"))
         except (FileNotFoundError, OSError):
             self.proc = None
         time.sleep(0.3)
@@ -125,7 +134,7 @@ class ClockSampler:
                 err = open(self.path + ".err").read().strip()[:200]
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"no nvidia-smi samples {err}".strip()],
                     "samples": 0}
-        inside = [r for r in rows if t0 - 0.11 <= r[0] <= t1 + 0.11] or rows[-3:]
+        inside = [r for r in rows if t0 - 0.03 <= r[0] <= t1 + 0.03] or rows[-3:]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
@@ -136,6 +145,24 @@ class ClockSampler:
 def appends(w: wl.Workload) -> bool:
     """Whether a step of the workload appends one token per sequence first."""
     return w.append_tokens > 0
+
+
+def arm_config(w: wl.Workload, world: int) -> dict:
+    """The workload's identity, the same dict in both arms of the benchmark."""
+    app = appends(w)
+    blocks = w.select_blocks > 0
+    return {"workload": w.name, "description": w.description, "batch": w.batch, "heads": wl.HEADS,
+            "head_dim": wl.HEAD_DIM, "page_size": wl.PAGE_SIZE, "kv_dtype": w.kv_dtype,
+            "queries_per_sequence": w.queries,
+            "step": ("mfa_kv_append(1 token/seq) + " if app else "") +
+                    ("mfa_decode_attention_blocks" if blocks else
+                     "mfa_decode_attention_mtp" if w.queries > 1 else
+                     "mfa_decode_attention_fp4" if w.kv_dtype == "fp4" else
+                     "mfa_decode_attention_fp8" if w.kv_dtype == "fp8" else "mfa_decode_attention") +
+                    " (split + LSE combine)",
+            "l2": "steps rotate over device-resident copies of the cache, together more than 3x the 135 MB L2, "
+                  "so no step finds its cache in L2",
+            "parallelism": f"dp{world} (independent batch per GPU)"}
 
 
 def bench_lengths(w: wl.Workload) -> np.ndarray:
@@ -151,9 +178,17 @@ def first_attended(w: wl.Workload) -> np.ndarray:
 def choose_copies(w: wl.Workload, lens: np.ndarray, total_steps: int) -> int:
     kv_copy = float(lens.sum()) * acc.kv_bytes_per_token(w.kv_dtype)
     need_l2 = math.ceil(3 * L2_BYTES / kv_copy) + 1
-    need_drift = math.ceil(total_steps / max(1.0, 0.01 * float(lens.mean()))) if appends(w) else 0
+    need_drift = math.ceil(total_steps / max(1.0, DRIFT * float(lens.mean()))) if appends(w) else 0
     cap = max(2, int(COPY_MEM_BUDGET // (2.2 * kv_copy)))
     return int(max(2, min(cap, max(need_l2, need_drift))))
+
+
+def est_step_seconds(w: wl.Workload, lens) -> float:
+    """Rough step time (algorithmic bytes at 5 TB/s), used only to size the timed regions."""
+    L = np.asarray(lens, dtype=np.int64)
+    if w.select_blocks:
+        return max(5e-6, 1024.0 * (8 * w.select_blocks + 8) * L.size / 5e12)
+    return max(5e-6, acc.decode_step_bytes(L, w.kv_dtype, appended_tokens=w.append_tokens, n_query=w.queries) / 5e12)
 
 
 def kernel_source_sha() -> str:
@@ -199,7 +234,10 @@ def query_traffic():
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, rank, world, local):
+def run_ours(args, rank, world, local, workload=None, region_s=None, with_e2e=None):
+    """One workload through the C ABI. The headline times K steps in each of several
+    regions (about `region_s` seconds of them in all, so the clock sampler sees the load);
+    its value is the median region."""
     import torch
     from decode_attention_mfa_gb300 import capi
     from decode_attention_mfa_gb300.build import build
@@ -207,10 +245,14 @@ def run_ours(args, rank, world, local):
     build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = wl.WORKLOADS[args.workload]
+    w = wl.WORKLOADS[workload or args.workload]
+    e2e_on = (not args.no_e2e) if with_e2e is None else with_e2e
+    region_s = args.region_seconds if region_s is None else region_s
     lens0 = bench_lengths(w)
     B = int(lens0.size)
-    total_steps = args.warmup + args.steps * (1 if args.no_e2e else 2) + 2
+    est_step_s = est_step_seconds(w, lens0)
+    n_reg = max(3, min(math.ceil(region_s / (args.steps * est_step_s)), max(3, MAX_HEADLINE_STEPS // args.steps)))
+    total_steps = args.warmup + args.steps * (n_reg + (1 if e2e_on else 0)) + 2
     total_steps += max(2, min(args.steps, 512))  # the region that times the split kernel alone
     blocks = w.select_blocks > 0
     if blocks:  # block gather: the caller's selection, the same every step
@@ -388,50 +430,57 @@ def run_ours(args, rank, world, local):
                 copy_in(j + 2)  # after step j's result left buffer j % 2
         stream.wait_stream(cs)
 
-    def timed(n_steps, with_events, e2e_bufs=None):
+    def timed(n_steps, with_events, e2e_bufs=None, regions=1):
+        """Times `regions` regions of n_steps steps each (the same captured graphs replayed); returns
+        the device ms of every region, the split-launch event times (with_events), the lengths of the
+        last R steps, the wall-clock span, and the algorithmic bytes of every region."""
         nonlocal cursor
         order = [(cursor + i) % R for i in range(n_steps)]
-        # one graph holds the R copies once, or (end to end) several times, so that the copy pipeline
-        # runs over at least 16 steps before a graph boundary drains it
-        grp = R if e2e_bufs is None else R * max(1, -(-16 // R))
+        # one graph holds at least MIN_GRAPH_STEPS steps (a whole number of passes over the R copies), so
+        # that graph launches are amortised; end to end, at least 16, so the copy pipeline rarely drains
+        grp = R * max(1, -(-(MIN_GRAPH_STEPS if e2e_bufs is None else 16) // R))
+        if with_events:
+            grp = R
         full = order[:grp] if n_steps >= grp else []
         reps = n_steps // grp if full else 0
         tail = order[reps * grp:]
         g_full, ev_full = capture(full, with_events, e2e_bufs) if full else (None, [])
         g_tail, ev_tail = capture(tail, with_events, e2e_bufs) if tail else (None, [])
-        # the captures did not run: lengths are unchanged; account in execution order
-        lens_seen = []
-        for r in order:
-            lens_seen.append(account(r))
-        torch.cuda.synchronize()
-        mdist.barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.time()
-        with torch.cuda.stream(stream):  # replay() launches on the current stream
-            e0.record(stream)
-            for _ in range(reps):
-                g_full.replay()
-            if g_tail is not None:
-                g_tail.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        t1 = time.time()
-        mdist.barrier()
-        cursor += n_steps
-        ms = e0.elapsed_time(e1)
+        region_ms, region_bytes, lens_seen = [], [], []
+        t_first = None
+        for _ in range(regions):
+            # the captures did not run: lengths are unchanged; account in execution order
+            n0 = len(step_bytes)
+            lens_seen = [account(r) for r in order]
+            region_bytes.append(float(sum(step_bytes[n0:])))
+            torch.cuda.synchronize()
+            mdist.barrier()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.time()
+            t_first = t0 if t_first is None else t_first
+            with torch.cuda.stream(stream):  # replay() launches on the current stream
+                e0.record(stream)
+                for _ in range(reps):
+                    g_full.replay()
+                if g_tail is not None:
+                    g_tail.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            t1 = time.time()
+            mdist.barrier()
+            cursor += n_steps
+            region_ms.append(e0.elapsed_time(e1))
         evs = ev_full if ev_full else ev_tail
         split_ms = [a.elapsed_time(b) for a, b in evs]
         last_lens = lens_seen[(reps - 1) * grp:(reps - 1) * grp + R] if reps else lens_seen[-len(tail):]
-        return ms, split_ms, last_lens, (t0, t1)
+        return region_ms, split_ms, last_lens, (t_first, t1), region_bytes
 
     clocks = ClockSampler(local)
     clocks.start()
-    # headline: K steps, no events in the graph (an event node between the
+    # headline: n_reg regions of K steps, no events in the graphs (an event node between the
     # kernels of a step would break their programmatic overlap)
-    n_before = len(step_bytes)
-    ms, _, last_lens, (t0, t1) = timed(args.steps, with_events=False)
-    bytes_k = float(sum(step_bytes[n_before:]))
+    reg_ms, _, last_lens, (t0, t1), reg_bytes = timed(args.steps, with_events=False, regions=n_reg)
     time.sleep(0.15)
     clocks.stop()
     clk = clocks.summary(t0, t1)
@@ -441,19 +490,22 @@ def run_ours(args, rank, world, local):
     # recorded around every split launch on its stream
     n_ev = max(2, min(args.steps, 512))
     n_before = len(split_bytes)
-    _, split_ms, _, _ = timed(n_ev, with_events=True)
+    _, split_ms, _, _, _ = timed(n_ev, with_events=True)
     split_bytes_last = split_bytes[n_before:][-len(split_ms):]
     capi.mfa_check_device_errors(workspace, clear=True, stream=stream)
 
-    total_bytes, max_s = mdist.aggregate(bytes_k, ms / 1e3)
-    value = total_bytes / max_s / 1e12
+    tot_b, max_s = mdist.aggregate_many(reg_bytes, [m / 1e3 for m in reg_ms])
+    reg_val = [b / t / 1e12 for b, t in zip(tot_b, max_s)]
+    med = int(np.argsort(reg_val)[len(reg_val) // 2])  # the median region
+    value = reg_val[med]
+    max_s = max_s[med]
     peak_gbs, peak_kind = measured_peaks()
     avg_split_s = float(np.mean(split_ms)) / 1e3 if split_ms else float("nan")
     achieved = float(np.mean(split_bytes_last)) / avg_split_s / 1e9 if split_ms else None
     tokens_per_launch = float(np.mean([float(np.sum(L)) for L in last_lens]))
 
     e2e = None
-    if not args.no_e2e:
+    if e2e_on:
         hq = torch.empty(q[0].shape, dtype=torch.bfloat16).pin_memory()
         hq.copy_(q[0].cpu())
         hkv = torch.empty((2, B, 1, wl.HEAD_DIM), dtype=torch.bfloat16).pin_memory()
@@ -465,13 +517,14 @@ def run_ours(args, rank, world, local):
         dout = [torch.empty_like(out_main) for _ in range(2)]
         dlse = [torch.empty_like(lse_main) for _ in range(2)]
         n_before = len(step_bytes)
-        e_ms, _, _, _ = timed(args.steps, with_events=False, e2e_bufs=(hq, hkv, hout, hlse, dq, dkv, dout, dlse))
-        e_bytes, e_s = mdist.aggregate(float(sum(step_bytes[n_before:])), e_ms / 1e3)
+        e_ms, _, _, _, e_reg_b = timed(args.steps, with_events=False,
+                                       e2e_bufs=(hq, hkv, hout, hlse, dq, dkv, dout, dlse))
+        e_bytes, e_s = mdist.aggregate(e_reg_b[0], e_ms[0] / 1e3)
         capi.mfa_check_device_errors(workspace, clear=True, stream=stream)
         e2e = {"value": e_bytes / e_s / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(hq.numel() * 2 + (hkv.numel() * 2 if app else 0)),
                "d2h_bytes_per_step": int(hout.numel() * 2 + hlse.numel() * 4),
-               "ms_per_step": e_ms / args.steps,
+               "ms_per_step": e_ms[0] / args.steps,
                "how": "CUDA graph of the C-ABI calls; each step's inputs copied in from pinned host memory and its "
                       "result copied back, on a copy stream overlapping the neighbouring steps (double buffers)"}
 
@@ -480,17 +533,11 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": max_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e2m1" if fp4 else "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), bf16)",
-        "config": {"workload": w.name, "description": w.description, "batch": B, "heads": wl.HEADS,
-                   "head_dim": wl.HEAD_DIM, "page_size": wl.PAGE_SIZE, "kv_dtype": w.kv_dtype,
-                   "mean_attended_len": mean_len,
-                   "queries_per_sequence": nq,
-                   "step": ("mfa_kv_append(1 token/seq) + " if app else "") +
-                           ("mfa_decode_attention_blocks" if blocks else
-                            "mfa_decode_attention_mtp" if nq > 1 else "mfa_decode_attention") +
-                           " (split + LSE combine)",
-                   "l2": f"inputs rotate over {R} device-resident cache copies "
-                         f"({R * float(lens0.sum()) * acc.kv_bytes_per_token(w.kv_dtype) / 1e9:.1f} GB >> 135 MB L2)",
-                   "parallelism": f"dp{world} (independent batch per GPU)"},
+        "config": arm_config(w, world),
+        "mean_attended_len": mean_len,
+        "cache_copies": R,
+        "regions": {"count": len(reg_val), "steps_each": args.steps, "value_of_each": "median reported",
+                    "min": min(reg_val), "max": max(reg_val)},
         "steps_per_s": args.steps * world / max_s,
         "pct_of_measured_peak": 100.0 * value * 1e3 / peak_gbs,
         "pct_of_8TBps": 100.0 * value * 1e3 / NOMINAL_HBM_GBS,
@@ -507,6 +554,28 @@ def run_ours(args, rank, world, local):
         "e2e": e2e,
     }
     return result, lens0
+
+
+def extra_workloads(args, rank, world, local) -> dict:
+    """After the headline, the other full-size configurations timed the same way (no
+    end-to-end leg, no CPU baseline): step time, throughput, split-kernel time, clocks."""
+    import torch
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        r, _ = run_ours(args, rank, world, local, workload=name, region_s=min(args.region_seconds, 0.2),
+                        with_e2e=False)
+        rf = r["roofline"]
+        out[name] = {"description": r["config"]["description"], "value": r["value"], "unit": r["unit"],
+                     "ms_per_step": r["ms_per_step"], "steps_per_s": r["steps_per_s"],
+                     "pct_of_measured_peak": r["pct_of_measured_peak"], "pct_of_8TBps": r["pct_of_8TBps"],
+                     "mean_attended_len": r["mean_attended_len"], "regions": r["regions"],
+                     "split_kernel": {"avg_launch_us": rf["avg_launch_us"], "achieved_gbs": rf["achieved"],
+                                      "frac": rf["frac"], "traffic": rf["traffic"]},
+                     "clocks": r["clocks"], "dtype": r["dtype"]}
+        del r
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ oracle
@@ -663,8 +732,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1), bf16)",
-            "config": {"workload": w.name, "description": w.description, "batch": int(lens.size),
-                       "heads": wl.HEADS, "head_dim": wl.HEAD_DIM, "kv_dtype": w.kv_dtype},
+            "config": arm_config(w, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -789,7 +857,7 @@ def run_qproj(args, rank_id, world, local):
     avg_us = float(np.mean(per_call)) * 1e3
     achieved = step_bytes / (avg_us * 1e-6) / 1e9
     e2e = None
-    if not args.no_e2e:
+    if e2e_on:
         hx = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
         hx.copy_(x.cpu())
         hq = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
@@ -861,6 +929,8 @@ def main():
         return
     rank, world, local = mdist.init()
     res, lens0 = run_ours(args, rank, world, local)
+    if args.workload == "ctx4k" and not args.no_extra:
+        res["workloads"] = extra_workloads(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(wl.WORKLOADS[args.workload], first_attended(wl.WORKLOADS[args.workload]))

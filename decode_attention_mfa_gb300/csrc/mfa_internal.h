@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -97,7 +98,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Raises a kernel's dynamic shared-memory opt-in (and, with full_carveout, its preferred carve-out to all
 // of the unified L1 / shared array) on the current device before a launch that needs `bytes`. The
 // attributes belong to each device's context, so `record` keeps the largest value set per device
-// ordinal; a device past its end is set on every call.
+// ordinal. One process-wide lock covers the check, the attribute calls and the record, so host
+// threads that launch with different sizes at once can never lower the opt-in below what another
+// launch was promised: the value only ever grows. A device past the record's end reads the
+// attribute back and raises it only when needed.
+inline std::mutex& smem_attr_mutex() {
+  static std::mutex m;
+  return m;
+}
 constexpr int kTrackedDevices = 64;
 template <typename... KArgs>
 inline cudaError_t ensure_dynamic_smem(void (*kernel)(KArgs...), size_t bytes, int (&record)[kTrackedDevices],
@@ -105,8 +113,14 @@ inline cudaError_t ensure_dynamic_smem(void (*kernel)(KArgs...), size_t bytes, i
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(smem_attr_mutex());
   int* rec = (dev >= 0 && dev < kTrackedDevices) ? &record[dev] : nullptr;
   if (rec && (int)bytes <= *rec) return cudaSuccess;
+  if (!rec) {
+    cudaFuncAttributes a{};
+    if ((e = cudaFuncGetAttributes(&a, kernel)) != cudaSuccess) return e;
+    if ((int)bytes <= a.maxDynamicSharedSizeBytes) return cudaSuccess;
+  }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess && full_carveout)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);

@@ -58,6 +58,20 @@ def aggregate(bytes_done: float, seconds: float) -> tuple[float, float]:
     return reduce_scalar(bytes_done, "sum"), reduce_scalar(seconds, "max")
 
 
+def aggregate_many(bytes_done, seconds) -> tuple[list, list]:
+    """aggregate() for several timed regions at once (one collective per list):
+    per region, bytes summed over ranks and the slowest rank's seconds."""
+    b = [float(x) for x in bytes_done]
+    t = [float(x) for x in seconds]
+    if not dist.is_initialized():
+        return b, t
+    tb = torch.tensor(b, dtype=torch.float64, device=_device())
+    tt = torch.tensor(t, dtype=torch.float64, device=_device())
+    dist.all_reduce(tb, op=dist.ReduceOp.SUM)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return tb.cpu().tolist(), tt.cpu().tolist()
+
+
 def finalize():
     if dist.is_initialized():
         dist.destroy_process_group()

@@ -28,7 +28,8 @@ def _worker(rank, world, port, out):
     mx = mdist.reduce_scalar(1.0 + rank, "max")
     sm = mdist.reduce_scalar(10.0 * (rank + 1), "sum")
     total_bytes, max_s = mdist.aggregate(bytes_done=100.0 * (rank + 1), seconds=0.5 + rank)
-    out[rank] = (mx, sm, total_bytes, max_s)
+    many_b, many_s = mdist.aggregate_many([1.0 + rank, 2.0], [0.25 * (rank + 1), 3.0 - rank])
+    out[rank] = (mx, sm, total_bytes, max_s, tuple(many_b), tuple(many_s))
     mdist.finalize()
 
 
@@ -44,7 +45,7 @@ def test_two_rank_timing_reduction():
         p.join(timeout=120)
         assert p.exitcode == 0
     for r in range(2):
-        assert out[r] == (2.0, 30.0, 300.0, 1.5)
+        assert out[r] == (2.0, 30.0, 300.0, 1.5, (3.0, 4.0), (0.5, 3.0))
 
 
 def test_single_process_is_identity(monkeypatch):
@@ -53,3 +54,4 @@ def test_single_process_is_identity(monkeypatch):
     from decode_attention_mfa_gb300 import dist as mdist
     assert mdist.init() == (0, 1, 0)
     assert mdist.aggregate(5.0, 2.0) == (5.0, 2.0)
+    assert mdist.aggregate_many([5.0, 6.0], [2.0, 1.0]) == ([5.0, 6.0], [2.0, 1.0])
