@@ -156,7 +156,8 @@ def arm_config(w: wl.Workload, world: int) -> dict:
             "queries_per_sequence": w.queries,
             "step": ("mfa_kv_append(1 token/seq) + " if app else "") +
                     ("mfa_decode_attention_blocks" if blocks else
-                     "mfa_decode_attention_mtp" if w.queries > 1 else
+                     ("mfa_decode_attention_mtp" + {"fp8": "_fp8", "fp4": "_fp4"}.get(w.kv_dtype, "")
+                      + f" (n_query={w.queries})") if w.queries > 1 else
                      "mfa_decode_attention_fp4" if w.kv_dtype == "fp4" else
                      "mfa_decode_attention_fp8" if w.kv_dtype == "fp8" else "mfa_decode_attention") +
                     " (split + LSE combine)",
@@ -274,6 +275,7 @@ def run_ours(args, rank, world, local, workload=None, region_s=None, with_e2e=No
     row_bytes = wl.HEAD_DIM // 2 if fp4 else wl.HEAD_DIM
     append_q = capi.mfa_kv_append_fp4 if fp4 else capi.mfa_kv_append_fp8
     decode_q = capi.mfa_decode_attention_fp4 if fp4 else capi.mfa_decode_attention_fp8
+    mtp_q = capi.mfa_decode_attention_mtp_fp4 if fp4 else capi.mfa_decode_attention_mtp_fp8
     stream = torch.cuda.Stream(device=dev)
     copy_stream = torch.cuda.Stream(device=dev)
     ws_hint = int(acc.blocks_attended(lens0, nblk_h).max()) if blocks else int(lens0.max()) + headroom
@@ -335,9 +337,12 @@ def run_ours(args, rank, world, local, workload=None, region_s=None, with_e2e=No
             if app:
                 append_q(kn, vn, 1, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table,
                                        sl, B, max_pages, num_pages, workspace, stream)
-            decode_q(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl,
-                                          out, lse, wl.SCALE, B, max_pages, num_pages, ws_hint, workspace,
-                                          ws_bytes, stream)
+            if nq > 1:
+                mtp_q(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl, out, lse, wl.SCALE, B,
+                      nq, max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
+            else:
+                decode_q(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl,
+                         out, lse, wl.SCALE, B, max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
         else:
             if app:
                 capi.mfa_kv_append(kn, vn, 1, k_caches[r], v_caches[r], page_table, sl, B, max_pages, num_pages,
@@ -539,6 +544,7 @@ def run_ours(args, rank, world, local, workload=None, region_s=None, with_e2e=No
         "regions": {"count": len(reg_val), "steps_each": args.steps, "value_of_each": "median reported",
                     "min": min(reg_val), "max": max(reg_val)},
         "steps_per_s": args.steps * world / max_s,
+        "decoded_tokens_per_s": args.steps * world * B * nq / max_s,
         "pct_of_measured_peak": 100.0 * value * 1e3 / peak_gbs,
         "pct_of_8TBps": 100.0 * value * 1e3 / NOMINAL_HBM_GBS,
         "gpu_launches": (3 if app else 2) * args.steps,

@@ -20,7 +20,7 @@ MFA_OK = 0
 STATUS_NAMES = {0: "MFA_OK", 1: "MFA_ERR_INVALID_ARG", 2: "MFA_ERR_UNSUPPORTED", 3: "MFA_ERR_CUDA",
                 4: "MFA_ERR_WORKSPACE", 5: "MFA_ERR_DEVICE_PAGE", 6: "MFA_ERR_DEVICE_CAPACITY",
                 7: "MFA_ERR_DEVICE_TIMEOUT"}
-HEADS, HEAD_DIM, PAGE_SIZE, MAX_BATCH = 64, 256, 64, 1024
+HEADS, HEAD_DIM, PAGE_SIZE, MAX_BATCH, MAX_QUERY_TOKENS = 64, 256, 64, 1024, 8
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +53,8 @@ _SIGNATURES = {
     "mfa_query_lowrank_workspace_bytes": ([_I, _I, _I], _Z),
     "mfa_query_lowrank": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _Z, _P], _I),
     "mfa_decode_attention_mtp": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_decode_attention_mtp_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_decode_attention_mtp_fp4": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_blocks": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_check_device_errors": ([_P, _I, _P], _I),
     "mfa_set_wait_budget_ns": ([_U64], None),
@@ -203,6 +205,26 @@ def mfa_decode_attention_mtp(q, k_cache, v_cache, page_table, seq_lens, out, lse
                                            _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch, n_query,
                                            max_pages, num_pages, max_len_hint, _ptr(workspace),
                                            workspace_bytes, _stream(stream)))
+
+
+def mfa_decode_attention_mtp_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse, scale,
+                                 batch, n_query, max_pages, num_pages, max_len_hint, workspace, workspace_bytes,
+                                 stream=None):
+    """Multi-token decode over an E4M3 cache with per-token fp32 scales."""
+    _check(load().mfa_decode_attention_mtp_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                               _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale),
+                                               batch, n_query, max_pages, num_pages, max_len_hint, _ptr(workspace),
+                                               workspace_bytes, _stream(stream)))
+
+
+def mfa_decode_attention_mtp_fp4(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse, scale,
+                                 batch, n_query, max_pages, num_pages, max_len_hint, workspace, workspace_bytes,
+                                 stream=None):
+    """Multi-token decode over a packed E2M1 cache with per-token fp32 scales."""
+    _check(load().mfa_decode_attention_mtp_fp4(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                               _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale),
+                                               batch, n_query, max_pages, num_pages, max_len_hint, _ptr(workspace),
+                                               workspace_bytes, _stream(stream)))
 
 
 def mfa_decode_attention_blocks(q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks, max_blocks, out,

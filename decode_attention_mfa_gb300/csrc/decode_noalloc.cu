@@ -138,6 +138,8 @@ extern "C" mfa_status_t mfa_decode_attention_noalloc(const void* q, const void* 
   p.grid = plan.grid_ctas;
   p.piece_cost = kPieceCostPages;
   p.n_query = 1;
+  p.q_per_cta = 1;
+  p.q_groups = 1;
   p.wait_budget_ns = current_wait_budget_ns();
   CUtensorMap kmap, vmap, qmap;
   if ((st = encode_map(&kmap, k_cache, (uint64_t)num_pages * kPageSize)) != MFA_OK ||

@@ -129,6 +129,13 @@ struct Cfg<true, false> {
   static constexpr int kOHalfCols = 128;  // [term][head]
 };
 
+// Token groups (multi-token decode) run on the two-token kernel and on the E4M3 kernel; the
+// single-token bf16 kernel always serves one group, so its index arithmetic folds away.
+template <bool kFp8, bool kMtp>
+__device__ __forceinline__ int q_groups_of(const DecodeParams& p) {
+  return (kFp8 || kMtp) ? p.q_groups : 1;
+}
+
 constexpr int kSlotBytes = 16384;
 constexpr int kStageBytes = 16384;        // one E4M3 V page: 64 rows x 256 B (two 128 B-wide swizzled boxes)
 constexpr int kKTileBytes = 32768;        // one E4M3 K tile: box h (dims [128h, 128h+128)) of 128 rows at 16 KB * h
@@ -385,8 +392,11 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   using C = Cfg<kFp8, kMtp>;
   using Bb = Bars<kFp8, kMtp>;
   const int lane = threadIdx.x & 31;
-  const uint64_t pol_stream = policy_evict_first();
+  // the CTAs of one range (token groups) read the same pages: keep them in L2 for the others
+  const int qg = q_groups_of<kFp8, kMtp>(p);
+  const uint64_t pol_stream = qg > 1 ? policy_evict_normal() : policy_evict_first();
   const uint64_t pol_keep = policy_evict_last();
+  const int q_tok0 = (int)(blockIdx.x % qg) * C::kQ;  // first query token of this CTA's group
   const SmemLayout L = smem_layout<kFp8, kMtp>(p.B);
   uint32_t cc = 0, seg_i = 0, sc_cnt = 0;  // chunks (bf16) or staged K tiles (E4M3); pieces; tiles
   Seg s;
@@ -534,8 +544,8 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
       mbar_arrive_expect_tx(cx.bar(Bb::QFull + qb), (uint32_t)(C::kQ * kQBytes));
       for (int d = 0; d < 4; ++d)
         for (int t = 0; t < C::kQ; ++t)
-          tma_load_2d(q_dst + (d * C::kQ + t) * 8192, qmap, d * 64, (s.b * C::kQ + t) * kHeads,
-                      cx.bar(Bb::QFull + qb), pol_keep);
+          tma_load_2d(q_dst + (d * C::kQ + t) * 8192, qmap, d * 64, (s.b * p.n_query + q_tok0 + t) * kHeads,
+                      cx.bar(Bb::QFull + qb), pol_keep);  // a row past the last token reads zeros
     }
     issued_q = true;
     last_q_parity = qn & 1;
@@ -630,7 +640,7 @@ __device__ void producer_v_role(const DecodeParams& p, const CUtensorMap* vmap, 
   using C = Cfg<true>;
   using Bb = Bars<true>;
   const int lane = threadIdx.x & 31;
-  const uint64_t pol_stream = policy_evict_first();
+  const uint64_t pol_stream = p.q_groups > 1 ? policy_evict_normal() : policy_evict_first();
   const SmemLayout L = smem_layout<true>(p.B);
   uint32_t vc = 0;  // V pages staged
   Seg s;
@@ -1169,6 +1179,8 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   const int row = threadIdx.x & 127;     // TMEM lane = token of the tile = dim of each O^T half
   const int quad = row >> 5, lane = row & 31;
   const int h0 = g * kHpt;
+  const int qg = q_groups_of<kFp8, kMtp>(p);
+  const int tau = (c % qg) * C::kQ + (kMtp ? g : 0);  // the query token this thread serves
   const SmemLayout L = smem_layout<kFp8, kMtp>(p.B);
   float* red = reinterpret_cast<float*>(gbase + L.red);  // [4][kCols] per-warp partial reductions
   float* mref = red + 4 * kCols;                         // [kCols] reference maxima (log2 units), uniform
@@ -1256,10 +1268,12 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
 #pragma unroll
     for (int h = 0; h < kHpt; ++h) lp[h] = 0.0f;
     const int T = tiles_of(s);
+    const int vis_len = min(s.len, s.len - (p.n_query - 1 - tau));
     for (int t = 0; t < T; ++t) {
       const int tok0 = (s.pg0 + 2 * t) * kPageSize;
-      // valid rows of the tile; query token g of kQ sees the first len - (kQ - 1 - g) positions
-      const int rows = max(0, min(pages_in_tile(s, t) * kPageSize, s.len - (kMtp ? C::kQ - 1 - g : 0) - tok0));
+      // valid rows of the tile: query token tau of T sees the first len - (T - 1 - tau) positions (a
+      // token past the last, which only fills a group, is clamped to len; its result is not used)
+      const int rows = max(0, min(pages_in_tile(s, t) * kPageSize, vis_len - tok0));
       const bool full = rows == 128, valid = row < rows;
       // E4M3: this token's K and V scales (the tile's scale block, slot = tile count)
       float kmul = c2, vmul = 1.0f;
@@ -1374,7 +1388,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
 #pragma unroll
     for (int i = 0; i < kHpt / 32; ++i) red[quad * kCols + h0 + (kHpt / 32) * lane + i] = lp[i];
     barrier_group(g);
-    const size_t slot = (size_t)c + s.b;
+    const size_t slot = ((size_t)(c / qg) + s.b) * qg + c % qg;
     if (row < kHpt) {
       const int h = h0 + row;
       const float l = red[h] + red[kCols + h] + red[2 * kCols + h] + red[3 * kCols + h];
@@ -1469,7 +1483,10 @@ __global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const long long units = s_cost[p.B];  // total cost units
   const int c = blockIdx.x;
-  const long long lo = cta_cost_lo(c, units, p.grid), hi = cta_cost_lo(c + 1, units, p.grid);
+  // token groups: CTA c works on range c / q_groups of a partition into grid / q_groups ranges
+  const int qg = q_groups_of<kFp8, kMtp>(p);
+  const int ranges = p.grid / qg, range = c / qg;
+  const long long lo = cta_cost_lo(range, units, ranges), hi = cta_cost_lo(range + 1, units, ranges);
   Ctx cx{base, bars, abort_flag, p.err, p.wait_budget_ns};
 
   if (warp < 4 * C::kGroups) {

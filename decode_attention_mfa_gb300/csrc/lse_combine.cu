@@ -8,8 +8,9 @@
 // softmax sum exactly).
 //
 // With several query tokens per sequence (multi-token decode) every token t
-// is merged on its own: its partials are [slot][token][head][dim], and token
-// t of a sequence of length L sees the first L - (n_query - 1 - t) positions.
+// is merged on its own, over the partials of its token group (a slot holds
+// [token of the group][head][dim]); token t of a sequence of length L sees the
+// first L - (n_query - 1 - t) positions.
 //
 // One CTA of 256 threads per (sequence, token, group of kH heads); kH is chosen from
 // the batch so that small batches still spread over the SMs. Per head,
@@ -71,7 +72,10 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
   const int r = threadIdx.x % Sh::kThreadsPerHead;
   const int dt = r % Sh::kDimThreads, sub = r / Sh::kDimThreads;
   const int h = blockIdx.x * kH + hl;
-  const int G = p.grid;
+  // token groups: the split ran q_groups copies of a partition into G ranges; token tq sits in group grp
+  // at position t, and range c's partial of it is row ((c + b) * q_groups + grp) * q_per_cta + t
+  const int P = p.q_groups, kq = p.q_per_cta, grp = tq / kq, t = tq % kq;
+  const int G = p.grid / P;
   const long long C = s_cost[p.B];
   const int np = pages_of_len(s_len[b]);
   uint16_t* out = p.out + ((size_t)blockIdx.y * kHeads + h) * kHeadDim;
@@ -88,8 +92,9 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
   const long long first = (long long)s_cost[b] + p.piece_cost;
   const int c_first = cta_of_cost(first, C, G);
   const int n = cta_of_cost(first + np - 1, C, G) - c_first + 1;
-  const size_t kSlotStride = (size_t)nq * kHeads * kHeadDim;  // floats from one slot to the next
-  const float* src = p.part_o + (((size_t)(c_first + b) * nq + tq) * kHeads + h) * kHeadDim + 4 * Sh::kVec * dt;
+  const size_t kSlotStride = (size_t)P * kq * kHeads * kHeadDim;  // floats from one range's slot to the next
+  const float* src =
+      p.part_o + ((((size_t)(c_first + b) * P + grp) * kq + t) * kHeads + h) * kHeadDim + 4 * Sh::kVec * dt;
 
   pdl_wait_prior_grid();
   // first round of O loads (partials sub, sub + S, ...), before the weights
@@ -109,7 +114,8 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
     for (int i = lane; i < n; i += 32) {
       const int c = c_first + i;
       const float v =
-          cta_range_nonempty(c, C, G) ? __ldcg(p.part_lse + ((size_t)(c + b) * nq + tq) * kHeads + hh) : -INFINITY;
+          cta_range_nonempty(c, C, G) ? __ldcg(p.part_lse + ((((size_t)(c + b) * P + grp) * kq + t) * kHeads + hh))
+                                      : -INFINITY;
       w[i] = v;
       mx = fmaxf(mx, v);
     }

@@ -79,12 +79,27 @@ int plan_grid(int batch, int max_len_hint, int num_sms) {
   return (int)g;
 }
 
-// A partial slot holds the results of every query token of its sequence piece.
-void fill_plan(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan, int n_query = 1) {
-  plan->grid_ctas = plan_grid(batch, max_len_hint, num_sms);
-  plan->partial_slots = plan->grid_ctas + batch - 1;
+// Token groups of multi-token decode: a CTA serves q_per_cta query tokens, so the T tokens form
+// q_groups = ceil(T / q_per_cta) groups, and the grid holds q_groups copies of a partition of the
+// work into `ranges` ranges (q_groups CTAs read each range's pages together). A partial slot holds
+// the results of the q_per_cta tokens of its group for one sequence piece.
+struct TokenGroups {
+  int q_per_cta, q_groups;
+};
+TokenGroups token_groups(int n_query, bool quantised) {
+  TokenGroups g;
+  g.q_per_cta = (!quantised && n_query >= 2) ? 2 : 1;
+  g.q_groups = (n_query + g.q_per_cta - 1) / g.q_per_cta;
+  return g;
+}
+
+void fill_plan(int batch, int max_len_hint, int num_sms, mfa_plan_t* plan, TokenGroups tg = {1, 1}) {
+  int ranges = plan_grid(batch, max_len_hint, num_sms);
+  if (tg.q_groups > 1) ranges = std::max(1, std::min(ranges, num_sms / tg.q_groups));
+  plan->grid_ctas = ranges * tg.q_groups;
+  plan->partial_slots = (ranges + batch - 1) * tg.q_groups;
   plan->workspace_bytes =
-      kWsHeaderBytes + (size_t)plan->partial_slots * n_query * (kPartialOBytes + kPartialLseBytes);
+      kWsHeaderBytes + (size_t)plan->partial_slots * tg.q_per_cta * (kPartialOBytes + kPartialLseBytes);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -206,7 +221,7 @@ mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v
                                const int32_t* page_table, const int32_t* seq_lens, const void* out,
                                const float* lse, int batch, int max_pages, int num_pages,
                                int max_len_hint, const void* workspace, size_t workspace_bytes,
-                               int num_sms, mfa_plan_t* plan, int n_query = 1) {
+                               int num_sms, mfa_plan_t* plan, TokenGroups tg = {1, 1}) {
   if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out || !lse)
     return fail(MFA_ERR_INVALID_ARG, "null pointer argument");
   if (batch < 1 || batch > kMaxBatch) return fail(MFA_ERR_INVALID_ARG, "batch %d outside [1, %d]", batch, kMaxBatch);
@@ -218,7 +233,7 @@ mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v
     return fail(MFA_ERR_INVALID_ARG, "misaligned pointer (q, caches, out need 16 bytes)");
   if (!workspace || !aligned(workspace, 256))
     return fail(MFA_ERR_WORKSPACE, "workspace missing or not 256-byte aligned");
-  fill_plan(batch, max_len_hint, num_sms, plan, n_query);
+  fill_plan(batch, max_len_hint, num_sms, plan, tg);
   if (workspace_bytes < plan->workspace_bytes)
     return fail(MFA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, plan->workspace_bytes);
   return MFA_OK;
@@ -227,7 +242,7 @@ mfa_status_t check_decode_args(const void* q, const void* k_cache, const void* v
 DecodeParams make_decode_params(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                                 const float* v_scale, const int32_t* page_table, const int32_t* seq_lens,
                                 void* out, float* lse, float scale, int batch, int max_pages, int num_pages,
-                                void* workspace, const mfa_plan_t& plan, int n_query = 1) {
+                                void* workspace, const mfa_plan_t& plan, int n_query = 1, TokenGroups tg = {1, 1}) {
   DecodeParams p{};
   char* ws = static_cast<char*>(workspace);
   p.q = static_cast<const uint16_t*>(q);
@@ -242,7 +257,7 @@ DecodeParams make_decode_params(const void* q, const void* k_cache, const void* 
   p.err = reinterpret_cast<uint32_t*>(ws);
   p.part_o = reinterpret_cast<float*>(ws + kWsHeaderBytes);
   p.part_lse =
-      reinterpret_cast<float*>(ws + kWsHeaderBytes + (size_t)plan.partial_slots * n_query * kPartialOBytes);
+      reinterpret_cast<float*>(ws + kWsHeaderBytes + (size_t)plan.partial_slots * tg.q_per_cta * kPartialOBytes);
   p.scale = scale;
   p.B = batch;
   p.max_pages = max_pages;
@@ -250,6 +265,8 @@ DecodeParams make_decode_params(const void* q, const void* k_cache, const void* 
   p.grid = plan.grid_ctas;
   p.piece_cost = kPieceCostPages;
   p.n_query = n_query;
+  p.q_per_cta = tg.q_per_cta;
+  p.q_groups = tg.q_groups;
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   return p;
 }
@@ -307,11 +324,12 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
     return fail(MFA_ERR_INVALID_ARG, "misaligned scales (16 bytes needed)");
   mfa_plan_t plan;
+  const TokenGroups tg = token_groups(n_query, fp8);
   st = check_decode_args(q, k_cache, v_cache, page_table, seq_lens, out, lse, batch, max_pages, num_pages,
-                         max_len_hint, workspace, workspace_bytes, info.num_sms, &plan, n_query);
+                         max_len_hint, workspace, workspace_bytes, info.num_sms, &plan, tg);
   if (st != MFA_OK) return st;
   DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse,
-                                      scale, batch, max_pages, num_pages, workspace, plan, n_query);
+                                      scale, batch, max_pages, num_pages, workspace, plan, n_query, tg);
   if (fp8) p.piece_cost = kPieceCostPagesFp8;
   p.kv_fp4 = kv_fp4;
   p.block_idx = block_idx;
@@ -343,7 +361,8 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
                (st = encode_rows_bf16(&vmap, v_cache, rows)) != MFA_OK) {
       return st;
     }
-    e = n_query == 2 ? launch_decode_split_tc_mtp(p, kmap, vmap, qmap, s) : launch_decode_split_tc(p, kmap, vmap, qmap, s);
+    e = tg.q_per_cta == 2 ? launch_decode_split_tc_mtp(p, kmap, vmap, qmap, s)
+                          : launch_decode_split_tc(p, kmap, vmap, qmap, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
   if (g_prof_stop && (e = cudaEventRecordWithFlags(g_prof_stop, s, cudaEventRecordExternal)) != cudaSuccess)
@@ -384,9 +403,17 @@ size_t mfa_decode_workspace_bytes(int batch, int max_len_hint) {
 
 size_t mfa_decode_mtp_workspace_bytes(int batch, int n_query, int max_len_hint) {
   mfa_plan_t plan;
-  if (n_query < 1 || n_query > 2 || mfa_plan_decode(batch, max_len_hint, 0, &plan) != MFA_OK) return 0;
-  fill_plan(batch, max_len_hint, plan.grid_ctas, &plan, n_query);
-  return plan.workspace_bytes;
+  if (n_query < 1 || n_query > MFA_MAX_QUERY_TOKENS || mfa_plan_decode(batch, max_len_hint, 0, &plan) != MFA_OK)
+    return 0;
+  DeviceInfo info;
+  if (current_device(nullptr, &info) != MFA_OK) return 0;
+  // enough for the bf16 kernels (two tokens a CTA) and the quantised ones (one token a CTA)
+  size_t need = 0;
+  for (const bool quantised : {false, true}) {
+    fill_plan(batch, max_len_hint, info.num_sms, &plan, token_groups(n_query, quantised));
+    need = std::max(need, plan.workspace_bytes);
+  }
+  return need;
 }
 
 mfa_status_t mfa_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -530,9 +557,35 @@ mfa_status_t mfa_decode_attention_mtp(const void* q, const void* k_cache, const 
                                       const int32_t* page_table, const int32_t* seq_lens, void* out, float* lse,
                                       float scale, int batch, int n_query, int max_pages, int num_pages,
                                       int max_len_hint, void* workspace, size_t workspace_bytes, void* stream) {
-  if (n_query < 1 || n_query > 2) return fail(MFA_ERR_INVALID_ARG, "n_query %d is not 1 or 2", n_query);
+  if (n_query < 1 || n_query > MFA_MAX_QUERY_TOKENS)
+    return fail(MFA_ERR_INVALID_ARG, "n_query %d outside [1, %d]", n_query, MFA_MAX_QUERY_TOKENS);
   return decode_common(q, k_cache, v_cache, nullptr, nullptr, false, page_table, seq_lens, out, lse, scale, batch,
                        max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, n_query);
+}
+
+mfa_status_t mfa_decode_attention_mtp_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scale, const float* v_scale, const int32_t* page_table,
+                                          const int32_t* seq_lens, void* out, float* lse, float scale, int batch,
+                                          int n_query, int max_pages, int num_pages, int max_len_hint,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_query < 1 || n_query > MFA_MAX_QUERY_TOKENS)
+    return fail(MFA_ERR_INVALID_ARG, "n_query %d outside [1, %d]", n_query, MFA_MAX_QUERY_TOKENS);
+  return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, n_query);
+}
+
+mfa_status_t mfa_decode_attention_mtp_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scale, const float* v_scale, const int32_t* page_table,
+                                          const int32_t* seq_lens, void* out, float* lse, float scale, int batch,
+                                          int n_query, int max_pages, int num_pages, int max_len_hint,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_query < 1 || n_query > MFA_MAX_QUERY_TOKENS)
+    return fail(MFA_ERR_INVALID_ARG, "n_query %d outside [1, %d]", n_query, MFA_MAX_QUERY_TOKENS);
+  if (!aligned(k_cache, 32) || !aligned(v_cache, 32))
+    return fail(MFA_ERR_INVALID_ARG, "misaligned 4-bit cache (32 bytes needed)");
+  return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, n_query, nullptr,
+                       nullptr, 0, 1);
 }
 
 mfa_status_t mfa_decode_attention_blocks(const void* q, const void* k_cache, const void* v_cache,

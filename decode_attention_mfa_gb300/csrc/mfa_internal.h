@@ -73,7 +73,14 @@ struct DecodeParams {
   float scale;
   int B, max_pages, num_pages, grid;
   int piece_cost;          // cost units charged per sequence piece (work partition)
-  int n_query;             // query tokens per sequence (1, or 2 for multi-token decode); q is [B][n_query][64][256]
+  int n_query;             // query tokens per sequence (T, multi-token decode); q is [B][T][64][256]
+  // Token groups (multi-token decode): a CTA serves q_per_cta consecutive query tokens (2 on the
+  // two-token bf16 kernel, else 1), so the T tokens form q_groups = ceil(T / q_per_cta) groups. The grid
+  // is q_groups interleaved copies of the stream-K partition: CTA c works on range c / q_groups of the
+  // partition for token group c % q_groups, so the CTAs of one range read the same pages at the
+  // same time and the cache comes from HBM about once. Partial slot of (range i, sequence b, group r):
+  // (i + b) * q_groups + r, holding q_per_cta tokens.
+  int q_per_cta, q_groups;
   uint64_t wait_budget_ns;
 };
 

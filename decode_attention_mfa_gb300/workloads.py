@@ -58,6 +58,12 @@ WORKLOADS = {
     "mtp4k": Workload("mtp4k", 32, ("fixed", 4096), "bf16", True, 0, 66,
                       "B=32, L=4096, two query tokens per sequence (multi-token decode), pages randomly permuted",
                       queries=2),
+    "mtp4k_t4": Workload("mtp4k_t4", 32, ("fixed", 4096), "bf16", True, 0, 67,
+                         "B=32, L=4096, four query tokens per sequence (multi-token decode), pages randomly permuted",
+                         queries=4),
+    "mtp4k_fp8": Workload("mtp4k_fp8", 32, ("fixed", 4096), "fp8", True, 0, 68,
+                          "B=32, L=4096, E4M3 cache with per-token fp32 scales, two query tokens per sequence "
+                          "(multi-token decode), pages randomly permuted", queries=2),
     "blocks32k": Workload("blocks32k", 32, ("fixed", 32768), "bf16", True, 0, 77,
                           "B=32, L=32768, 512 selected 8-token blocks plus the last block per sequence "
                           "(4104 tokens attended, block-gather decode), pages randomly permuted",

@@ -63,6 +63,7 @@ extern "C" {
 #define MFA_MAX_BATCH 1024
 #define MFA_MAX_QUERY_BATCH 256  /* batch limit of mfa_query_lowrank */
 #define MFA_MAX_QUERY_RANK 16384 /* rank limit of mfa_query_lowrank */
+#define MFA_MAX_QUERY_TOKENS 8   /* query tokens per sequence of the multi-token decode calls */
 
 typedef enum {
   MFA_OK = 0,
@@ -234,27 +235,46 @@ mfa_status_t mfa_query_lowrank(const void* x, const void* w_down, const void* ga
                                int batch, int d_model, int rank, int n_out, float eps,
                                void* workspace, size_t workspace_bytes, void* stream);
 
-/* Multi-token (MTP) decode over a bf16 paged cache ("Step-3 is Large yet
+/* Multi-token (MTP) decode over a paged cache ("Step-3 is Large yet
  * Affordable", section 5.2: with multi-token prediction a decode step carries
- * extra predicted tokens that read the same KV cache). Each sequence has
- * n_query (1 or 2) query tokens, its last n_query positions: the cache of
+ * extra predicted tokens that read the same KV cache, which raises the
+ * attention's arithmetic intensity). Each sequence has n_query (1 to
+ * MFA_MAX_QUERY_TOKENS) query tokens, its last n_query positions: the cache of
  * seq_lens[b] tokens already holds them (mfa_kv_append with n_new = n_query).
  * Query token t attends, causally, to positions j < seq_lens[b] - n_query + 1
  * + t; a token that sees no position gets out = 0 and lse = -inf.
  *   q:   [device] bf16 [batch][n_query][64][256], 16-byte aligned
  *   out: [device] bf16 [batch][n_query][64][256]; lse: fp32 [batch][n_query][64]
- * With n_query = 2 both tokens share every pass over the cache: their 64 heads
- * each form one 128-column product with a tile of keys (and of values), so
- * the cache is read once for the two tokens. workspace: at least
- * mfa_decode_mtp_workspace_bytes(batch, n_query, max_len_hint) bytes (0 for a
- * bad argument). Host errors: MFA_ERR_INVALID_ARG also for n_query outside
- * {1, 2}. Everything else as mfa_decode_attention. */
+ * How the cache is read once for all tokens: on the bf16 cache a CTA serves two
+ * tokens (their 64 heads each form one 128-column product with a tile of keys,
+ * and of values); the quantised calls serve one token a CTA. With more tokens
+ * than one CTA serves, the tokens form groups, and the grid holds one CTA per
+ * group for every range of the work partition: the CTAs of a range stream the
+ * same pages at the same time, so the cache is read from HBM about once and
+ * shared through L2. mfa_decode_attention_mtp_fp8 / _fp4 take the E4M3 / E2M1
+ * caches and scales of mfa_decode_attention_fp8 / _fp4.
+ * workspace: at least mfa_decode_mtp_workspace_bytes(batch, n_query,
+ * max_len_hint) bytes (0 for a bad argument; it covers all three cache
+ * formats). Host errors: MFA_ERR_INVALID_ARG also for n_query outside
+ * [1, MFA_MAX_QUERY_TOKENS]. Everything else as mfa_decode_attention. */
 size_t mfa_decode_mtp_workspace_bytes(int batch, int n_query, int max_len_hint);
 mfa_status_t mfa_decode_attention_mtp(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* page_table, const int32_t* seq_lens,
                                       void* out, float* lse, float scale,
                                       int batch, int n_query, int max_pages, int num_pages, int max_len_hint,
                                       void* workspace, size_t workspace_bytes, void* stream);
+mfa_status_t mfa_decode_attention_mtp_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scale, const float* v_scale,
+                                          const int32_t* page_table, const int32_t* seq_lens,
+                                          void* out, float* lse, float scale,
+                                          int batch, int n_query, int max_pages, int num_pages, int max_len_hint,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+mfa_status_t mfa_decode_attention_mtp_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scale, const float* v_scale,
+                                          const int32_t* page_table, const int32_t* seq_lens,
+                                          void* out, float* lse, float scale,
+                                          int batch, int n_query, int max_pages, int num_pages, int max_len_hint,
+                                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* Decode attention over caller-selected 8-token blocks of a bf16 paged cache
  * ("Step-5-Preview" page, sparse attention section: the query attends to the

@@ -26,11 +26,14 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_mtp_query_count_is_checked_before_any_device_work(lib):
-    """n_query outside {1, 2}: MFA_ERR_INVALID_ARG from the host checks; the
-    workspace size query answers 0."""
-    for nq in (0, 3, -1):
+    """n_query outside [1, MFA_MAX_QUERY_TOKENS]: MFA_ERR_INVALID_ARG from the
+    host checks of all three cache formats; the workspace size query answers 0."""
+    for nq in (0, capi.MAX_QUERY_TOKENS + 1, -1):
         assert lib.mfa_decode_attention_mtp(None, None, None, None, None, None, None, 0.0625, 1, nq, 1, 1, 0,
                                             None, 0, None) == 1
+        for fn in (lib.mfa_decode_attention_mtp_fp8, lib.mfa_decode_attention_mtp_fp4):
+            assert fn(None, None, None, None, None, None, None, None, None, 0.0625, 1, nq, 1, 1, 0, None, 0,
+                      None) == 1
         assert lib.mfa_decode_mtp_workspace_bytes(4, nq, 1024) == 0
 
 
@@ -133,3 +136,56 @@ def test_partition_slots_are_unique_and_combine_finds_them(seed):
         cf, cl = _cta_of_cost(first, C, G), _cta_of_cost(first + pages[b] - 1, C, G)
         found = [c for c in range(cf, cl + 1) if _cta_lo(c, C, G) < _cta_lo(c + 1, C, G)]
         assert found == owners[b]
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_token_group_slots_are_unique_and_combine_finds_them(seed):
+    """Multi-token decode with token groups: T query tokens, q_per_cta of them
+    a CTA, so g = ceil(T / q_per_cta) groups; the grid holds g CTAs for each of
+    R ranges (CTA c: range c // g, group c % g). The piece of sequence b that
+    range i holds, for group r, is written to slot (i + b) * g + r, each slot
+    holding q_per_cta tokens. Every (sequence, token, page) is covered by
+    exactly one CTA, slots never collide and stay below (R + B - 1) * g, and
+    the combine's address for (b, token, range) is the slot that range wrote."""
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 40))
+    T = int(rng.integers(1, capi.MAX_QUERY_TOKENS + 1))
+    q_per_cta = int(rng.integers(1, 3)) if T > 1 else 1
+    g = -(-T // q_per_cta)
+    pages = rng.integers(0, 30, size=B) * (rng.random(B) < 0.9)
+    R = int(rng.integers(1, 152 // g + 1))
+    piece_cost = 1
+    cost = np.where(pages > 0, pages + piece_cost, 0)
+    C = int(cost.sum())
+    if C == 0:
+        return
+    prefix = np.concatenate([[0], np.cumsum(cost)])
+    written = {}  # (slot, token in slot) -> (b, token, pages covered)
+    covered = np.zeros((B, T), dtype=np.int64)
+    for c in range(R * g):
+        i, r = c // g, c % g
+        lo, hi = _cta_lo(i, C, R), _cta_lo(i + 1, C, R)
+        for b in range(B):
+            first = prefix[b] + piece_cost
+            pg0, pg1 = max(lo - first, 0), min(hi - first, pages[b])
+            if pages[b] == 0 or pg0 >= pg1:
+                continue
+            slot = (i + b) * g + r
+            assert slot < (R + B - 1) * g
+            for t in range(q_per_cta):
+                tau = r * q_per_cta + t
+                assert (slot, t) not in written
+                written[(slot, t)] = (b, tau)
+                if tau < T:
+                    covered[b, tau] += pg1 - pg0
+    assert (covered == pages[:, None]).all()
+    for b in range(B):
+        if pages[b] == 0:
+            continue
+        first = prefix[b] + piece_cost
+        cf, cl = _cta_of_cost(first, C, R), _cta_of_cost(first + pages[b] - 1, C, R)
+        for tau in range(T):
+            r, t = tau // q_per_cta, tau % q_per_cta
+            for i in range(cf, cl + 1):
+                if _cta_lo(i, C, R) < _cta_lo(i + 1, C, R):
+                    assert written[((i + b) * g + r, t)] == (b, tau)

@@ -36,7 +36,7 @@ def dense_rows(oracle_mod, rows_bits, lengths):
     return out
 
 
-@pytest.mark.parametrize("T", [2, 3])
+@pytest.mark.parametrize("T", [2, 3, 4, 8])
 def test_mtp_matches_masked_softmax_in_extended_precision(oracle_mod, T):
     """Explicit causal mask over the dense K/V rows, long double, no max subtraction."""
     lengths = [3, 5, 70, 129]
@@ -54,9 +54,13 @@ def test_mtp_matches_masked_softmax_in_extended_precision(oracle_mod, T):
         mask = np.arange(L)[None, :] <= (L - T + np.arange(T))[:, None]   # [T, L]: j <= position of token t
         e = np.where(mask[:, None, :], np.exp(s), 0.0)
         z = e.sum(axis=2)
-        ref = np.einsum("thj,jd->thd", e, V) / z[..., None]
-        np.testing.assert_allclose(out[b], ref.astype(np.float64), rtol=1e-11, atol=1e-13)
-        np.testing.assert_allclose(lse[b], np.log(z).astype(np.float64), rtol=0, atol=1e-12)
+        seen = z > 0  # a token whose mask is empty (L < T) sees nothing: out = 0, lse = -inf
+        with np.errstate(invalid="ignore", divide="ignore"):
+            ref = np.einsum("thj,jd->thd", e, V) / z[..., None]
+            ref_lse = np.log(z)
+        np.testing.assert_allclose(out[b][seen], ref[seen].astype(np.float64), rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(lse[b][seen], ref_lse[seen].astype(np.float64), rtol=0, atol=1e-12)
+        assert np.all(out[b][~seen] == 0) and np.all(np.isneginf(lse[b][~seen]))
 
 
 def test_mtp_with_one_token_is_single_token_decode(oracle_mod):
@@ -98,3 +102,39 @@ def test_mtp_sequence_shorter_than_the_tokens(oracle_mod):
     assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
     v0 = oracle_mod.bf16_to_f64(wl.bits(case.v_rows[:1]))[0]
     np.testing.assert_array_equal(out[0, 2], np.broadcast_to(v0, (H, D)))
+
+
+def test_mtp_on_an_e4m3_cache_is_the_masked_softmax_of_the_dequantised_rows(oracle_mod):
+    """Quantised cache: the same causal masked softmax, in long double, over
+    decode(code) * scale of every row (codes and scales from the oracle's own
+    per-token quantiser, whose codec is pinned against the OCP table)."""
+    T, lengths = 3, [2, 66, 129]
+    case, q = mtp_case(lengths, T, seed=11)
+    kcodes, kscale = oracle_mod.quantize_tokens_e4m3(wl.bits(case.k_rows))
+    vcodes, vscale = oracle_mod.quantize_tokens_e4m3(wl.bits(case.v_rows))
+    n = case.num_pages * wl.PAGE_SIZE
+    slots = wl.slots_of(case.lengths0, case.page_table)
+    kc = np.zeros((n, D), np.uint8); vc = np.zeros((n, D), np.uint8)
+    ks = np.ones(n, np.float32); vs = np.ones(n, np.float32)
+    kc[slots], vc[slots], ks[slots], vs[slots] = kcodes, vcodes, kscale, vscale
+    sl = case.lengths0.astype(np.int32)
+    out, lse = oracle_mod.mfa_decode_mtp(wl.bits(q), kc.reshape(-1, 64, D), vc.reshape(-1, 64, D), case.page_table,
+                                         sl, wl.SCALE, k_scale=ks.reshape(-1, 64), v_scale=vs.reshape(-1, 64))
+    kd = oracle_mod.e4m3_decode(kcodes).astype(np.longdouble) * kscale.astype(np.longdouble)[:, None]
+    vd = oracle_mod.e4m3_decode(vcodes).astype(np.longdouble) * vscale.astype(np.longdouble)[:, None]
+    qf = oracle_mod.bf16_to_f64(wl.bits(q)).astype(np.longdouble)
+    off = 0
+    for b, L in enumerate(lengths):
+        K, V = kd[off:off + L], vd[off:off + L]
+        off += L
+        s = np.longdouble(wl.SCALE) * np.einsum("thd,jd->thj", qf[b], K)
+        mask = np.arange(L)[None, :] <= (L - T + np.arange(T))[:, None]
+        e = np.where(mask[:, None, :], np.exp(s), 0.0)
+        z = e.sum(axis=2)
+        with np.errstate(invalid="ignore", divide="ignore"):
+            ref = np.einsum("thj,jd->thd", e, V) / z[..., None]
+            ref_lse = np.log(z)
+        seen = z > 0
+        np.testing.assert_allclose(out[b][seen], ref[seen].astype(np.float64), rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(lse[b][seen], ref_lse[seen].astype(np.float64), rtol=0, atol=1e-12)
+        assert np.all(out[b][~seen] == 0) and np.all(np.isneginf(lse[b][~seen]))
