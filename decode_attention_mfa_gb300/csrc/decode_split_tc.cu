@@ -125,7 +125,7 @@ struct Cfg<true, false> {
   static constexpr int kQ = 1;
   static constexpr int kPBufs = 2;
   static constexpr int kCols = 64;        // per-head statistics (the two terms are summed)
-  static constexpr int kHpt = 32;
+  static constexpr int kHpt = 64 / kGroups;
   static constexpr int kOHalfCols = 128;  // [term][head]
 };
 
@@ -239,7 +239,8 @@ struct Ctx {
 };
 
 // Named barriers of the softmax warps: 1 + g for warpgroup g (128 threads),
-// 3 for all of them.
+// kAllSoftmaxBarrier for all of them.
+constexpr int kAllSoftmaxBarrier = 8;
 __device__ __forceinline__ void barrier_group(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
 // The group barrier, returning the OR of `pred` over the group's threads.
 __device__ __forceinline__ bool barrier_group_or(int g, bool pred) {
@@ -253,7 +254,7 @@ __device__ __forceinline__ bool barrier_group_or(int g, bool pred) {
 }
 template <int kThreadsAll>
 __device__ __forceinline__ void barrier_softmax_all() {
-  asm volatile("bar.sync 3, %0;" ::"n"(kThreadsAll) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"n"(kAllSoftmaxBarrier), "n"(kThreadsAll) : "memory");
 }
 // 2^x with the multi-function unit's approximation (relative error below
 // 2^-22; subnormal results flush to zero, 2^-inf = 0).
@@ -995,22 +996,39 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
 // rescale decisions and named barrier.
 
 // Butterfly reduce-scatter over the warp: afterwards lane l holds the result
-// for columns (N / 32) * l + i, i < N / 32, in v[i].
+// for columns (N / 32) * l + i, i < N / 32, in v[i] (N >= 32); with N = 16,
+// lanes 2k and 2k + 1 both hold column k in v[0] (the last step is a plain
+// reduction between lane pairs).
 template <int N, bool kMax>
 __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
-  static_assert(N % 32 == 0, "columns");
+  static_assert(N % 32 == 0 || N == 16, "columns");
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
     const int half = (N / 2) >> step;
     const int o = 16 >> step;
-    const bool up = (lane & o) != 0;
+    if (half >= 1) {
+      const bool up = (lane & o) != 0;
 #pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float keep = up ? v[i + half] : v[i];
-      const float send = up ? v[i] : v[i + half];
-      const float other = __shfl_xor_sync(0xffffffffu, send, o);
-      v[i] = kMax ? fmaxf(keep, other) : keep + other;
+      for (int i = 0; i < half; ++i) {
+        const float keep = up ? v[i + half] : v[i];
+        const float send = up ? v[i] : v[i + half];
+        const float other = __shfl_xor_sync(0xffffffffu, send, o);
+        v[i] = kMax ? fmaxf(keep, other) : keep + other;
+      }
+    } else {
+      const float other = __shfl_xor_sync(0xffffffffu, v[0], o);
+      v[0] = kMax ? fmaxf(v[0], other) : v[0] + other;
     }
+  }
+}
+// Stores the reduce-scattered columns of a group's kHpt heads at dst[0 .. kHpt) (one copy each).
+template <int kHpt>
+__device__ __forceinline__ void store_scattered(float* dst, const float (&v)[kHpt], int lane) {
+  if constexpr (kHpt >= 32) {
+#pragma unroll
+    for (int i = 0; i < kHpt / 32; ++i) dst[(kHpt / 32) * lane + i] = v[i];
+  } else {
+    if ((lane & 1) == 0) dst[lane >> 1] = v[0];
   }
 }
 
@@ -1022,15 +1040,16 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
 template <bool kFp8, int kHpt>
 __device__ __forceinline__ float load_logits(uint32_t taddr, bool full, bool valid, float mult, const float* m,
                                              float (&x)[kHpt]) {
+  constexpr int kLd = kHpt < 32 ? kHpt : 32;  // columns per tcgen05.ld
 #pragma unroll
-  for (int q = 0; q < kHpt / 32; ++q) {
-    tmem_ld32(taddr + q * 32, x + q * 32);
+  for (int q = 0; q < kHpt / kLd; ++q) {
+    tmem_ld_cols<kLd>(taddr + q * kLd, x + q * kLd);
     if constexpr (kFp8) {
-      float y[32];
-      tmem_ld32(taddr + 64 + q * 32, y);
+      float y[kLd];
+      tmem_ld_cols<kLd>(taddr + 64 + q * kLd, y);
       tc_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 32; ++h) x[q * 32 + h] += y[h];
+      for (int h = 0; h < kLd; ++h) x[q * kLd + h] += y[h];
     }
   }
   if constexpr (!kFp8) tc_wait_ld();
@@ -1142,15 +1161,16 @@ __device__ __forceinline__ void scale_o_columns(uint32_t taddr_o, int h0, const 
   for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
     for (int tm = 0; tm < (kFp8 ? 2 : 1); ++tm) {
+      constexpr int kLd = kHpt < 32 ? kHpt : 32;
 #pragma unroll
-      for (int q = 0; q < kHpt / 32; ++q) {
-        const uint32_t a = taddr_o + hf * kHalfCols + tm * 64 + h0 + q * 32;
-        float o[32];
-        tmem_ld32(a, o);
+      for (int q = 0; q < kHpt / kLd; ++q) {
+        const uint32_t a = taddr_o + hf * kHalfCols + tm * 64 + h0 + q * kLd;
+        float o[kLd];
+        tmem_ld_cols<kLd>(a, o);
         tc_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) o[h] *= col_scale[q * 32 + h];
-        tmem_st32(a, o);
+        for (int h = 0; h < kLd; ++h) o[h] *= col_scale[q * kLd + h];
+        tmem_st_cols<kLd>(a, o);
       }
     }
   }
@@ -1217,22 +1237,23 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     constexpr int kHalfCols = C::kOHalfCols;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
+      constexpr int kLd = kHpt < 32 ? kHpt : 32;
 #pragma unroll
-      for (int q = 0; q < kHpt / 32; ++q) {
-        float o[32];
-        tmem_ld32(ta + hf * kHalfCols + h0 + q * 32, o);
+      for (int q = 0; q < kHpt / kLd; ++q) {
+        float o[kLd];
+        tmem_ld_cols<kLd>(ta + hf * kHalfCols + h0 + q * kLd, o);
         if constexpr (kFp8) {  // + the second P term's columns
-          float o2[32];
-          tmem_ld32(ta + hf * kHalfCols + 64 + h0 + q * 32, o2);
+          float o2[kLd];
+          tmem_ld_cols<kLd>(ta + hf * kHalfCols + 64 + h0 + q * kLd, o2);
           tc_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) o[h] += o2[h];
+          for (int h = 0; h < kLd; ++h) o[h] += o2[h];
         } else {
           tc_wait_ld();
         }
         const int dim = hf * 128 + row;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) dst[(q * 32 + h) * kHeadDim + dim] = o[h] * il[q * 32 + h];
+        for (int h = 0; h < kLd; ++h) dst[(q * kLd + h) * kHeadDim + dim] = o[h] * il[q * kLd + h];
       }
     }
     tc_fence_before();
@@ -1298,8 +1319,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
       if (barrier_group_or(g, mine)) {
         (void)load_logits<kFp8, kHpt>(taddr_s, full, valid, kmul, nullptr, x);
         warp_reduce_scatter<kHpt, true>(x, lane);  // x is reloaded below
-#pragma unroll
-        for (int i = 0; i < kHpt / 32; ++i) red[quad * kCols + h0 + (kHpt / 32) * lane + i] = x[i];
+        store_scattered<kHpt>(red + quad * kCols + h0, x, lane);
         barrier_group(g);
         if (row < kHpt) {
           const int h = h0 + row;
@@ -1385,8 +1405,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
     // LSE (final once the last P is out); O^T / l follows later (write_o)
     warp_reduce_scatter<kHpt, false>(lp, lane);
     barrier_group(g);  // earlier readers of red/alpha are done
-#pragma unroll
-    for (int i = 0; i < kHpt / 32; ++i) red[quad * kCols + h0 + (kHpt / 32) * lane + i] = lp[i];
+    store_scattered<kHpt>(red + quad * kCols + h0, lp, lane);
     barrier_group(g);
     const size_t slot = ((size_t)(c / qg) + s.b) * qg + c % qg;
     if (row < kHpt) {

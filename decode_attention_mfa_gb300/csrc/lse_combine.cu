@@ -18,17 +18,17 @@
 // there are more than 64 of them, also the partials (S interleaved subsets,
 // summed through shared memory at the end). Warp i < kH turns the partial
 // LSEs of head i into normalised weights (maximum and sum by warp shuffles).
-// The first round of partial-O loads is issued before the weights are known,
-// so the LSE and O reads overlap; a value read from a slot whose weight turns
-// out to be 0 (an empty CTA range, whose slot may hold data of an earlier
-// call, or an underflowed exponent) is discarded by a select, never scaled.
+// The partial-O rows come into shared memory by TMA bulk copies issued right
+// after the grid dependency wait, so they travel while the LSEs are read and
+// the weights formed; a row whose weight turns out to be 0 (an empty CTA
+// range, whose slot may hold data of an earlier call, or an underflowed
+// exponent) is skipped, never scaled.
 #include "mfa_device.cuh"
 
 namespace mfa {
 namespace {
 
 constexpr int kCombineThreads = 256;
-constexpr int kRound = 4;  // partials per thread and round (loads in flight)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -51,18 +51,32 @@ struct CombineShape {
   static_assert(kH <= 8, "weights are computed by warps 0 .. kH-1");
 };
 
-// At most 64 registers a thread, so four CTAs share an SM (608 on 152 SMs), which holds the whole
-// grid of batches up to 64 sequences in one wave (at 80 registers, three a SM, B = 64 took two).
+// Partial-O rows staged in shared memory per round: the rows of kChunkBytes / (kH KB) partials, brought
+// by TMA bulk copies issued right after the grid dependency wait, while warps 0 .. kH-1 read the LSEs.
+// One round covers every partial of the configurations' sequences (4K context: about 6 partials of 4
+// heads; 128K context: about 20 of one head), so the merge waits on L2 once.
+constexpr int kChunkBytes = 32 * 1024;
+
+// At most 64 registers a thread and about 36 KB of shared memory, so four CTAs share an SM (608 on 152
+// SMs), which holds the whole grid of batches up to 64 sequences in one wave.
 template <int kH>
 __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeParams p) {
   using Sh = CombineShape<kH>;
-  extern __shared__ int smem_i[];
-  int* s_len = smem_i;
-  int* s_cost = smem_i + p.B;
-  float* s_w = reinterpret_cast<float*>(smem_i + 2 * p.B + 1);  // [kH][G] normalised weights
+  constexpr int kPartBytes = kH * 1024;            // the kH heads' rows of one partial
+  constexpr int kChunk = kChunkBytes / kPartBytes;  // partials per round
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  int* s_len = reinterpret_cast<int*>(smem_raw + kChunkBytes);
+  int* s_cost = s_len + p.B;
+  float* s_w = reinterpret_cast<float*>(s_cost + p.B + 1);  // [kH][G] normalised weights
   __shared__ float s_lse[kH];
   __shared__ float4 s_acc[Sh::kSubsets > 1 ? kCombineThreads * Sh::kVec : 1];
-  // seq_lens is final before the split kernel starts; the partials are not
+  __shared__ __align__(8) uint64_t s_bar;
+  const uint32_t o_base = smem_u32(smem_raw), bar = smem_u32(&s_bar);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  // seq_lens is final before the split kernel starts; the partials are not (ends with a barrier)
   build_cost_prefix(p.seq_lens, p.B, p.max_pages * kPageSize, nullptr, p.piece_cost, s_len, s_cost, p.n_blocks,
                     p.max_blocks);
   const int nq = p.n_query;
@@ -71,7 +85,7 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
   const int hl = threadIdx.x / Sh::kThreadsPerHead;
   const int r = threadIdx.x % Sh::kThreadsPerHead;
   const int dt = r % Sh::kDimThreads, sub = r / Sh::kDimThreads;
-  const int h = blockIdx.x * kH + hl;
+  const int h0 = blockIdx.x * kH, h = h0 + hl;
   // token groups: the split ran q_groups copies of a partition into G ranges; token tq sits in group grp
   // at position t, and range c's partial of it is row ((c + b) * q_groups + grp) * q_per_cta + t
   const int P = p.q_groups, kq = p.q_per_cta, grp = tq / kq, t = tq % kq;
@@ -92,23 +106,25 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
   const long long first = (long long)s_cost[b] + p.piece_cost;
   const int c_first = cta_of_cost(first, C, G);
   const int n = cta_of_cost(first + np - 1, C, G) - c_first + 1;
-  const size_t kSlotStride = (size_t)P * kq * kHeads * kHeadDim;  // floats from one range's slot to the next
-  const float* src =
-      p.part_o + ((((size_t)(c_first + b) * P + grp) * kq + t) * kHeads + h) * kHeadDim + 4 * Sh::kVec * dt;
+  // the kH heads' rows of range c_first + i's partial (kH KB, contiguous)
+  auto part_rows = [&](int i) -> const float* {
+    return p.part_o + ((((size_t)(c_first + i + b) * P + grp) * kq + t) * kHeads + h0) * kHeadDim;
+  };
+  // round k brings partials [k kChunk, min(n, (k + 1) kChunk)); a slot of an empty range holds stale data
+  // and is copied all the same (its weight is 0)
+  // issued by warp 0, one copy a lane (kChunk <= 32), after lane 0 has announced the round's bytes
+  auto issue_round = [&](int k) {
+    const int i0 = k * kChunk, cnt = min(kChunk, n - i0);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(cnt * kPartBytes));
+    __syncwarp();
+    if (lane < cnt) bulk_load(o_base + (uint32_t)(lane * kPartBytes), part_rows(i0 + lane), kPartBytes, bar);
+  };
+  static_assert(kChunk <= 32, "one copy a lane");
 
   pdl_wait_prior_grid();
-  // first round of O loads (partials sub, sub + S, ...), before the weights
-  float4 x[kRound][Sh::kVec];
-#pragma unroll
-  for (int u = 0; u < kRound; ++u) {
-    const int i = sub + u * Sh::kSubsets;
-#pragma unroll
-    for (int v = 0; v < Sh::kVec; ++v)
-      x[u][v] = (i < n) ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)i * kSlotStride) + v)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  if (warp == 0) issue_round(0);
   if (warp < kH) {
-    const int hh = blockIdx.x * kH + warp;
+    const int hh = h0 + warp;
     float* w = s_w + warp * G;
     float mx = -INFINITY;
     for (int i = lane; i < n; i += 32) {
@@ -139,29 +155,28 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
   float4 acc[Sh::kVec];
 #pragma unroll
   for (int v = 0; v < Sh::kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = 0; i0 < n; i0 += kRound * Sh::kSubsets) {
-    if (i0 > 0) {
-#pragma unroll
-      for (int u = 0; u < kRound; ++u) {
-        const int i = i0 + sub + u * Sh::kSubsets;
-#pragma unroll
-        for (int v = 0; v < Sh::kVec; ++v)
-          x[u][v] = (i < n && w[i] != 0.0f)
-                        ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)i * kSlotStride) + v)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+  const int rounds = (n + kChunk - 1) / kChunk;
+  for (int k = 0; k < rounds; ++k) {
+    if (k > 0) {
+      __syncthreads();  // every thread is done with the previous round's rows
+      if (warp == 0) issue_round(k);
     }
-#pragma unroll
-    for (int u = 0; u < kRound; ++u) {
-      const int i = i0 + sub + u * Sh::kSubsets;
-      const float wi = (i < n) ? w[i] : 0.0f;
-      if (wi != 0.0f) {
+    // bounded; on expiry the error word records it and the output is meaningless, but every thread
+    // still reaches the barriers below
+    (void)mbar_wait(bar, k & 1, p.wait_budget_ns, nullptr, p.err);
+    const int i0 = k * kChunk, cnt = min(kChunk, n - i0);
+    for (int i = sub; i < cnt; i += Sh::kSubsets) {
+      const float wi = w[i0 + i];
+      if (wi != 0.0f) {  // a zero weight (empty range, underflow) is skipped, never scaled
+        const float4* row =
+            reinterpret_cast<const float4*>(smem_raw + i * kPartBytes + hl * 1024) + dt * Sh::kVec;
 #pragma unroll
         for (int v = 0; v < Sh::kVec; ++v) {
-          acc[v].x += wi * x[u][v].x;
-          acc[v].y += wi * x[u][v].y;
-          acc[v].z += wi * x[u][v].z;
-          acc[v].w += wi * x[u][v].w;
+          const float4 y = row[v];
+          acc[v].x = fmaf(wi, y.x, acc[v].x);
+          acc[v].y = fmaf(wi, y.y, acc[v].y);
+          acc[v].z = fmaf(wi, y.z, acc[v].z);
+          acc[v].w = fmaf(wi, y.w, acc[v].w);
         }
       }
     }
@@ -195,7 +210,10 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
 template <int kH>
 cudaError_t launch_kh(const DecodeParams& p, cudaStream_t stream) {
   dim3 grid(kHeads / kH, p.B * p.n_query);
-  const size_t smem = sizeof(int) * (2 * (size_t)p.B + 1) + sizeof(float) * (size_t)kH * p.grid;
+  const size_t smem = kChunkBytes + sizeof(int) * (2 * (size_t)p.B + 1) + sizeof(float) * (size_t)kH * p.grid;
+  static int configured[kTrackedDevices] = {};
+  const cudaError_t e = ensure_dynamic_smem(lse_combine_kernel<kH>, smem, configured);
+  if (e != cudaSuccess) return e;
   return launch_pdl(lse_combine_kernel<kH>, grid, dim3(kCombineThreads), smem, stream, p);
 }
 
