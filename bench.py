@@ -863,7 +863,7 @@ def run_qproj(args, rank_id, world, local):
     avg_us = float(np.mean(per_call)) * 1e3
     achieved = step_bytes / (avg_us * 1e-6) / 1e9
     e2e = None
-    if e2e_on:
+    if not args.no_e2e:
         hx = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
         hx.copy_(x.cpu())
         hq = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()

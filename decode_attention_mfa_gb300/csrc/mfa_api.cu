@@ -330,7 +330,7 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
   if (st != MFA_OK) return st;
   DecodeParams p = make_decode_params(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, out, lse,
                                       scale, batch, max_pages, num_pages, workspace, plan, n_query, tg);
-  if (fp8) p.piece_cost = kPieceCostPagesFp8;
+  p.piece_cost = fp8 ? kPieceCostPagesFp8 : tg.q_per_cta == 2 ? kPieceCostPagesTwoTokens : kPieceCostPages;
   p.kv_fp4 = kv_fp4;
   p.block_idx = block_idx;
   p.n_blocks = n_blocks;

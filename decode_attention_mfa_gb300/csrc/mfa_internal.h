@@ -26,8 +26,16 @@ constexpr size_t kPartialLseBytes = (size_t)kHeads * sizeof(float);
 
 // Work partition of the split kernel: besides its pages, every sequence piece
 // is charged this many page-equivalents (a CTA pays for loading Q and page
-// ids and for writing the partial result of each piece it holds).
-constexpr int kPieceCostPages = 1;
+// ids and for writing the partial result of each piece it holds, during which
+// its softmax warps stream nothing). Measured per kernel variant (a sweep of
+// 1, 2 and 3 on the bf16 workloads): the bf16 kernel's best is 2 (ragged
+// 112.8 -> 111.5 us, ctx4k unchanged) and the two-token kernel's 3 (its pieces
+// write two partials: mtp4k 41.2 -> 39.4 us). Block gather measured best at 1
+// (blocks32k 33.5 against 34.1 us) but keeps the bf16 kernel's charge, so that
+// selecting every block splits exactly like the dense call and gives the same
+// bits (a parity test relies on it).
+constexpr int kPieceCostPages = 2;
+constexpr int kPieceCostPagesTwoTokens = 3;
 // E4M3: a piece also splits Q into E4M3 terms and finds the largest V scale,
 // and a tile (two pages) streams in about half the time of a bf16 tile, so a
 // piece is worth more pages.

@@ -91,8 +91,8 @@ typedef struct {
 
 /* Split-KV planning (host only). The split kernel lays the sequences end to
  * end on a line of cost units: a sequence with n = ceil(L_b / 64) > 0 pages
- * takes n + 1 units (one unit charged per piece, then one per page), an
- * empty one none. The C units are cut into `grid_ctas` = G contiguous, equal
+ * takes n + k units (k units charged per piece, then one per page; k is a
+ * property of the kernel variant, 1 to 3), an empty one none. The C units are cut into `grid_ctas` = G contiguous, equal
  * ranges that cross sequence boundaries: CTA c owns the pages whose units lie
  * in [floor(c*C/G), floor((c+1)*C/G)) and writes one partial result per
  * sequence b it holds pages of, into slot c + b. `max_len_hint` is the expected
