@@ -300,28 +300,37 @@ def selected_positions(seq_len, blocks):
 
 
 def mfa_decode_blocks(q_bits, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks, scale, *,
-                      threads=None):
+                      k_scale=None, v_scale=None, threads=None):
     """MFA decode attention over caller-selected 8-token blocks, in fp64.
 
     The selection rule of ``selected_positions`` with the block list
     block_idx[b, :n_blocks[b]] of sequence b, applied to MFA's shared K/V head
     (the selection itself is an input). The selected rows are copied, in
     ascending position order, into a fresh paged cache of their own (a plain
-    gather), and ``mfa_decode`` runs over it with the selected count as length.
+    gather; for a quantised cache the codes and their per-token scales move
+    together), and ``mfa_decode`` runs over it with the selected count as length.
 
-    q_bits [B, H, D] uint16; caches [num_pages, 64, D] uint16 (bf16 bits);
+    q_bits [B, H, D] uint16; caches [num_pages, 64, D] uint16 (bf16 bits) or the
+    quantised formats of ``mfa_decode`` with k_scale/v_scale [num_pages, 64];
     page_table [B, max_pages], seq_lens [B], block_idx [B, max_blocks],
     n_blocks [B] int32. Returns (out [B, H, D], lse [B, H]) fp64."""
     q = _c(q_bits, np.uint16)
     B, H, D = q.shape
-    kc = _c(k_cache, np.uint16)
-    vc = _c(v_cache, np.uint16)
+    fmt = _kv_format(k_cache, D)
+    quantised = fmt != 0
+    kc = _c(k_cache, np.uint8 if quantised else np.uint16)
+    vc = _c(v_cache, np.uint8 if quantised else np.uint16)
+    if quantised and (k_scale is None or v_scale is None):
+        raise ValueError("a quantised cache needs k_scale and v_scale")
     pt = _c(page_table, np.int32)
     sl = _c(seq_lens, np.int32)
     bi = np.asarray(block_idx, dtype=np.int32).reshape(B, -1)
     nb = np.asarray(n_blocks, dtype=np.int32).reshape(B)
-    num_pages, page = kc.shape[0], kc.shape[1]
-    k_rows, v_rows = kc.reshape(-1, D), vc.reshape(-1, D)
+    num_pages, page, W = kc.shape[0], kc.shape[1], kc.shape[2]
+    k_rows, v_rows = kc.reshape(-1, W), vc.reshape(-1, W)
+    if quantised:
+        ks_rows = _c(k_scale, np.float32).reshape(-1)
+        vs_rows = _c(v_scale, np.float32).reshape(-1)
     sel = []
     for b in range(B):
         if not 0 <= nb[b] <= bi.shape[1]:
@@ -335,16 +344,24 @@ def mfa_decode_blocks(q_bits, k_cache, v_cache, page_table, seq_lens, block_idx,
     pages_of = [(n + page - 1) // page for n in lens]
     max_p = max(1, max(pages_of))
     tot = max(1, sum(pages_of))
-    gk = np.zeros((tot * page, D), dtype=np.uint16)
-    gv = np.zeros((tot * page, D), dtype=np.uint16)
+    gk = np.zeros((tot * page, W), dtype=kc.dtype)
+    gv = np.zeros((tot * page, W), dtype=vc.dtype)
+    gks = np.ones(tot * page, dtype=np.float32)
+    gvs = np.ones(tot * page, dtype=np.float32)
     gpt = np.zeros((B, max_p), dtype=np.int32)
     nxt = 0
     for b in range(B):
         gk[nxt * page:nxt * page + lens[b]] = k_rows[sel[b]]
         gv[nxt * page:nxt * page + lens[b]] = v_rows[sel[b]]
+        if quantised:
+            gks[nxt * page:nxt * page + lens[b]] = ks_rows[sel[b]]
+            gvs[nxt * page:nxt * page + lens[b]] = vs_rows[sel[b]]
         gpt[b, :pages_of[b]] = np.arange(nxt, nxt + pages_of[b])
         nxt += pages_of[b]
-    return mfa_decode(q, gk.reshape(tot, page, D), gv.reshape(tot, page, D), gpt, lens, scale, threads=threads)
+    if not quantised:
+        return mfa_decode(q, gk.reshape(tot, page, W), gv.reshape(tot, page, W), gpt, lens, scale, threads=threads)
+    return mfa_decode(q, gk.reshape(tot, page, W), gv.reshape(tot, page, W), gpt, lens, scale,
+                      k_scale=gks.reshape(tot, page), v_scale=gvs.reshape(tot, page), threads=threads)
 
 
 def query_lowrank(x_bits, w_down_bits, gamma_bits, w_up_bits, eps):

@@ -129,3 +129,70 @@ def test_draw_blocks_is_a_valid_selection():
         sel = bi[b, :nb[b]]
         assert len(set(sel.tolist())) == nb[b] and np.all((sel >= 0) & (sel < hist))
         assert np.all(bi[b, nb[b]:] == -1)
+
+
+def quantised_case(oracle_mod, lengths, kv, seed):
+    """Codes and per-token scales of the oracle's own quantiser, laid out in pages (unused slots hold the
+    format's poison and NaN scales)."""
+    w = wl.Workload("blocks-pin-q", len(lengths), ("list", tuple(lengths)), "bf16", True, 0, seed)
+    case = wl.make_case(w, lengths=lengths)
+    quant = oracle_mod.quantize_tokens_e2m1 if kv == "fp4" else oracle_mod.quantize_tokens_e4m3
+    width = D // 2 if kv == "fp4" else D
+    kcodes, kscale = quant(wl.bits(case.k_rows))
+    vcodes, vscale = quant(wl.bits(case.v_rows))
+    n = case.num_pages * wl.PAGE_SIZE
+    slots = wl.slots_of(case.lengths0, case.page_table)
+    poison = 0x77 if kv == "fp4" else 0x7F
+    kc = np.full((n, width), poison, np.uint8); vc = np.full((n, width), poison, np.uint8)
+    ks = np.full(n, np.nan, np.float32); vs = np.full(n, np.nan, np.float32)
+    kc[slots], vc[slots], ks[slots], vs[slots] = kcodes, vcodes, kscale, vscale
+    shape = (case.num_pages, wl.PAGE_SIZE)
+    return case, kc.reshape(shape + (width,)), vc.reshape(shape + (width,)), ks.reshape(shape), vs.reshape(shape)
+
+
+@pytest.mark.parametrize("kv", ["fp8", "fp4"])
+def test_every_block_on_a_quantised_cache_is_dense_decode(oracle_mod, kv):
+    """E4M3 / E2M1 cache: the codes and their scales are gathered together, so
+    selecting every block is the dense quantised decode, bit for bit."""
+    lengths = [1, 9, 65, 200, 513]
+    case, kc, vc, ks, vs = quantised_case(oracle_mod, lengths, kv, seed=21)
+    hist = [(L - 1) // 8 for L in lengths]
+    bi = np.full((len(lengths), max(hist)), -1, dtype=np.int32)
+    for b, n in enumerate(hist):
+        bi[b, :n] = np.arange(n)
+    sl = case.lengths0.astype(np.int32)
+    out, lse = oracle_mod.mfa_decode_blocks(wl.bits(case.q), kc, vc, case.page_table, sl, bi,
+                                            np.array(hist, dtype=np.int32), wl.SCALE, k_scale=ks, v_scale=vs)
+    ref, ref_lse = oracle_mod.mfa_decode(wl.bits(case.q), kc, vc, case.page_table, sl, wl.SCALE, k_scale=ks,
+                                         v_scale=vs)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)
+
+
+def test_quantised_selection_ignores_other_rows(oracle_mod):
+    """E4M3: poisoning every code and scale outside the selection (NaN codes, NaN scales) changes nothing,
+    and the result is the masked softmax of the dequantised selected rows in extended precision."""
+    lengths = [300, 777]
+    case, kc, vc, ks, vs = quantised_case(oracle_mod, lengths, "fp8", seed=22)
+    bi, nb = wl.draw_blocks(lengths, 12, [22])
+    sl = case.lengths0.astype(np.int32)
+    out, lse = oracle_mod.mfa_decode_blocks(wl.bits(case.q), kc, vc, case.page_table, sl, bi, nb, wl.SCALE,
+                                            k_scale=ks, v_scale=vs)
+    kc2, vc2, ks2, vs2 = kc.copy(), vc.copy(), ks.copy(), vs.copy()
+    qf = oracle_mod.bf16_to_f64(wl.bits(case.q)).astype(np.longdouble)
+    for b, L in enumerate(lengths):
+        pos = oracle_mod.selected_positions(L, bi[b, :nb[b]])
+        keep = np.zeros(L, bool); keep[pos] = True
+        for j in np.nonzero(~keep)[0]:
+            page, row = case.page_table[b][j // 64], j % 64
+            kc2[page, row] = 0x7F; vc2[page, row] = 0x7F; ks2[page, row] = np.nan; vs2[page, row] = np.nan
+        # extended-precision reference over the selected rows
+        pg, rw = case.page_table[b][pos // 64], pos % 64
+        K = oracle_mod.e4m3_decode(kc[pg, rw]).astype(np.longdouble) * ks[pg, rw].astype(np.longdouble)[:, None]
+        V = oracle_mod.e4m3_decode(vc[pg, rw]).astype(np.longdouble) * vs[pg, rw].astype(np.longdouble)[:, None]
+        e = np.exp(np.longdouble(wl.SCALE) * (qf[b] @ K.T))
+        z = e.sum(axis=1)
+        np.testing.assert_allclose(out[b], ((e @ V) / z[:, None]).astype(np.float64), rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(lse[b], np.log(z).astype(np.float64), rtol=0, atol=1e-12)
+    out2, lse2 = oracle_mod.mfa_decode_blocks(wl.bits(case.q), kc2, vc2, case.page_table, sl, bi, nb, wl.SCALE,
+                                              k_scale=ks2, v_scale=vs2)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
