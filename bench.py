@@ -155,7 +155,8 @@ def arm_config(w: wl.Workload, world: int) -> dict:
             "head_dim": wl.HEAD_DIM, "page_size": wl.PAGE_SIZE, "kv_dtype": w.kv_dtype,
             "queries_per_sequence": w.queries,
             "step": ("mfa_kv_append(1 token/seq) + " if app else "") +
-                    ("mfa_decode_attention_blocks" if blocks else
+                    (("mfa_decode_attention_blocks_fp8" if w.kv_dtype == "fp8" else "mfa_decode_attention_blocks")
+                     if blocks else
                      ("mfa_decode_attention_mtp" + {"fp8": "_fp8", "fp4": "_fp4"}.get(w.kv_dtype, "")
                       + f" (n_query={w.queries})") if w.queries > 1 else
                      "mfa_decode_attention_fp4" if w.kv_dtype == "fp4" else
@@ -337,7 +338,12 @@ def run_ours(args, rank, world, local, workload=None, region_s=None, with_e2e=No
             if app:
                 append_q(kn, vn, 1, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table,
                                        sl, B, max_pages, num_pages, workspace, stream)
-            if nq > 1:
+            if blocks:
+                capi.mfa_decode_attention_blocks_fp8(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r],
+                                                     page_table, sl, block_idx, n_blocks, block_idx.shape[1], out,
+                                                     lse, wl.SCALE, B, max_pages, num_pages, ws_hint, workspace,
+                                                     ws_bytes, stream)
+            elif nq > 1:
                 mtp_q(qq, k_caches[r], v_caches[r], k_scales[r], v_scales[r], page_table, sl, out, lse, wl.SCALE, B,
                       nq, max_pages, num_pages, ws_hint, workspace, ws_bytes, stream)
             else:
@@ -668,16 +674,29 @@ class BlockOracleSampler:
     def _prepare(self, n):
         if self.inputs is None or self.inputs[0] < n:
             case = wl.make_case(self.w, lengths=self.lens[:n], headroom_tokens=0)
-            kc = wl.bits(wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
-            vc = wl.bits(wl.scatter_rows(case.v_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
-            self.inputs = (n, wl.bits(case.q), kc, vc, case.page_table)
+            ks = vs = None
+            if self.w.kv_dtype == "fp8":  # the oracle's own per-token E4M3 quantiser
+                kcodes, kscale = self.oracle.quantize_tokens_e4m3(wl.bits(case.k_rows))
+                vcodes, vscale = self.oracle.quantize_tokens_e4m3(wl.bits(case.v_rows))
+                slots = wl.slots_of(case.lengths0, case.page_table)
+                rows = case.num_pages * wl.PAGE_SIZE
+                kc = np.zeros((rows, wl.HEAD_DIM), np.uint8); kc[slots] = kcodes
+                vc = np.zeros((rows, wl.HEAD_DIM), np.uint8); vc[slots] = vcodes
+                ks = np.ones(rows, np.float32); ks[slots] = kscale
+                vs = np.ones(rows, np.float32); vs[slots] = vscale
+                shape = (case.num_pages, wl.PAGE_SIZE)
+                kc, vc, ks, vs = kc.reshape(shape + (-1,)), vc.reshape(shape + (-1,)), ks.reshape(shape), vs.reshape(shape)
+            else:
+                kc = wl.bits(wl.scatter_rows(case.k_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
+                vc = wl.bits(wl.scatter_rows(case.v_rows, case.lengths0, case.page_table, case.num_pages, fill=0.0))
+            self.inputs = (n, wl.bits(case.q), kc, vc, ks, vs, case.page_table)
         return self.inputs
 
     def run(self, n: int) -> float:
-        _, q, kc, vc, pt = self._prepare(n)
+        _, q, kc, vc, ks, vs, pt = self._prepare(n)
         t = time.perf_counter()
         self.oracle.mfa_decode_blocks(q[:n], kc, vc, pt[:n], self.lens[:n].astype(np.int32), self.bi[:n],
-                                      self.nb[:n], wl.SCALE, threads=self.threads)
+                                      self.nb[:n], wl.SCALE, k_scale=ks, v_scale=vs, threads=self.threads)
         return time.perf_counter() - t
 
     def rows_for(self, budget_s: float) -> int:

@@ -56,6 +56,8 @@ _SIGNATURES = {
     "mfa_decode_attention_mtp_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_mtp_fp4": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _Z, _P], _I),
     "mfa_decode_attention_blocks": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _F, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "mfa_decode_attention_blocks_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _F, _I, _I, _I, _I, _P, _Z,
+                                         _P], _I),
     "mfa_check_device_errors": ([_P, _I, _P], _I),
     "mfa_set_wait_budget_ns": ([_U64], None),
     "mfa_selftest_wait_timeout": ([_P, _U64, _P], _I),
@@ -255,6 +257,17 @@ def mfa_decode_attention_noalloc(q, k_cache, v_cache, page_table, seq_lens, out,
                                                _ptr(seq_lens), _ptr(out), _ptr(lse), float(scale), batch,
                                                max_pages, num_pages, max_len_hint, _ptr(device_error_word),
                                                _stream(stream)))
+
+
+def mfa_decode_attention_blocks_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, block_idx,
+                                    n_blocks, max_blocks, out, lse, scale, batch, max_pages, num_pages, max_len_hint,
+                                    workspace, workspace_bytes, stream=None):
+    """Block gather over an E4M3 cache with per-token fp32 scales."""
+    _check(load().mfa_decode_attention_blocks_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                                  _ptr(v_scale), _ptr(page_table), _ptr(seq_lens), _ptr(block_idx),
+                                                  _ptr(n_blocks), max_blocks, _ptr(out), _ptr(lse), float(scale),
+                                                  batch, max_pages, num_pages, max_len_hint, _ptr(workspace),
+                                                  workspace_bytes, _stream(stream)))
 
 
 def mfa_check_device_errors(workspace, clear: bool = True, stream=None):

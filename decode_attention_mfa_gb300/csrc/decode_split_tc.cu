@@ -386,7 +386,7 @@ struct BlockRows {
 // tile t >= 1 those of K(t) and V(t-1), then V(T-1) -- the order in which the
 // MMA warp consumes them (bf16). E4M3: Q, then per tile the raw K tile and
 // its scale block (the V pages come from the V producer warp).
-template <bool kFp8, bool kMtp>
+template <bool kFp8, bool kMtp, bool kGather8 = false>
 __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               const CUtensorMap* qmap, const Ctx& cx, const int* s_cost, const int* s_len,
                               long long lo, long long hi) {
@@ -517,7 +517,61 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
   auto issue_v_blocks_tile = [&](int row, bool two_pages) -> bool {
     return issue_v_pair(0, row) && (!two_pages || issue_v_pair(1, row));
   };
+  uint32_t vc = 0;  // E4M3 block gather: V stages issued by this warp
+  // E4M3 block gather. A K tile is staged as [block j][128-dim half h][8 rows x 128 B] (block j at 2 KB * j,
+  // one 3-D copy of 2 KB per block: both halves of its 8 rows), the S^T MMA taking 2 KB between 8-row
+  // groups; the tile's scale block receives each block's 8 K and 8 V scales (32 B each) at 32 B * j.
+  // Lane j < 16 holds the cache row of block j of the tile (-1 past the end).
+  auto stage_k_blocks = [&](int row) -> bool {
+    uint32_t dst, bar;
+    if (!wait_slot(dst, bar)) return false;
+    const bool mine = lane < 16 && row >= 0;
+    const uint32_t n = __popc(__ballot_sync(0xffffffffu, mine));
+    if (lane == 0) mbar_arrive_expect_tx(bar, n * 2048u);
+    __syncwarp();
+    if (mine) tma_load_3d(dst + lane * 2048, kmap, 0, row, 0, bar, pol_stream);
+    ++cc;
+    return true;
+  };
+  auto stage_block_scales = [&](int row) -> bool {
+    constexpr uint32_t kRingSc = C::kScaleSlots > 0 ? C::kScaleSlots : 1;
+    const uint32_t slot = sc_cnt % kRingSc, n = sc_cnt / kRingSc;
+    const bool r = cx.wait(Bb::ScEmpty + slot, (n & 1) ^ 1);
+    __syncwarp();
+    if (!r) return false;
+    const bool mine = lane < 16 && row >= 0;
+    const uint32_t nb = __popc(__ballot_sync(0xffffffffu, mine));
+    const uint32_t dst = cx.base + L.scales + slot * kScaleBytes, bar = cx.bar(Bb::ScFull + slot);
+    if (lane == 0) mbar_arrive_expect_tx(bar, nb * 64u);
+    __syncwarp();
+    if (mine) {
+      bulk_load(dst + lane * 32, p.k_scale + row, 32u, bar);
+      bulk_load(dst + 512 + lane * 32, p.v_scale + row, 32u, bar);
+    }
+    ++sc_cnt;
+    return true;
+  };
+  // virtual page i (blocks 8i .. 8i + 7 of the tile) of V as [block][half][8 rows x 128 B]; a block past the
+  // end is read from above the top of the cache, which fills it with zeros (0 * NaN would poison P.V)
+  auto stage_v_blocks = [&](int i, int row) -> bool {
+    const uint32_t slot = C::kKStages + vc % (C::kVStages > 0 ? C::kVStages : 1);
+    const uint32_t n = vc / (C::kVStages > 0 ? C::kVStages : 1);
+    const bool r = cx.wait(Bb::StEmpty + slot, (n & 1) ^ 1);
+    __syncwarp();
+    if (!r) return false;
+    const uint32_t dst = cx.base + L.stage + C::kKStages * kKTileBytes +
+                         (vc % (C::kVStages > 0 ? C::kVStages : 1)) * kStageBytes;
+    const uint32_t bar = cx.bar(Bb::StFull + slot);
+    if (lane == 0) mbar_arrive_expect_tx(bar, 8u * 2048u);
+    __syncwarp();
+    if (lane >= 8 * i && lane < 8 * i + 8)
+      tma_load_3d(dst + (uint32_t)(lane - 8 * i) * 2048u, vmap, 0, row >= 0 ? row : -8, 0, bar, pol_stream);
+    ++vc;
+    return true;
+  };
   const bool gather = !kFp8 && !kMtp && p.block_idx != nullptr;
+  constexpr bool gather8 = kGather8;  // E4M3 block gather (its own instantiation): this warp stages V as well
+  static_assert(!kGather8 || (kFp8 && !kMtp), "block gather instantiation of the E4M3 kernel only");
   int pend_row = -1;  // gather: this lane's block row of the tile whose V is still to be issued
   bool pend_two = false, pend_valid = false;
   int pend_a = -1, pend_b = -1;  // pages of the tile whose V is still to be issued (tile stream)
@@ -528,9 +582,9 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     PageIds ids;
     ids.row = p.page_table + (size_t)s.b * p.max_pages;
     ids.pg1 = s.pg1;
-    if (!gather) ids.start(s.pg0, p, lane);
+    if (!gather && !kGather8) ids.start(s.pg0, p, lane);
     BlockRows blk;
-    if (gather) blk.start(s, p);
+    if (gather || kGather8) blk.start(s, p);
     // Q of this sequence; its buffer is free once every S MMA of the piece that
     // last used it is done (with two buffers the loads of this piece need not
     // wait for the previous piece to finish)
@@ -586,6 +640,26 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
         pend_a = pa;
         pend_b = pb;
       }
+    } else if constexpr (kGather8) {
+      // K(t) and its scales, then V(t - 1), in the MMA warp's per-piece order; the block rows of tile t + 1
+      // and the block ids of tile t + 2 are in flight meanwhile
+      int pos0, pos1;
+      const int r0 = blk.block_id(0, lane), r1 = blk.block_id(1, lane);
+      const int id0 = blk.page_id(0, lane, r0, pos0, p);
+      int id1 = blk.page_id(1, lane, r1, pos1, p);
+      int r2 = blk.block_id(2, lane);
+      int row = blk.row(id0, pos0, p), prev_row = -1;
+      for (int t = 0; good && t <= T; ++t) {
+        if (t < T) good = stage_k_blocks(row) && stage_block_scales(row);
+        if (good && t > 0) {
+          const int np = pages_in_tile(s, t - 1);
+          for (int i = 0; good && i < np; ++i) good = stage_v_blocks(i, prev_row);
+        }
+        prev_row = row;
+        row = blk.row(id1, pos1, p);
+        id1 = blk.page_id(t + 2, lane, r2, pos1, p);
+        r2 = blk.block_id(t + 3, lane);
+      }
     } else {
     for (int t = 0; good && t <= T; ++t) {
       if (t < T) {
@@ -627,6 +701,11 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
       for (uint32_t k = (sc_cnt > (uint32_t)C::kScaleSlots ? sc_cnt - C::kScaleSlots : 0); k < sc_cnt; ++k)
         (void)mbar_wait(cx.bar(Bb::ScFull + k % C::kScaleSlots), (k / C::kScaleSlots) & 1, cx.budget, nullptr,
                         p.err);
+      if constexpr (kGather8) {  // the V stages this warp issued
+        for (uint32_t k = (vc > (uint32_t)C::kVStages ? vc - C::kVStages : 0); k < vc; ++k)
+          (void)mbar_wait(cx.bar(Bb::StFull + C::kKStages + k % C::kVStages), (k / C::kVStages) & 1, cx.budget,
+                          nullptr, p.err);
+      }
     }
     if (issued_q) (void)mbar_wait(cx.bar(Bb::QFull + last_qb), last_q_parity, cx.budget, nullptr, p.err);
   }
@@ -680,6 +759,7 @@ __device__ void producer_v_role(const DecodeParams& p, const CUtensorMap* vmap, 
 // E4M3: the largest V scale of each sequence piece (vref), published for the
 // softmax warps before they form the piece's first P (two slots, so this warp
 // works up to two pieces ahead).
+template <bool kGather8>
 __device__ void vref_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len, long long lo,
                           long long hi, float* s_vref) {
   using Bb = Bars<true>;
@@ -693,7 +773,43 @@ __device__ void vref_role(const DecodeParams& p, const Ctx& cx, const int* s_cos
     // lane i takes page g + i of each group of 32: its 64 scales in 16 vector loads
     const int32_t* row = p.page_table + (size_t)s.b * p.max_pages;
     float mx = 0.0f;
-    for (int g = s.pg0; g < s.pg1; g += 32) {
+    if constexpr (kGather8) {
+      // block gather: the piece's virtual blocks [8 pg0, 8 pg1) -- the selected blocks, then the block of the
+      // last token -- four a lane per round (block id, page id, then its 8 scales); a bad block or page id
+      // (reported by the producer) is read as block 0 / page 0, as the producer reads it
+      const int len = clamp_len(__ldg(p.seq_lens + s.b), p.max_pages * kPageSize, nullptr);
+      const int nb = selected_blocks(len, p.n_blocks, s.b, p.max_blocks, nullptr);
+      const int cur = (len - 1) >> 3, nvb = len > 0 ? nb + 1 : 0;
+      const int vb_hi = min(8 * s.pg1, nvb);
+      const int32_t* bidx = p.block_idx + (size_t)s.b * p.max_blocks;
+      for (int vb0 = 8 * s.pg0; vb0 < vb_hi; vb0 += 128) {
+        int r[4], id[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int vb = vb0 + 32 * u + lane;
+          r[u] = vb < vb_hi ? (vb < nb ? __ldg(bidx + vb) : cur) : -1;
+          if (vb < nb && (r[u] < 0 || r[u] >= cur)) r[u] = 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          id[u] = r[u] >= 0 ? __ldg(row + ((8 * r[u]) >> 6)) : 0;
+          if (id[u] < 0 || id[u] >= p.num_pages) id[u] = 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (r[u] < 0) continue;
+          const int vb = vb0 + 32 * u + lane;
+          const int cnt = vb < nb ? 8 : len - 8 * cur;  // rows of the block that hold tokens
+          const float4* sc = reinterpret_cast<const float4*>(p.v_scale + (size_t)id[u] * kPageSize + ((8 * r[u]) & 63));
+          const float4 a = __ldg(sc), b4 = __ldg(sc + 1);
+          const float v8[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (k < cnt) mx = fmaxf(mx, v8[k]);
+        }
+      }
+    }
+    for (int g = s.pg0; !kGather8 && g < s.pg1; g += 32) {
       const int pg = g + lane;
       if (pg < s.pg1) {
         const int id = __ldg(row + pg);
@@ -738,7 +854,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4 v) {
 }
 
 // ---------------------------------------------------------------- MMA issue
-template <bool kFp8, bool kMtp>
+template <bool kFp8, bool kMtp, bool kGather8 = false>
 __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost, const int* s_len, long long lo,
                          long long hi, uint32_t tmem) {
   using C = Cfg<kFp8, kMtp>;
@@ -761,6 +877,7 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
   const uint32_t idesc_a_fmt = p.kv_fp4 ? kIdescAE2M1 : 0u;  // E4M3 kernel on a 4-bit cache
   // block gather: operand chunks are pairs of adjacent ring slots, in the producer's sequence
   const bool gather = !kFp8 && !kMtp && p.block_idx != nullptr;
+  constexpr bool gather8 = kGather8;  // E4M3 block gather: [block][half] staging
   auto next_pair = [&](uint32_t& slot, uint32_t& ph) {
     if (cc % C::kSlots == C::kSlots - 1) ++cc;
     slot = cc % C::kSlots;
@@ -781,12 +898,21 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         tc_fence_after();
         const uint32_t ka = cx.base + L.stage + kslot * kKTileBytes;
         const uint32_t qa = cx.base + L.q + qb * C::kQ * kQBytes;
+        if constexpr (gather8) {  // block gather: [block][half][8 rows]: half h at 1 KB * h, 8-row groups 2 KB apart
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_f8(d_tmem, smem_desc(ka + h * 16384 + ks * 32, 16, 1024, 2),
-                      smem_desc(qa + h * 16384 + ks * 32, 16, 1024, 2), idesc_s_e4m3() | idesc_a_fmt, (h | ks) != 0);
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_f8(d_tmem, smem_desc(ka + h * 1024 + ks * 32, 16, 2048, 2),
+                        smem_desc(qa + h * 16384 + ks * 32, 16, 1024, 2), idesc_s_e4m3() | idesc_a_fmt, (h | ks) != 0);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_f8(d_tmem, smem_desc(ka + h * 16384 + ks * 32, 16, 1024, 2),
+                        smem_desc(qa + h * 16384 + ks * 32, 16, 1024, 2), idesc_s_e4m3() | idesc_a_fmt, (h | ks) != 0);
+        }
         tc_commit(cx.bar(Bb::StEmpty + kslot));
         tc_commit(cx.bar(Bb::SFull + buf));
       }
@@ -859,7 +985,18 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         const uint32_t vslot = C::kKStages + (vc + i) % C::kVStages;
         if (!wait_all(Bb::StFull + vslot, ((vc + i) / C::kVStages) & 1)) return false;
         vs[i] = cx.base + L.stage + C::kKStages * kKTileBytes + ((vc + i) % C::kVStages) * kStageBytes;
-        if (nv < kPageSize && !p.kv_fp4) {  // E2M1 has no NaN code: a 4-bit page needs no zeroing
+        if constexpr (gather8) {
+          // blocks past the end arrived as zeros; the rows past the last token inside the last block hold
+          // other tokens' codes (possibly 0x7F, NaN): zero them ([block][half][8 rows x 128 B] layout)
+          const int nz = min(kPageSize, (nv + 7) & ~7);
+          if (nv < nz) {
+            for (int r = nv; r < nz; ++r)
+              for (int hf = 0; hf < 2; ++hf)
+                for (int off = 0; off < 128; off += 16)
+                  st_shared_v4(vs[i] + (r >> 3) * 2048 + hf * 1024 + (r & 7) * 128 + off, make_uint4(0u, 0u, 0u, 0u));
+            fence_proxy_async_smem();
+          }
+        } else if (nv < kPageSize && !p.kv_fp4) {  // E2M1 has no NaN code: a 4-bit page needs no zeroing
           // rows [nv, 64) of both boxes (whole 128 B rows): code 0x7F is NaN and 0 * NaN would poison P.V
           const int nbytes = (kPageSize - nv) * 128;
           for (int off = 0; off < nbytes; off += 16) {
@@ -873,13 +1010,23 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         tc_fence_after();
         for (int i = 0; i < np; ++i) {
           const uint32_t bp = cx.base + L.p + buf * C::kQ * kPBytes + i * 8192;  // token rows 64i..
+          if constexpr (gather8) {  // block gather: [block][half][8 rows], 8-token groups 2 KB apart
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
+            for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks)
-              tc_mma_f8(tmem + tmem_o<kFp8, kMtp>() + hf * 128, smem_desc(vs[i] + hf * 8192 + ks * 4096, 16, 1024, 2),
-                        smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3() | idesc_a_fmt,
-                        !(first_of_seg && i == 0 && ks == 0));
+              for (int ks = 0; ks < 2; ++ks)
+                tc_mma_f8(tmem + tmem_o<kFp8, kMtp>() + hf * 128, smem_desc(vs[i] + hf * 1024 + ks * 8192, 16, 2048, 2),
+                          smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3() | idesc_a_fmt,
+                          !(first_of_seg && i == 0 && ks == 0));
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+              for (int ks = 0; ks < 2; ++ks)
+                tc_mma_f8(tmem + tmem_o<kFp8, kMtp>() + hf * 128, smem_desc(vs[i] + hf * 8192 + ks * 4096, 16, 1024, 2),
+                          smem_desc(bp + ks * 4096, 16, 1024, 2), idesc_o_e4m3() | idesc_a_fmt,
+                          !(first_of_seg && i == 0 && ks == 0));
+          }
           // the V page's stage is free once these MMAs are done
           tc_commit(cx.bar(Bb::StEmpty + C::kKStages + (vc + i) % C::kVStages));
         }
@@ -1424,7 +1571,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
   if (pend) (void)write_o();
 }
 
-template <bool kFp8, bool kMtp>
+template <bool kFp8, bool kMtp, bool kGather8 = false>
 __global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads, 1)
     decode_split_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap) {
@@ -1511,14 +1658,15 @@ __global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads, 1)
   if (warp < 4 * C::kGroups) {
     softmax_role<kFp8, kMtp>(p, cx, s_cost, s_len, lo, hi, tmem, c, gbase);
   } else if (warp == C::kProducerWarp) {
-    producer_role<kFp8, kMtp>(p, &kmap, &vmap, &qmap, cx, s_cost, s_len, lo, hi);
+    producer_role<kFp8, kMtp, kGather8>(p, &kmap, &vmap, &qmap, cx, s_cost, s_len, lo, hi);
   } else if (warp == C::kMmaWarp) {
-    if ((threadIdx.x & 31) == 0) mma_role<kFp8, kMtp>(p, cx, s_cost, s_len, lo, hi, tmem);
+    if ((threadIdx.x & 31) == 0) mma_role<kFp8, kMtp, kGather8>(p, cx, s_cost, s_len, lo, hi, tmem);
   } else if constexpr (kFp8) {
-    if (warp == C::kVProducerWarp)
-      producer_v_role(p, &vmap, cx, s_cost, s_len, lo, hi);
+    if (warp == C::kVProducerWarp) {
+      if constexpr (!kGather8) producer_v_role(p, &vmap, cx, s_cost, s_len, lo, hi);  // gather: the K producer
+    }
     else if (warp == C::kVRefWarp)
-      vref_role(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 9 * C::kCols);
+      vref_role<kGather8>(p, cx, s_cost, s_len, lo, hi, reinterpret_cast<float*>(gbase + L.red) + 9 * C::kCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -1527,14 +1675,15 @@ __global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
 }
 
-template <bool kFp8, bool kMtp>
+template <bool kFp8, bool kMtp, bool kGather8 = false>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, cudaStream_t stream) {
   const size_t smem = (size_t)smem_layout<kFp8, kMtp>(p.B).total + 1024;
   static int configured[kTrackedDevices] = {};  // largest opt-in set so far, per device
-  const cudaError_t e = ensure_dynamic_smem(decode_split_tc_kernel<kFp8, kMtp>, smem, configured);
+  const cudaError_t e = ensure_dynamic_smem(decode_split_tc_kernel<kFp8, kMtp, kGather8>, smem, configured);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_split_tc_kernel<kFp8, kMtp>, dim3(p.grid), dim3(Cfg<kFp8, kMtp>::kThreads), smem, stream, p, kmap,
+  return launch_pdl(decode_split_tc_kernel<kFp8, kMtp, kGather8>, dim3(p.grid), dim3(Cfg<kFp8, kMtp>::kThreads), smem,
+                    stream, p, kmap,
                     vmap, qmap);
 }
 
@@ -1552,6 +1701,11 @@ cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& kma
 cudaError_t launch_decode_split_tc_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                        const CUtensorMap& qmap, cudaStream_t stream) {
   return launch_tc<true, false>(p, kmap, vmap, qmap, stream);
+}
+
+cudaError_t launch_decode_split_tc_fp8_blocks(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                              const CUtensorMap& qmap, cudaStream_t stream) {
+  return launch_tc<true, false, true>(p, kmap, vmap, qmap, stream);
 }
 
 cudaError_t launch_decode_split_tc_mtp(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -179,6 +179,24 @@ mfa_status_t encode_blocks_bf16(CUtensorMap* map, const void* base, uint64_t row
   return MFA_OK;
 }
 
+// Block gather on an E4M3 cache: the cache [rows][256] bytes viewed as 3-D -- x = the 128 bytes of a
+// 128-dim half, y = row (256-byte stride), z = half (128-byte stride) -- read in boxes of 8 rows x both
+// halves, which land as two swizzle atoms [8 rows x 128 B], half 0 then half 1 (2 KB per block).
+mfa_status_t encode_blocks_e4m3(CUtensorMap* map, const void* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  mfa_status_t st = get_encoder(&enc);
+  if (st != MFA_OK) return st;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)rows, 2};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim, 128};
+  const cuuint32_t box[3] = {128, 8, 2};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MFA_ERR_CUDA, "cuTensorMapEncodeTiled (E4M3 block view) failed (%d)", (int)r);
+  return MFA_OK;
+}
+
 // 2-D byte tensor [rows][256] (E4M3 codes) read in [64 rows x 128 bytes]
 // boxes with the 128-byte swizzle.
 mfa_status_t encode_rows_e4m3(CUtensorMap* map, const void* base, uint64_t rows) {
@@ -347,11 +365,15 @@ mfa_status_t decode_common(const void* q, const void* k_cache, const void* v_cac
       if ((st = encode_rows_e2m1(&kmap, k_cache, rows)) != MFA_OK ||
           (st = encode_rows_e2m1(&vmap, v_cache, rows)) != MFA_OK)
         return st;
+    } else if (block_idx) {  // block gather: one 8-row box of both halves per block
+      if ((st = encode_blocks_e4m3(&kmap, k_cache, rows)) != MFA_OK ||
+          (st = encode_blocks_e4m3(&vmap, v_cache, rows)) != MFA_OK)
+        return st;
     } else if ((st = encode_rows_e4m3(&kmap, k_cache, rows)) != MFA_OK ||
                (st = encode_rows_e4m3(&vmap, v_cache, rows)) != MFA_OK) {
       return st;
     }
-    e = launch_decode_split_tc_fp8(p, kmap, vmap, qmap, s);
+    e = block_idx ? launch_decode_split_tc_fp8_blocks(p, kmap, vmap, qmap, s) : launch_decode_split_tc_fp8(p, kmap, vmap, qmap, s);
   } else {
     if (block_idx) {  // block gather: one 8-token block per box, K by column-block pairs, V whole
       if ((st = encode_blocks_bf16(&kmap, k_cache, rows, 2)) != MFA_OK ||
@@ -598,6 +620,21 @@ mfa_status_t mfa_decode_attention_blocks(const void* q, const void* k_cache, con
   if (max_blocks < 1 || (long long)max_blocks > (long long)max_pages * (kPageSize / 8))
     return fail(MFA_ERR_INVALID_ARG, "max_blocks %d outside [1, 8 * max_pages]", max_blocks);
   return decode_common(q, k_cache, v_cache, nullptr, nullptr, false, page_table, seq_lens, out, lse, scale, batch,
+                       max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, 1, block_idx,
+                       n_blocks, max_blocks);
+}
+
+mfa_status_t mfa_decode_attention_blocks_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                             const float* k_scale, const float* v_scale, const int32_t* page_table,
+                                             const int32_t* seq_lens, const int32_t* block_idx,
+                                             const int32_t* n_blocks, int max_blocks, void* out, float* lse,
+                                             float scale, int batch, int max_pages, int num_pages, int max_len_hint,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (!block_idx || !n_blocks) return fail(MFA_ERR_INVALID_ARG, "null block_idx or n_blocks");
+  if (!aligned(block_idx, 4) || !aligned(n_blocks, 4)) return fail(MFA_ERR_INVALID_ARG, "misaligned block lists");
+  if (max_blocks < 1 || (long long)max_blocks > (long long)max_pages * (kPageSize / 8))
+    return fail(MFA_ERR_INVALID_ARG, "max_blocks %d outside [1, 8 * max_pages]", max_blocks);
+  return decode_common(q, k_cache, v_cache, k_scale, v_scale, true, page_table, seq_lens, out, lse, scale, batch,
                        max_pages, num_pages, max_len_hint, workspace, workspace_bytes, stream, 1, block_idx,
                        n_blocks, max_blocks);
 }

@@ -149,6 +149,9 @@ cudaError_t launch_decode_split_tc(const DecodeParams& p, const CUtensorMap& k_m
                                    const CUtensorMap& q_map, cudaStream_t stream);
 cudaError_t launch_decode_split_tc_fp8(const DecodeParams& p, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                        const CUtensorMap& q_map, cudaStream_t stream);
+// Block gather over an E4M3 cache: an instantiation of its own, so the dense kernel's code stays as it is.
+cudaError_t launch_decode_split_tc_fp8_blocks(const DecodeParams& p, const CUtensorMap& k_map,
+                                              const CUtensorMap& v_map, const CUtensorMap& q_map, cudaStream_t stream);
 size_t decode_split_tc_smem_bytes(int B);
 size_t decode_split_tc_fp8_smem_bytes(int B);
 // Two query tokens per sequence (multi-token decode), bf16 cache.

@@ -68,6 +68,10 @@ WORKLOADS = {
                           "B=32, L=32768, 512 selected 8-token blocks plus the last block per sequence "
                           "(4104 tokens attended, block-gather decode), pages randomly permuted",
                           select_blocks=512),
+    "blocks32k_fp8": Workload("blocks32k_fp8", 32, ("fixed", 32768), "fp8", True, 0, 78,
+                              "B=32, L=32768, E4M3 cache with per-token fp32 scales, 512 selected 8-token blocks plus "
+                              "the last block per sequence (block-gather decode), pages randomly permuted",
+                              select_blocks=512),
     "long": Workload("long", 8, ("uniform", 65536, 131072), "bf16", True, 0, 55,
                      "B=8, L uniform in [65536, 131072], pages randomly permuted"),
 }

@@ -306,6 +306,21 @@ mfa_status_t mfa_decode_attention_blocks(const void* q, const void* k_cache, con
                                          int batch, int max_pages, int num_pages, int max_len_hint,
                                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Block gather over an FP8-E4M3 paged cache with per-token fp32 scales: the
+ * attention of mfa_decode_attention_blocks over the dequantised cache of
+ * mfa_decode_attention_fp8 (k_scale, v_scale [num_pages][64], [device],
+ * 16-byte aligned). Each selected block moves as its 8 rows of codes and their
+ * 8 K and 8 V scales; Q and P enter the 8-bit products as in
+ * mfa_decode_attention_fp8. Arguments, errors and the workspace as
+ * mfa_decode_attention_blocks. */
+mfa_status_t mfa_decode_attention_blocks_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                             const float* k_scale, const float* v_scale,
+                                             const int32_t* page_table, const int32_t* seq_lens,
+                                             const int32_t* block_idx, const int32_t* n_blocks, int max_blocks,
+                                             void* out, float* lse, float scale,
+                                             int batch, int max_pages, int num_pages, int max_len_hint,
+                                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Allocation-free variant of mfa_decode_attention (bf16 cache). The paper
  * has no counterpart: it exists for callers that cannot give the library a
  * workspace -- a plugin or foreign-function host that passes only tensors it
