@@ -1572,7 +1572,7 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
 }
 
 template <bool kFp8, bool kMtp, bool kGather8 = false>
-__global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads)
     decode_split_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap) {
   using C = Cfg<kFp8, kMtp>;
