@@ -72,6 +72,10 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
   __shared__ float4 s_acc[Sh::kSubsets > 1 ? kCombineThreads * Sh::kVec : 1];
   __shared__ __align__(8) uint64_t s_bar;
   const uint32_t o_base = smem_u32(smem_raw), bar = smem_u32(&s_bar);
+  // whatever follows on the stream may be scheduled once every CTA of this grid is resident (its grid
+  // dependency wait still covers this grid's results): it then starts as these CTAs leave their SMs,
+  // without a launch gap after the last one
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();

@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // x and the weights may come from the previous kernel: wait for it, then let the up launch start
     pdl_wait_prior_grid();
     pdl_launch_dependents();
+  } else {
+    // whatever follows may be scheduled once every CTA of this grid is resident; its own grid dependency
+    // wait still covers this grid's results
+    pdl_launch_dependents();
   }
 
   if (warp == 4) {
