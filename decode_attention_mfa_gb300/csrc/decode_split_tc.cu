@@ -1116,14 +1116,17 @@ __device__ void mma_role(const DecodeParams& p, const Ctx& cx, const int* s_cost
         pend_piece = seg_i;
       }
     } else {
-      alive = do_s(qb);
-      if (alive && T == 1) tc_commit(cx.bar(Bb::QEmpty + qb));
-      for (int t = 1; alive && t < T; ++t) {
-        alive = do_s(qb);
-        if (alive && t == T - 1) tc_commit(cx.bar(Bb::QEmpty + qb));
-        if (alive) alive = do_pv(s, t - 1, seg_i);
+      // S^T(t) goes out before P.V(t - kLag): with kLag = 2 the K stage of tile t is released a tile
+      // earlier than in strict alternation (S(t) waits only for the softmax to have read S(t - 2), which
+      // it does before it forms P(t - 2)), so the next K tiles are requested sooner
+      constexpr int kLag = 2;
+      for (int t = 0; alive && t < T + kLag; ++t) {
+        if (t < T) {
+          alive = do_s(qb);
+          if (alive && t == T - 1) tc_commit(cx.bar(Bb::QEmpty + qb));
+        }
+        if (alive && t >= kLag) alive = do_pv(s, t - kLag, seg_i);
       }
-      if (alive) alive = do_pv(s, T - 1, seg_i);
     }
     ++seg_i;
   }
