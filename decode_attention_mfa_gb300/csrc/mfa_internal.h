@@ -39,7 +39,7 @@ constexpr int kPieceCostPagesTwoTokens = 3;
 // E4M3: a piece also splits Q into E4M3 terms and finds the largest V scale,
 // and a tile (two pages) streams in about half the time of a bf16 tile, so a
 // piece is worth more pages.
-constexpr int kPieceCostPagesFp8 = 2;
+constexpr int kPieceCostPagesFp8 = 3;
 
 // Cache formats: bf16 rows, E4M3 codes + per-token scale, packed E2M1 codes + per-token scale.
 constexpr int kKvBf16 = 0, kKvE4M3 = 1, kKvE2M1 = 2;
