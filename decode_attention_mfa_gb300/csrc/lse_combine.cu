@@ -51,11 +51,14 @@ struct CombineShape {
   static_assert(kH <= 8, "weights are computed by warps 0 .. kH-1");
 };
 
-// Partial-O rows staged in shared memory per round: the rows of kChunkBytes / (kH KB) partials, brought
+// Partial-O rows staged in shared memory per round: the rows of chunk_bytes / (kH KB) partials, brought
 // by TMA bulk copies issued right after the grid dependency wait, while warps 0 .. kH-1 read the LSEs.
 // One round covers every partial of the configurations' sequences (4K context: about 6 partials of 4
 // heads; 128K context: about 20 of one head), so the merge waits on L2 once.
-constexpr int kChunkBytes = 32 * 1024;
+// Eight heads a CTA take 8 KB a partial: 48 KB keep a sequence of six pieces in one round; four CTAs of
+// that size still share an SM.
+template <int kH>
+__host__ __device__ constexpr int chunk_bytes() { return kH == 8 ? 48 * 1024 : 32 * 1024; }
 
 // At most 64 registers a thread and about 36 KB of shared memory, so four CTAs share an SM (608 on 152
 // SMs), which holds the whole grid of batches up to 64 sequences in one wave.
@@ -63,6 +66,7 @@ template <int kH>
 __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeParams p) {
   using Sh = CombineShape<kH>;
   constexpr int kPartBytes = kH * 1024;            // the kH heads' rows of one partial
+  constexpr int kChunkBytes = chunk_bytes<kH>();
   constexpr int kChunk = kChunkBytes / kPartBytes;  // partials per round
   extern __shared__ __align__(128) uint8_t smem_raw[];
   int* s_len = reinterpret_cast<int*>(smem_raw + kChunkBytes);
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(kCombineThreads, 4) lse_combine_kernel(DecodeP
 template <int kH>
 cudaError_t launch_kh(const DecodeParams& p, cudaStream_t stream) {
   dim3 grid(kHeads / kH, p.B * p.n_query);
-  const size_t smem = kChunkBytes + sizeof(int) * (2 * (size_t)p.B + 1) + sizeof(float) * (size_t)kH * p.grid;
+  const size_t smem = chunk_bytes<kH>() + sizeof(int) * (2 * (size_t)p.B + 1) + sizeof(float) * (size_t)kH * p.grid;
   static int configured[kTrackedDevices] = {};
   const cudaError_t e = ensure_dynamic_smem(lse_combine_kernel<kH>, smem, configured);
   if (e != cudaSuccess) return e;
@@ -223,12 +227,13 @@ cudaError_t launch_kh(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// Heads per CTA: the grid (64 / kH) x B should be about 2-4 CTAs per SM, so
-// fewer heads per CTA (and partial subsets) for small batches.
+// Heads per CTA: the grid (64 / kH) x rows, rows = B x query tokens, should be about 2-4 CTAs per SM, so
+// fewer heads per CTA (and partial subsets) for few rows, and one wave up to 64 rows.
 cudaError_t launch_lse_combine(const DecodeParams& p, cudaStream_t stream) {
-  if (p.B <= 8) return launch_kh<1>(p, stream);
-  if (p.B <= 16) return launch_kh<2>(p, stream);
-  if (p.B <= 48) return launch_kh<4>(p, stream);
+  const long long rows = (long long)p.B * p.n_query;
+  if (rows <= 8) return launch_kh<1>(p, stream);
+  if (rows <= 16) return launch_kh<2>(p, stream);
+  if (rows <= 48) return launch_kh<4>(p, stream);
   return launch_kh<8>(p, stream);
 }
 
