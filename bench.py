@@ -216,6 +216,18 @@ def ncu_traffic(workload: str, tokens_per_launch: float):
     return float(entry["dram_bytes_per_token"]) * tokens_per_launch
 
 
+def ncu_step_share(workload: str):
+    """The split kernel's share of a step's device time in the committed ncu launch list of this workload
+    (cold, serialised launches), if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    entry = json.load(open(path)).get("step_share", {}).get(workload)
+    if not entry or entry.get("source_sha") != kernel_source_sha():
+        return None
+    return float(entry["split_share"])
+
+
 def query_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_mfa_gb300", "csrc")
@@ -514,6 +526,15 @@ def run_ours(args, rank, world, local, workload=None, region_s=None, with_e2e=No
     avg_split_s = float(np.mean(split_ms)) / 1e3 if split_ms else float("nan")
     achieved = float(np.mean(split_bytes_last)) / avg_split_s / 1e9 if split_ms else None
     tokens_per_launch = float(np.mean([float(np.sum(L)) for L in last_lens]))
+    share = ncu_step_share(w.name)
+    in_step = None
+    if share is not None and split_ms:
+        us = share * max_s * 1e6 / args.steps
+        ach = float(np.mean(split_bytes_last)) / (us * 1e-6) / 1e9
+        in_step = {"share_of_step": share, "us": us, "achieved": ach, "frac": ach / peak_gbs,
+                   "how": "the split kernel's share of the step's device time in the committed ncu launch list "
+                          "(profiles/), times this run's step time: the kernel as it runs inside the step, "
+                          "overlapped with its neighbours"}
 
     e2e = None
     if e2e_on:
@@ -564,7 +585,8 @@ def run_ours(args, rank, world, local, workload=None, region_s=None, with_e2e=No
                      "how": "CUDA events around each split launch on its stream, in a timed region of "
                             "the same steps run right after the headline region; the events keep the split "
                             "kernel from overlapping its neighbours (programmatic dependent launch), so this is "
-                            "the kernel's stand-alone duration, which can exceed the overlapped step time"},
+                            "the kernel's stand-alone duration, which can exceed the overlapped step time",
+                     "in_step": in_step},
         "e2e": e2e,
     }
     return result, lens0
