@@ -52,8 +52,8 @@ COPY_MEM_BUDGET = 100e9
 DRIFT = 0.03              # with an append, each cache copy grows by at most about this fraction of its length
 MAX_HEADLINE_STEPS = 20000
 MIN_GRAPH_STEPS = 32      # steps per captured graph (graph launches amortised over at least this many)
-E2E_GROUP = 8             # end to end: steps per stream synchronisation (two sets of per-step buffers)
-E2E_GRAPH_STEPS = 256     # end to end: steps per captured graph (its first group's inputs are copied in at its start)
+E2E_GROUP = 16            # end to end: steps per stream synchronisation (two sets of per-step buffers)
+E2E_GRAPH_STEPS = 512     # end to end: steps per captured graph (its first group's inputs are copied in at its start)
 EXTRA_WORKLOADS = ("long", "fp8", "ragged")
 
 
