@@ -330,6 +330,16 @@ struct PageIds {
   }
 };
 
+// ---------------------------------------------------------------- LSU async copies
+// 16 bytes from global to shared memory through the LSU (both addresses 16-byte aligned), and an arrival on
+// an mbarrier once every such copy this thread issued has landed (the barrier's count includes it).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Block gather: cache rows of the virtual blocks of one sequence piece (the
 // selected blocks in the caller's order, then the block of the last token).
 // Lane j < 16 looks up block j of each 16-block tile in three steps -- the
@@ -533,21 +543,25 @@ __device__ void producer_role(const DecodeParams& p, const CUtensorMap* kmap, co
     ++cc;
     return true;
   };
+  // the 8 K and 8 V scales of each of the tile's 16 blocks by LSU copies (cp.async, 16 bytes each), not by
+  // the TMA unit: these 32-byte rows are half of this mode's copies a tile, and the TMA unit takes about as
+  // long per copy whatever its size. Lane i < 16 brings block i's K scales, lane 16 + i its V scales; every
+  // lane's arrival (on completion of its copies) counts on the scale barrier (32 arrivals in this mode).
   auto stage_block_scales = [&](int row) -> bool {
     constexpr uint32_t kRingSc = C::kScaleSlots > 0 ? C::kScaleSlots : 1;
     const uint32_t slot = sc_cnt % kRingSc, n = sc_cnt / kRingSc;
     const bool r = cx.wait(Bb::ScEmpty + slot, (n & 1) ^ 1);
     __syncwarp();
     if (!r) return false;
-    const bool mine = lane < 16 && row >= 0;
-    const uint32_t nb = __popc(__ballot_sync(0xffffffffu, mine));
-    const uint32_t dst = cx.base + L.scales + slot * kScaleBytes, bar = cx.bar(Bb::ScFull + slot);
-    if (lane == 0) mbar_arrive_expect_tx(bar, nb * 64u);
-    __syncwarp();
-    if (mine) {
-      bulk_load(dst + lane * 32, p.k_scale + row, 32u, bar);
-      bulk_load(dst + 512 + lane * 32, p.v_scale + row, 32u, bar);
+    const int blk = lane & 15;
+    const int brow = __shfl_sync(0xffffffffu, row, blk);  // block blk's cache row (-1: no block)
+    const uint32_t dst = cx.base + L.scales + slot * kScaleBytes + (lane < 16 ? 0u : 512u) + (uint32_t)blk * 32u;
+    if (brow >= 0) {
+      const float* src = (lane < 16 ? p.k_scale : p.v_scale) + brow;
+      cp_async_16(dst, src);
+      cp_async_16(dst + 16, src + 4);
     }
+    cp_async_mbar_arrive_noinc(cx.bar(Bb::ScFull + slot));
     ++sc_cnt;
     return true;
   };
@@ -1618,7 +1632,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kMtp>::kThreads)
       mbar_init(bars + 8 * (Bb::VRefEmpty + i), C::kSoftmaxThreads);
     }
     for (int i = 0; i < C::kScaleSlots; ++i) {
-      mbar_init(bars + 8 * (Bb::ScFull + i), 1);
+      mbar_init(bars + 8 * (Bb::ScFull + i), kGather8 ? 32 : 1);  // block gather: one arrival per producer lane
       mbar_init(bars + 8 * (Bb::ScEmpty + i), C::kSoftmaxThreads);
     }
     *abort_flag = 0;
