@@ -1249,7 +1249,7 @@ __device__ __forceinline__ float load_logits(uint32_t taddr, bool full, bool val
 // warp. Returns 2^-e. Ends with every thread's terms written and fenced for
 // the tensor cores (the caller then arrives on the ready barrier).
 template <int kThreadsAll>
-__device__ __forceinline__ float split_q_e4m3(uint32_t q_addr, float* scratch, int tid) {
+__device__ __noinline__ float split_q_e4m3(uint32_t q_addr, float* scratch, int tid) {
   constexpr int kParts = kThreadsAll / 64, kDims = kHeadDim / kParts, kIn = kDims / 8;
   static_assert(kDims % 16 == 0, "16-dim output chunks");
   const int h = tid & 63, part = tid >> 6, d0 = part * kDims;
@@ -1339,6 +1339,11 @@ __device__ __forceinline__ void scale_o_columns(uint32_t taddr_o, int h0, const 
     }
   }
   tc_wait_st();
+}
+// The E4M3 softmax calls the rescale out of line: inlined into its loop it cost that loop spilled registers.
+template <int kHpt, int kHalfCols>
+__device__ __noinline__ void scale_o_columns_e4m3(uint32_t taddr_o, int h0, const float* col_scale) {
+  scale_o_columns<true, kHpt, kHalfCols>(taddr_o, h0, col_scale);
 }
 
 template <bool kFp8>
@@ -1506,7 +1511,10 @@ __device__ void softmax_role(const DecodeParams& p, const Ctx& cx, const int* s_
           // O^T holds the previous tiles: wait for their last P.V, then scale the group's columns
           if (!wait_pv(p_cnt - 1)) return;
           tc_fence_after();
-          scale_o_columns<kFp8, kHpt, C::kOHalfCols>(taddr_o, h0, alpha + h0);
+          if constexpr (kFp8)
+            scale_o_columns_e4m3<kHpt, C::kOHalfCols>(taddr_o, h0, alpha + h0);
+          else
+            scale_o_columns<kFp8, kHpt, C::kOHalfCols>(taddr_o, h0, alpha + h0);
         }
         (void)load_logits<kFp8, kHpt>(taddr_s, full, valid, kmul, mref + h0, x);
       }
