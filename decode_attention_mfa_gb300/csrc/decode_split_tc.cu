@@ -60,7 +60,7 @@ struct Cfg;
 template <>
 struct Cfg<false, false> {
   static constexpr int kThreads = 320;   // two softmax warpgroups, producer, MMA
-  static constexpr int kSlots = 7;       // 16 KB operand chunks
+  static constexpr int kSlots = 8;       // 16 KB operand chunks
   static constexpr int kKStages = 0;     // raw code pages: K ring
   static constexpr int kVStages = 0;     // raw code pages: V ring
   static constexpr int kStages = 0;
@@ -74,7 +74,7 @@ struct Cfg<false, false> {
   static constexpr int kSoftmaxThreads = 128 * kGroups;
   static constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = kProducerWarp + 1;
   static constexpr int kQ = 1;           // query tokens per sequence
-  static constexpr int kPBufs = 2;       // P buffers
+  static constexpr int kPBufs = 1;       // P buffers (one: its 16 KB buy the eighth ring slot)
   static constexpr int kCols = 64;       // softmax columns: [token][head]
   static constexpr int kHpt = 32;        // columns per softmax thread
   static constexpr int kOHalfCols = 64;  // O^T columns per 128-dim half
